@@ -1,0 +1,213 @@
+"""Plain-Python restatement of the load-balancing plan -- test infrastructure only.
+
+Follows page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎",
+核心机制 6 "负载均衡调度" (paper §3.3.1, Algorithm 1, Figure 6) and
+核心机制 7 (paper Appendix D.1-D.3), in that order:
+
+  * tile cost cost(l_q, l_kv) = alpha * l_q + beta * l_kv;
+  * the largest KV chunk L_kv = sum_i ceil(l_qo,i / T_q) * l_kv,i / #CTA;
+  * work sorted longest-first, then handed out through a priority queue of CTAs;
+  * no atomic aggregation: partial outputs of a split request go to fixed
+    workspace slots and a reduction map fixes the order they are merged in;
+  * only "long" work is split; everything else writes the final output directly;
+  * partial outputs are bounded by 2 * #CTA tiles.
+
+Readings (the algorithm listing itself is not on the page; these are listed in
+the design notes):
+  * Path / tile (核心机制 4, paper §3.2.2): rows of a tile are (query token, query
+    head in group) pairs.  If every request has l_q * g <= 8 rows, the whole
+    batch takes the CUDA-core decode path with one tile per (request, KV head)
+    covering all its query tokens, and rows_tile is the smallest of 1, 2, 4, 8
+    that fits; otherwise the tensor-core path with 128-row tiles,
+    tile_tokens = 128 // g.
+  * KV heads count as separate units in the L_kv sum; L_kv is raised to l_min
+    (default 256) and rounded up to a whole number of pages.
+  * A unit (request, KV head, query tile) sees e keys: l_kv, or under the causal
+    mask the keys visible to the tile's last token.  It is cut into
+    n = ceil(e / L_kv) chunks, evened out: chunk size cs = ceil(ceil(e / n) / page)
+    pages, and the chunks are [c*cs, min(e, (c+1)*cs)).  A unit with e = 0 is one
+    empty chunk (it writes the empty state).
+  * cost of an item = alpha * rows + beta * chunk length, rows = tokens in tile * g;
+    defaults alpha = beta = 1.
+  * Sort: cost descending, ties by enumeration order (request, KV head, tile,
+    chunk ascending).  Priority queue: smallest accumulated cost first, ties to
+    the lowest CTA id.
+  * Slots are numbered in enumeration order of the split units, chunk by chunk.
+
+The serialised form (`serialize`) is what the library's host-only plan entry
+point must reproduce bit for bit.
+"""
+from __future__ import annotations
+
+import heapq
+from dataclasses import dataclass
+
+import numpy as np
+
+PATH_DECODE = 0
+PATH_TENSOR = 1
+TC_ROWS = 128
+DECODE_MAX_ROWS = 8
+NOT_CAUSAL_DIAG = 1 << 30
+PLAN_MAGIC = 0x46495031
+HEADER_LEN = 16
+ITEM_FIELDS = 8
+UNIT_FIELDS = 8
+
+
+def _ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+@dataclass
+class Plan:
+    path: int
+    tile_tokens: int
+    rows_tile: int
+    group: int
+    num_ctas: int
+    l_kv_chunk: int
+    page_size: int
+    causal: bool
+    num_qo_heads: int
+    num_kv_heads: int
+    head_dim: int
+    batch: int
+    items: list            # enumeration order; each a dict
+    order: list            # item indices in assignment (sorted) order
+    cta_of: list           # CTA of each item (by enumeration index)
+    queues: list           # per CTA: item indices in queue order
+    units: list            # split units: dict(first_slot, n_chunks, q_start, q_len, kv_head)
+    slot_unit: list
+    loads: list            # accumulated cost per CTA
+
+
+def choose_path(l_q, group: int):
+    """Tile choice (核心机制 4, paper §3.2.2): CUDA cores for tiny row counts, tensor cores otherwise."""
+    max_rows = int(max((int(x) for x in l_q), default=0)) * group
+    if max_rows <= DECODE_MAX_ROWS:
+        tile_tokens = max(1, int(max((int(x) for x in l_q), default=1)))
+        rows = 1
+        while rows < tile_tokens * group:
+            rows *= 2
+        return PATH_DECODE, tile_tokens, rows
+    if group > TC_ROWS:
+        raise ValueError("group size above 128 rows")
+    return PATH_TENSOR, TC_ROWS // group, TC_ROWS
+
+
+def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, page_size: int,
+         causal: bool, num_ctas: int, head_dim: int = 128, alpha: int = 1, beta: int = 1,
+         l_min: int = 256) -> Plan:
+    qo = [int(x) for x in qo_indptr]
+    kv = [int(x) for x in kv_indptr]
+    last = [int(x) for x in last_page_len]
+    batch = len(qo) - 1
+    g = num_qo_heads // num_kv_heads
+
+    # a1: lengths
+    l_q = [qo[i + 1] - qo[i] for i in range(batch)]
+    l_kv = []
+    for i in range(batch):
+        n_p = kv[i + 1] - kv[i]
+        l_kv.append((n_p - 1) * page_size + last[i] if n_p > 0 else 0)
+
+    # a2: path and tile
+    path, tile_tokens, rows_tile = choose_path(l_q, g)
+
+    # a3: KV chunk bound
+    total = 0
+    for i in range(batch):
+        total += num_kv_heads * _ceil_div(l_q[i], tile_tokens) * l_kv[i]
+    l_chunk = max(_ceil_div(total, num_ctas), l_min)
+    l_chunk = _ceil_div(l_chunk, page_size) * page_size
+
+    # a4: units -> chunks (items); a6: slots of split units
+    items, units, slot_unit = [], [], []
+    for i in range(batch):
+        n_tiles = _ceil_div(l_q[i], tile_tokens)
+        for h in range(num_kv_heads):
+            for j in range(n_tiles):
+                q0 = j * tile_tokens
+                qn = min(tile_tokens, l_q[i] - q0)
+                if causal:
+                    e = min(max(l_kv[i] - l_q[i] + q0 + qn, 0), l_kv[i])
+                    diag = l_kv[i] - l_q[i] + q0
+                else:
+                    e = l_kv[i]
+                    diag = NOT_CAUSAL_DIAG
+                if e == 0:
+                    n, cs = 1, 0
+                else:
+                    n = _ceil_div(e, l_chunk)
+                    cs = _ceil_div(_ceil_div(e, n), page_size) * page_size
+                    n = _ceil_div(e, cs)
+                unit = -1
+                if n > 1:
+                    unit = len(units)
+                    units.append(dict(first_slot=len(slot_unit), n_chunks=n, q_start=qo[i] + q0, q_len=qn,
+                                      kv_head=h))
+                    slot_unit.extend([unit] * n)
+                for c in range(n):
+                    lo, hi = c * cs, min(e, (c + 1) * cs)
+                    items.append(dict(
+                        request=i, kv_head=h, tile=j, chunk=c,
+                        page_base=kv[i], q_start=qo[i] + q0, q_len=qn, kv_lo=lo, kv_hi=hi, diag=diag,
+                        slot=(units[unit]["first_slot"] + c) if unit >= 0 else -1,
+                        cost=alpha * qn * g + beta * (hi - lo),
+                    ))
+
+    # a5: longest first, then a min-priority queue of CTAs keyed (load, cta id)
+    order = sorted(range(len(items)), key=lambda k: (-items[k]["cost"], k))
+    heap = [(0, c) for c in range(num_ctas)]
+    heapq.heapify(heap)
+    cta_of = [0] * len(items)
+    queues = [[] for _ in range(num_ctas)]
+    for k in order:
+        load, c = heapq.heappop(heap)
+        cta_of[k] = c
+        queues[c].append(k)
+        heapq.heappush(heap, (load + items[k]["cost"], c))
+    loads = [0] * num_ctas
+    for load, c in heap:
+        loads[c] = load
+
+    return Plan(path, tile_tokens, rows_tile, g, num_ctas, l_chunk, page_size, bool(causal), num_qo_heads,
+                num_kv_heads, head_dim, batch, items, order, cta_of, queues, units, slot_unit, loads)
+
+
+def serialize(p: Plan) -> np.ndarray:
+    """Flat int32 form: header[16] | cta_indptr | items (queue order) | units | slot_unit."""
+    header = [PLAN_MAGIC, p.path, p.tile_tokens, p.rows_tile, p.group, p.num_ctas, len(p.items), len(p.units),
+              len(p.slot_unit), p.l_kv_chunk, p.page_size, int(p.causal), p.num_qo_heads, p.num_kv_heads,
+              p.head_dim, p.batch]
+    indptr = [0]
+    for q in p.queues:
+        indptr.append(indptr[-1] + len(q))
+    flat_items = []
+    for q in p.queues:
+        for k in q:
+            it = p.items[k]
+            flat_items += [it["page_base"], it["q_start"], it["q_len"], it["kv_head"], it["kv_lo"], it["kv_hi"],
+                           it["diag"], it["slot"]]
+    flat_units = []
+    for u in p.units:
+        flat_units += [u["first_slot"], u["n_chunks"], u["q_start"], u["q_len"], u["kv_head"], 0, 0, 0]
+    return np.array(header + indptr + flat_items + flat_units + list(p.slot_unit), dtype=np.int64).astype(np.int32)
+
+
+def deserialize(buf) -> dict:
+    """Split a flat plan back into named int32 arrays (used to compare plans field by field)."""
+    buf = np.asarray(buf, dtype=np.int32)
+    h = buf[:HEADER_LEN]
+    n_cta, n_items, n_units, n_slots = int(h[5]), int(h[6]), int(h[7]), int(h[8])
+    o = HEADER_LEN
+    indptr = buf[o:o + n_cta + 1]
+    o += n_cta + 1
+    items = buf[o:o + n_items * ITEM_FIELDS].reshape(n_items, ITEM_FIELDS)
+    o += n_items * ITEM_FIELDS
+    units = buf[o:o + n_units * UNIT_FIELDS].reshape(n_units, UNIT_FIELDS)
+    o += n_units * UNIT_FIELDS
+    slot_unit = buf[o:o + n_slots]
+    o += n_slots
+    return dict(header=h, cta_indptr=indptr, items=items, units=units, slot_unit=slot_unit, length=o)
