@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark of the paged serving-attention hot path on GB300.
+
+A step is one pass of the whole path over one batch: the host plan (lengths,
+tile, chunking, longest-first CTA queues, reduction map) and one persistent
+kernel launch (page gather, attention, in-kernel merge of split rows).
+
+  value  -- decode KV GB/s of the Llama-3-8B-shaped batch (128 requests, 32/8
+            heads, page 16, KV ~ U[1,4096]) with inputs resident in HBM: KV
+            bytes per step / device time per step (CUDA events around K launches
+            on the launching stream; the plan is built once, as it is reused
+            across layers).
+  e2e    -- same metric through the C ABI from host buffers: every step plans
+            from host index arrays (pinned copy inside), copies q host->device
+            from pinned memory, runs, and reads o and lse back.
+  configs -- the other workloads (tiny, skewed long-context, causal prefill,
+            shared prefix) timed the same way, each with its own unit.
+
+`--impl reference` times the float64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this build).  Multi-GPU runs are independent
+replicas (no collective on the data path): value sums over ranks, time is the
+max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s (% of GB300 HBM peak); prefill TFLOPS (% bf16 peak); µs/batch"
+PRIMARY = "llama3_8b_decode"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ----------------------------------------------------------------------------------------------
+# workload accounting
+# ----------------------------------------------------------------------------------------------
+
+def lengths(b):
+    qo = b.qo_indptr.astype(np.int64)
+    kv = b.kv_indptr.astype(np.int64)
+    n_p = np.diff(kv)
+    l_kv = np.where(n_p > 0, (n_p - 1) * b.page_size + b.last_page_len, 0)
+    return np.diff(qo), l_kv
+
+
+def kv_bytes(b):
+    _, l_kv = lengths(b)
+    return int(l_kv.sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+
+
+def algorithmic_bytes(b):
+    """KV read + q read + o/lse written + page indices read (bytes one launch must move)."""
+    rows = b.total_q * b.num_qo_heads
+    return kv_bytes(b) + rows * b.head_dim * 2 * 2 + rows * 4 + int(b.kv_indptr[-1]) * 4
+
+
+def visible_pairs(b):
+    l_q, l_kv = lengths(b)
+    tot = 0
+    for lq, lk in zip(l_q.tolist(), l_kv.tolist()):
+        if b.causal:
+            t = np.arange(lq)
+            tot += int(np.clip(lk - lq + t + 1, 0, lk).sum())
+        else:
+            tot += lq * lk
+    return tot
+
+
+def flops(b):
+    return 4 * b.head_dim * visible_pairs(b) * b.num_qo_heads
+
+
+# ----------------------------------------------------------------------------------------------
+# device helpers
+# ----------------------------------------------------------------------------------------------
+
+def to_dev(a, torch, dev):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+class Case:
+    """One batch resident on the device with its workspace and plan."""
+
+    def __init__(self, b, torch, dev, num_ctas=0):
+        from serving_attention_plan_gb300 import binding as B
+        self.b = b
+        self.torch = torch
+        self.q, self.k, self.v = to_dev(b.q, torch, dev), to_dev(b.k_pages, torch, dev), to_dev(b.v_pages, torch, dev)
+        self.o = torch.empty((b.total_q, b.num_qo_heads, b.head_dim), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((b.total_q, b.num_qo_heads), dtype=torch.float32, device=dev)
+        self.ws = B.Workspace(b.batch_size, b.total_q, int(b.kv_indptr[-1]), b.num_qo_heads, b.num_kv_heads,
+                              b.head_dim, num_ctas)
+        self.plan()
+
+    def plan(self):
+        b = self.b
+        self.ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.page_size, b.causal)
+
+    def run(self):
+        self.ws.run(self.q, self.k, self.v, self.o, self.lse)
+
+
+def time_launches(torch, fn, steps, warmup, barrier=None):
+    """Device time of `steps` back-to-back calls (CUDA events on the current stream), after warm-up."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per step
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.idx)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r[0] for r in rows if r[2] > 200.0] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    h = hashlib.sha256()
+    for f in d.get("sources", []):
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return d.get("dram_bytes_per_launch") if h.hexdigest() == d.get("sources_sha256") else None
+
+
+# ----------------------------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------------------------
+
+def cpu_oracle_sample(b, budget_s=15.0):
+    """Time the float64 oracle over whole requests of `b` until ~budget_s; returns (GB/s, sample text, s)."""
+    from oracle import attention as A
+    order = list(range(b.batch_size))
+    t0 = time.perf_counter()
+    done = []
+    for i in order:
+        A.batch_attention(b, requests=[i])
+        done.append(i)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    _, l_kv = lengths(b)
+    nbytes = int(l_kv[done].sum()) * b.num_kv_heads * b.head_dim * 4
+    return nbytes / dt / 1e9, f"{len(done)} of {b.batch_size} requests ({int(l_kv[done].sum())} KV tokens)", dt
+
+
+def reference_arm(args):
+    from serving_attention_plan_gb300 import workloads as W
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    b = W.by_name(args.config)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(b, budget_s=2.0)
+    vals = []
+    samples = ""
+    for _ in range(args.steps):
+        v, samples, _ = cpu_oracle_sample(b, budget_s=max(2.0, 60.0 / max(args.steps, 1)))
+        vals.append(v)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.config},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": samples + " per step, float64 NumPy oracle"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def workload_config(name, b):
+    l_q, l_kv = lengths(b)
+    return {
+        "workload": name, "batch": b.batch_size, "num_qo_heads": b.num_qo_heads, "num_kv_heads": b.num_kv_heads,
+        "head_dim": b.head_dim, "page_size": b.page_size, "causal": bool(b.causal),
+        "kv_tokens": int(l_kv.sum()), "q_tokens": int(l_q.sum()),
+        "l2": "inputs larger than L2" if kv_bytes(b) > L2_BYTES else "inputs fit in L2 (no flush)",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--config", default=PRIMARY)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        barrier = dist.barrier
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from serving_attention_plan_gb300 import workloads as W
+
+    hbm_peak, bf16_peak, bf16_sus, peak_src = measured_peaks()
+    b = W.by_name(args.config)
+    case = Case(b, torch, dev)
+    nbytes = kv_bytes(b)
+    abytes = algorithmic_bytes(b)
+
+    with ClockSampler(local) as clk:
+        ms = time_launches(torch, case.run, args.steps, args.warmup, barrier)
+    clocks = clk.summary()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    achieved = abytes / (ms * 1e-3) / 1e9
+
+    # end to end through the C ABI from host buffers
+    q_host = torch.from_numpy(np.ascontiguousarray(b.q).view(np.int16)).pin_memory()
+    o_host = torch.empty((b.total_q, b.num_qo_heads, b.head_dim), dtype=torch.int16).pin_memory()
+    lse_host = torch.empty((b.total_q, b.num_qo_heads), dtype=torch.float32).pin_memory()
+    q_dev16 = case.q.view(torch.int16)
+    o_dev16 = case.o.view(torch.int16)
+
+    def e2e_step():
+        case.plan()
+        q_dev16.copy_(q_host, non_blocking=True)
+        case.run()
+        o_host.copy_(o_dev16, non_blocking=True)
+        lse_host.copy_(case.lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    e2e_steps = max(10, min(args.steps // 10, 200))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    hdr = case.ws.info()
+    plan_bytes = 4 * (16 + int(hdr[5]) + 1 + 8 * int(hdr[6]) + 8 * int(hdr[7]) + int(hdr[8]) + int(b.kv_indptr[-1]))
+    h2d = int(b.q.nbytes) + plan_bytes
+    d2h = int(o_host.numel() * 2 + lse_host.numel() * 4)
+
+    extra = {}
+    if not args.no_extra:
+        for name in ("tiny_decode", "skewed_long_decode", "ragged_causal_prefill", "shared_prefix_decode"):
+            try:
+                extra[name] = bench_other(name, torch, dev, hbm_peak, bf16_peak)
+            except Exception as e:  # report, never hide
+                extra[name] = {"error": f"{type(e).__name__}: {e}"}
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and world == 1:
+        v, sample, dt = cpu_oracle_sample(b, budget_s=15.0)
+        cpu = {"value": v, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": sample + f", {dt:.1f} s, float64 NumPy oracle (BLAS threads default)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "us_per_batch": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(args.config, b), parallelism=f"replicas x{world}"),
+        "frac_of_hbm_peak": value / world / hbm_peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+                     "traffic": ncu_traffic(f"decode_kernel/{args.config}"), "kernel": "decode_kernel<4,8,8>",
+                     "algorithmic_bytes_per_launch": abytes},
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "plan": {"path": int(hdr[1]), "rows_tile": int(hdr[3]), "num_ctas": int(hdr[5]), "items": int(hdr[6]),
+                 "split_rows": int(hdr[7]), "l_kv_chunk": int(hdr[9])},
+        "configs": extra,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
+    from serving_attention_plan_gb300 import binding as B
+    from serving_attention_plan_gb300 import workloads as W
+    w = W.by_name(name)
+    if name == "shared_prefix_decode":
+        pre, suf = Case(w.prefix, torch, dev), None
+        suf = Case.__new__(Case)
+        suf.b, suf.torch, suf.q, suf.k, suf.v = w.suffix, torch, pre.q, pre.k, pre.v
+        suf.o = torch.empty_like(pre.o)
+        suf.lse = torch.empty_like(pre.lse)
+        suf.ws = B.Workspace(w.suffix.batch_size, w.suffix.total_q, int(w.suffix.kv_indptr[-1]), 32, 8)
+        suf.plan()
+        o, lse = torch.empty_like(pre.o), torch.empty_like(pre.lse)
+
+        def step():
+            pre.run()
+            suf.run()
+            B.merge_states(pre.o, pre.lse, suf.o, suf.lse, o, lse)
+
+        ms = time_launches(torch, step, steps, warmup)
+        nbytes = kv_bytes(w.prefix) + kv_bytes(w.suffix)
+        return {"us_per_batch": ms * 1e3, "kv_gbs_unique": nbytes / (ms * 1e-3) / 1e9,
+                "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "launches_per_step": 3,
+                "prefix_plan": pre.ws.info().tolist()[:10], "suffix_plan": suf.ws.info().tolist()[:10]}
+    c = Case(w, torch, dev)
+    ms = time_launches(torch, c.run, steps, warmup)
+    hdr = c.ws.info()
+    out = {"us_per_batch": ms * 1e3, "path": "tensor-core" if hdr[1] == 1 else "cuda-core",
+           "config": workload_config(name, w)}
+    if hdr[1] == 1:
+        tf = flops(w) / (ms * 1e-3) / 1e12
+        out.update({"tflops": tf, "frac_of_bf16_peak": tf / bf16_peak})
+    else:
+        gbs = kv_bytes(w) / (ms * 1e-3) / 1e9
+        out.update({"kv_gbs": gbs, "frac_of_hbm_peak": gbs / hbm_peak})
+    return out
+
+
+if __name__ == "__main__":
+    main()

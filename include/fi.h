@@ -1,0 +1,217 @@
+/*
+ * fi.h -- C ABI of the GB300 (sm_103a) paged serving-attention library.
+ *
+ * The library computes attention over a block-sparse-row (BSR) paged KV-cache
+ * for batch decode and ragged causal prefill, under a deterministic
+ * load-balanced split-KV plan whose partial attention states (O, LSE) are
+ * merged in-kernel.  Source: page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎"
+ * (digest of the MLSys 2025 FlashInfer paper), sections cited per call below.
+ *
+ * Conventions for every call
+ *   - Plain C types only.  `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).
+ *   - Device pointers point to memory of the current CUDA device; host
+ *     pointers to ordinary or pinned host memory, as stated per argument.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (2 bytes each), row-major,
+ *     densely packed:
+ *        q, o       [total_q, num_qo_heads, head_dim]       (ragged rows, qo_indptr)
+ *        k_pages,
+ *        v_pages    [num_pages, num_kv_heads, page_size, head_dim]   ("HND")
+ *        lse        float32 [total_q, num_qo_heads], natural log, includes the
+ *                   softmax scale: lse = log sum_j exp(q.k_j / sqrt(head_dim)).
+ *     Query head h reads KV head h / (num_qo_heads / num_kv_heads).
+ *   - Every call returns an fi_status; 0 is success.  Nothing aborts,
+ *     throws or exits across this boundary.  On a host-side error no output
+ *     and no workspace state is changed.
+ *   - head_dim must be 128.
+ */
+#ifndef FI_H_
+#define FI_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fi_status {
+  FI_OK = 0,
+  FI_ERR_INVALID_ARG = 1, /* malformed indptr / lengths / pointers / sizes */
+  FI_ERR_CAPACITY = 2,    /* batch, tokens or pages exceed the workspace's capacity */
+  FI_ERR_UNSUPPORTED = 3, /* head_dim != 128, heads not divisible, page size the path can't tile */
+  FI_ERR_CUDA = 4,        /* a CUDA runtime call failed (the message is in fi_last_error_message) */
+  FI_ERR_DEVICE = 5,      /* a device-side check tripped (see fi_get_error) */
+  FI_ERR_NO_PLAN = 6      /* fi_run before a successful fi_plan on this workspace */
+} fi_status;
+
+/* Device-side error bits reported by fi_get_error. */
+#define FI_DEVERR_PAGE_OOB 0x1     /* a page index >= num_pages was skipped */
+#define FI_DEVERR_WAIT_TIMEOUT 0x2 /* a pipeline wait gave up after its iteration limit */
+#define FI_DEVERR_TMEM 0x4         /* tensor-memory allocation returned an unusable address */
+
+typedef struct fi_workspace fi_workspace;
+
+/*
+ * fi_workspace_create -- allocate the workspace once, at maximum capacity.
+ *
+ * Source: 核心机制 7 "CUDAGraph 兼容的静态化手段" (paper App. D.1, D.3): the
+ * workspace is sized for the largest batch up front and its segments keep
+ * fixed offsets, so a captured fi_run keeps valid pointers; the number of
+ * partial-output tiles is bounded by 2 * #CTA.
+ *
+ *   max_batch       most requests one plan may hold (>= 1)
+ *   max_total_q     most query tokens one plan may hold (>= 1)
+ *   max_kv_pages    most entries kv_indices may hold (>= 1)
+ *   num_qo_heads, num_kv_heads, head_dim   fixed for the workspace
+ *   num_ctas        persistent grid size; 0 selects the device's SM count
+ *                   (App. D.3 / App. E: #CTA = k * #SM, user-selectable)
+ *   out             receives the handle (owned by the caller; release with
+ *                   fi_workspace_destroy)
+ *
+ * Allocates one device buffer (plan segments, page-index copy, split
+ * counters, partial-output slots) and one pinned host buffer of the plan
+ * segments, on the current device.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int num_qo_heads, int num_kv_heads,
+                        int head_dim, int num_ctas, fi_workspace** out);
+
+/* Release a workspace (synchronises with its last plan copy first). NULL is a no-op. */
+int fi_workspace_destroy(fi_workspace* ws);
+
+/*
+ * fi_workspace_set_cost_model -- parameters of the scheduler's tile cost and chunk bound.
+ *
+ * Source: 核心机制 6 "负载均衡调度" (paper §3.3.1, Alg. 1): cost(l_q, l_kv) =
+ * alpha * l_q + beta * l_kv.  l_min is the smallest KV chunk the plan cuts
+ * (tokens).  Defaults: alpha = beta = 1, l_min = 256.  Takes effect at the
+ * next fi_plan.  Errors: INVALID_ARG (alpha < 0, beta < 1, l_min < 1).
+ */
+int fi_workspace_set_cost_model(fi_workspace* ws, int64_t alpha, int64_t beta, int32_t l_min);
+
+/*
+ * fi_plan -- inspector step: compute the work plan for one batch on the CPU.
+ *
+ * Source: 核心机制 6 (paper §3.3.1, Alg. 1, Fig. 6) and 核心机制 7 (App. D):
+ * per generation step the CPU derives lengths, picks the tile, bounds the KV
+ * chunk L_kv = sum ceil(l_qo/T_q) * l_kv / #CTA, cuts long work into chunks
+ * (short work writes the output directly), sorts work longest-first and
+ * hands it out through a CTA priority queue, and records the reduction map of
+ * split rows.  The plan is computed into pinned host memory and copied to the
+ * workspace with cudaMemcpyAsync on `stream`.  The plan depends only on the
+ * lengths, never on kv_indices values: identical lengths give a bit-identical
+ * plan.  It may be reused by any number of fi_run calls (e.g. every layer).
+ *
+ *   qo_indptr      HOST int32 [batch + 1], qo_indptr[0] = 0, non-decreasing
+ *   kv_indptr      HOST int32 [batch + 1], kv_indptr[0] = 0, non-decreasing;
+ *                  request i owns pages kv_indices[kv_indptr[i] .. kv_indptr[i+1])
+ *   kv_indices     HOST int32 [kv_indptr[batch]], page ids >= 0
+ *   last_page_len  HOST int32 [batch]; in [1, page_size] for requests with pages
+ *   causal         0 = full attention; 1 = query token t of request i sees keys
+ *                  j <= l_kv - l_q + t (mask aligned to the end of the KV)
+ *   stream         stream of the plan copy; fi_run on another stream must be
+ *                  ordered after it by the caller
+ *
+ * The index arrays are copied: the caller may free or reuse them on return.
+ * A new fi_plan replaces the previous plan of the workspace.  Not capturable
+ * in a CUDA graph (it waits for the previous plan's copy to finish before
+ * reusing the pinned buffer).
+ * Errors: INVALID_ARG, CAPACITY, UNSUPPORTED, CUDA.
+ */
+int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+            const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+            int page_size, int causal, void* stream);
+
+/*
+ * fi_run -- executor step: one persistent kernel (attention + merge of split rows).
+ *
+ * Source: 核心机制 6-7 (paper §3.3.1, App. D): attention and the contraction
+ * of partial outputs run in one persistent kernel of fixed grid; partial
+ * states of a split row go to workspace slots and are merged in the order
+ * the plan fixed (no atomic aggregation), so outputs are bit-identical from
+ * run to run.  Decode tiles (<= 8 rows) run on CUDA cores; larger tiles run on
+ * tcgen05 tensor cores (核心机制 4, paper §3.2.2).
+ *
+ *   q          DEVICE bf16 [total_q, num_qo_heads, 128]
+ *   k_pages    DEVICE bf16 [num_pages, num_kv_heads, page_size, 128]
+ *   v_pages    DEVICE bf16, same shape as k_pages
+ *   num_pages  rows of the page pool; every planned page id must be below it
+ *   o          DEVICE bf16 [total_q, num_qo_heads, 128]   (written)
+ *   lse        DEVICE float32 [total_q, num_qo_heads]     (written)
+ *
+ * Every row of o/lse that the plan covers is written; a row that sees no key
+ * gets o = 0, lse = -inf.  Asynchronous on `stream`; capturable in a CUDA
+ * graph, and a captured launch stays valid for later plans of the same
+ * workspace that keep the same path and tile (fi_plan_info header[1..3]).
+ * Calls that share a workspace must not overlap on the GPU.
+ * Errors: NO_PLAN, INVALID_ARG (null pointers, page id >= num_pages), CUDA.
+ */
+int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_pages, int num_pages, void* o,
+           float* lse, void* stream);
+
+/*
+ * fi_merge_states -- (O, LSE) of two disjoint KV sets merged into one.
+ *
+ * Source: 术语与记号 "Attention State 与 ⊕" (paper §2.2) and 核心机制 2
+ * "可组合格式" (paper §3.1.2, Fig. 3): states over disjoint key sets combine
+ * with an associative, commutative operator, so a shared-prefix sub-matrix
+ * and a per-request suffix sub-matrix can be computed separately and merged:
+ *   s = log(e^s_a + e^s_b),  O = e^(s_a - s) O_a + e^(s_b - s) O_b,
+ * with (0, -inf) as the identity.
+ *
+ *   o_a, o_b, o   DEVICE bf16 [rows, heads, head_dim]   (o may alias o_a or o_b)
+ *   lse_a, lse_b, lse   DEVICE float32 [rows, heads], natural log
+ * Asynchronous on `stream`.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+int fi_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
+                    int rows, int heads, int head_dim, void* stream);
+
+/*
+ * fi_get_error -- read and clear the workspace's device-side error word
+ * (FI_DEVERR_* bits).  Synchronises the device.  Errors: INVALID_ARG, CUDA.
+ */
+int fi_get_error(fi_workspace* ws, int32_t* err_bits);
+
+/*
+ * fi_plan_info -- copy the current plan's 16-int32 header to host memory:
+ *   [0] magic 0x46495031  [1] path (0 CUDA-core decode, 1 tensor core)
+ *   [2] tokens per tile   [3] rows per tile  [4] group size g  [5] #CTA
+ *   [6] work items  [7] split rows  [8] partial slots  [9] L_kv (tokens)
+ *   [10] page_size  [11] causal  [12] num_qo_heads  [13] num_kv_heads
+ *   [14] head_dim   [15] batch
+ * Errors: INVALID_ARG, NO_PLAN.
+ */
+int fi_plan_info(const fi_workspace* ws, int32_t* header16);
+
+/*
+ * fi_plan_compute -- the planner alone, on the host, with no device work.
+ *
+ * Same inputs and rules as fi_plan (kv_indices is not an input: plans never
+ * depend on it), plus the grid size and cost model.  Writes the plan as one
+ * flat int32 array:
+ *   header[16] | cta_indptr[num_ctas + 1] | items[n_items][8] (queue order)
+ *   | split rows[n_split][8] | slot_to_split_row[n_slots]
+ * item = {page_base, q_start, q_len, kv_head, kv_lo, kv_hi, diag, slot(-1 = direct)},
+ * split row = {first_slot, n_chunks, q_start, q_len, kv_head, 0, 0, 0}.
+ *   out       HOST int32 buffer of `capacity` elements (may be NULL to query)
+ *   out_len   receives the number of elements the plan needs
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (out too small; out_len is set).
+ */
+int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
+                    int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal, int num_ctas,
+                    int64_t alpha, int64_t beta, int32_t l_min, int32_t* out, int64_t capacity, int64_t* out_len);
+
+/* Number of SMs of the current device (the default #CTA). Errors: CUDA. */
+int fi_device_sm_count(int* out);
+
+/* Static text for a status code. */
+const char* fi_status_string(int status);
+
+/* Text of the last CUDA failure seen by this thread (empty if none). */
+const char* fi_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FI_H_ */

@@ -1,0 +1,483 @@
+// Persistent CUDA-core decode kernel: paged-KV attention for tiles of <= 8 rows,
+// fused with the merge of split-KV partial states.
+//
+// Page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎":
+//   核心机制 3 (paper §3.2): scattered KV tiles are gathered into contiguous
+//     shared memory, after which sparse and dense KV share one kernel body.
+//     Here each page-head run (page_size x 256 B, contiguous in the HND pool)
+//     is one bulk async copy into a 32-token shared-memory stage; a ring of
+//     stages keeps many copies in flight.
+//   核心机制 4 (paper §3.2.2): query tile 1 runs on CUDA cores, since MMA
+//     needs >= 16 rows; GQA heads of one KV head fold into the rows
+//     (术语与记号 "GQA 头组融合", paper App. A), so one KV load serves g rows.
+//   核心机制 6-7 (paper §3.3.1, App. D): one persistent CTA per queue of the
+//     plan; attention and the contraction of partial outputs in one kernel;
+//     a split row is merged by whichever of its chunks finishes last, reading
+//     the slots in the plan's fixed order (an arrival counter only counts; it
+//     never accumulates data), so results are bit-identical run to run.
+//
+// CTA layout: warp 0 = producer (page-index prefetch + bulk copies),
+// warps 1..NW = consumers.  Consumer warps take the CTA's KV stages round-robin
+// (stage n -> warp n % NW); each keeps an online-softmax state, and at the end
+// of a work item the NW states are merged through shared memory in warp order.
+//
+// Consumer lane mapping per 32-token stage, R rows (R = 1, 2, 4, 8):
+//   q.k: lane = (half tl, dim-lane dl); dl owns dims 8*dl..8*dl+7, tl owns
+//        tokens; partial dots of 16 (token, row) pairs are transposed through
+//        shared memory and summed, leaving one score per lane.
+//   p.v: lane owns dims 4*lane..4*lane+3 of all R accumulator rows.
+// Scores are kept in the log2 domain (q is pre-scaled by scale * log2 e).
+#pragma once
+
+#include "device_common.cuh"
+#include "plan.h"
+
+namespace fi {
+
+struct DecodeParams {
+  const int32_t* cta_indptr;
+  const int32_t* items;
+  const int32_t* units;
+  const int32_t* slot_unit;
+  const int32_t* kv_indices;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;
+  float* lse;
+  float* part_o;    // [slots][slot_rows][128] fp32, normalised O
+  float* part_lse;  // [slots][slot_rows] fp32, log2 domain
+  uint32_t* counters;
+  int32_t* err;
+  long long page_stride;  // elements per page (H_kv * page_size * 128)
+  long long head_stride;  // elements per page-head (page_size * 128)
+  int num_pages;
+  int page_size;
+  int hqo;
+  int group;
+  int slot_rows;
+  float scale_log2;
+};
+
+constexpr int kStageTokens = 32;
+constexpr int kIdxDepth = 4;  // page-index prefetch distance (stages)
+constexpr int kRedHalf = 336; // words between the two halves of the transpose scratch
+constexpr int kRedRow = 20;   // words per lane row of the transpose scratch
+
+template <int R, int NW, int S>
+struct DecodeSmem {
+  __nv_bfloat16 kv[S][2][kStageTokens][kHeadDim];  // [stage][K|V][token][dim]
+  float red[NW][2 * kRedHalf];
+  float pbuf[NW][kStageTokens * R];
+  float alpha[NW][8];
+  float macc[NW][R][kHeadDim];
+  float mm[NW][8];
+  float ml[NW][8];
+  int32_t idx[kIdxDepth][32];
+  uint64_t full[S];
+  uint64_t empty[S];
+  int flag;
+  int abort;
+};
+
+// Walks the stages of one CTA's queue in order: (item, stage within item).
+struct StageCursor {
+  int pos, end;
+  int st, nst;
+  int page_base, kv_head, kv_lo, kv_hi;
+
+  __device__ __forceinline__ bool load(const int32_t* items) {
+    while (pos < end) {
+      const int4 a = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields));
+      const int4 b = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields + 4));
+      page_base = a.x;
+      kv_head = a.w;
+      kv_lo = b.x;
+      kv_hi = b.y;
+      nst = (kv_hi - kv_lo + kStageTokens - 1) / kStageTokens;
+      st = 0;
+      if (nst > 0) return true;
+      ++pos;
+    }
+    return false;
+  }
+  __device__ __forceinline__ bool next(const int32_t* items) {
+    if (++st < nst) return true;
+    ++pos;
+    return load(items);
+  }
+  __device__ __forceinline__ int tok0() const { return kv_lo + st * kStageTokens; }
+  __device__ __forceinline__ int ntok() const { return min(kStageTokens, kv_hi - tok0()); }
+};
+
+template <int R, int NW, int S>
+__device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin, int end) {
+  const int lane = threadIdx.x & 31;
+  const int ps = p.page_size;
+  const uint64_t policy = policy_evict_first();
+  StageCursor cur{begin, end, 0, 0, 0, 0, 0, 0};
+  StageCursor ahead = cur;
+  bool cur_ok = cur.load(p.items);
+  bool ahead_ok = ahead.load(p.items);
+
+  auto fetch = [&](const StageCursor& c, int32_t* dst) {
+    const int t0 = c.tok0();
+    const int first = t0 / ps;
+    const int nseg = (t0 + c.ntok() - 1) / ps - first + 1;
+    if (lane < nseg) cp_async_4(dst + lane, p.kv_indices + c.page_base + first + lane);
+  };
+
+#pragma unroll
+  for (int d = 0; d < kIdxDepth; ++d) {
+    if (ahead_ok) {
+      fetch(ahead, sm.idx[d]);
+      ahead_ok = ahead.next(p.items);
+    }
+    cp_async_commit();
+  }
+
+  int issued = 0;
+  for (int n = 0; cur_ok; ++n) {
+    cp_async_wait<kIdxDepth - 1>();
+    const int t0 = cur.tok0();
+    const int nt = cur.ntok();
+    const int first = t0 / ps;
+    const int nseg = (t0 + nt - 1) / ps - first + 1;
+    int page = (lane < nseg) ? sm.idx[n % kIdxDepth][lane] : 0;
+    __syncwarp();
+    if (ahead_ok) {
+      fetch(ahead, sm.idx[n % kIdxDepth]);
+      ahead_ok = ahead.next(p.items);
+    }
+    cp_async_commit();
+
+    const int slot = n % S;
+    const int fill = n / S;
+    if (fill > 0) {
+      const bool got = mbar_wait(&sm.empty[slot], (fill - 1) & 1, p.err, &sm.abort);
+      if (!__all_sync(0xffffffffu, got)) break;
+    }
+
+    int seg_lo = 0, seg_n = 0;
+    bool ok = false;
+    if (lane < nseg) {
+      const int pg_tok = (first + lane) * ps;
+      seg_lo = max(t0, pg_tok);
+      seg_n = min(t0 + nt, pg_tok + ps) - seg_lo;
+      ok = page >= 0 && page < p.num_pages;
+      if (!ok) atomicOr(p.err, FI_DEVERR_PAGE_OOB);
+    }
+    const uint32_t bytes = ok ? uint32_t(seg_n) * (2u * kHeadDim * 2u) : 0u;
+    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+    if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], total);
+    __syncwarp();
+    if (ok) {
+      const long long src = (long long)page * p.page_stride + (long long)cur.kv_head * p.head_stride +
+                            (long long)(seg_lo - (first + lane) * ps) * kHeadDim;
+      const uint32_t nb = uint32_t(seg_n) * kHeadDim * 2u;
+      bulk_g2s(&sm.kv[slot][0][seg_lo - t0][0], p.k + src, nb, &sm.full[slot], policy);
+      bulk_g2s(&sm.kv[slot][1][seg_lo - t0][0], p.v + src, nb, &sm.full[slot], policy);
+    }
+    cur_ok = cur.next(p.items);
+    issued = n + 1;
+  }
+  cp_async_wait<0>();
+  // never leave with bulk copies still landing in this CTA's shared memory
+  for (int n = max(0, issued - S); n < issued; ++n) mbar_wait_bounded(&sm.full[n % S], (n / S) & 1);
+}
+
+template <int R>
+__device__ __forceinline__ void load_q_rows(const DecodeParams& p, int q_start, int q_len, int kv_head, int dl,
+                                            float2 (&q2)[R][4]) {
+  const int rows_valid = q_len * p.group;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (r < rows_valid) {
+      const int tok = q_start + r / p.group;
+      const int head = kv_head * p.group + r % p.group;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)tok * p.hqo + head) * kHeadDim + 8 * dl));
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float2 f = bf16x2_to_f2(w[c]);
+        q2[r][c] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) q2[r][c] = make_float2(0.f, 0.f);
+    }
+  }
+}
+
+template <int R, int NW, int S>
+__device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin, int end,
+                                                int w) {
+  constexpr int NT = 16 / R;  // tokens per half per sub-batch
+  const int lane = threadIdx.x & 31;
+  const int tl = lane >> 4, dl = lane & 15;
+  const int my_row = dl % R;
+  const int ctid = w * 32 + lane;
+  float* red = sm.red[w];
+  float* pb = sm.pbuf[w];
+  int stage_n = 0;
+  bool alive = true;
+
+  for (int pos = begin; pos < end; ++pos) {
+    const int4 ia = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields));
+    const int4 ib = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields + 4));
+    const int q_start = ia.y, q_len = ia.z, kv_head = ia.w;
+    const int kv_lo = ib.x, kv_hi = ib.y, diag = ib.z, slot_out = ib.w;
+    const int nst = (kv_hi - kv_lo + kStageTokens - 1) / kStageTokens;
+
+    float2 q2[R][4];
+    load_q_rows<R>(p, q_start, q_len, kv_head, dl, q2);
+    float2 acc[R][2];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
+    float m_run = -INFINITY, l_run = 0.f;
+    // token limit of my score row: key j visible iff j <= diag + (row / g)
+    const int row_limit = diag + my_row / p.group;
+
+    for (int st = 0; st < nst; ++st) {
+      const int n = stage_n + st;
+      if (n % NW != w) continue;
+      const int slot = n % S;
+      if (!alive) continue;
+      const bool got = mbar_wait(&sm.full[slot], (n / S) & 1, p.err, &sm.abort);
+      if (!__all_sync(0xffffffffu, got)) {
+        alive = false;  // keep joining the named barriers; outputs of an aborted run are undefined
+        continue;
+      }
+      const int t0 = kv_lo + st * kStageTokens;
+      const int nt = min(kStageTokens, kv_hi - t0);
+      const __nv_bfloat16* Ks = &sm.kv[slot][0][0][0];
+      const __nv_bfloat16* Vs = &sm.kv[slot][1][0][0];
+
+      // ---- scores: R sub-batches of 2*NT tokens -------------------------------
+      float sc[R];
+#pragma unroll
+      for (int b = 0; b < R; ++b) {
+        float part[16];
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+          const int t = b * 2 * NT + tl * NT + u;
+          const uint4 raw = *reinterpret_cast<const uint4*>(Ks + t * kHeadDim + 8 * dl);
+          const float2 k0 = bf16x2_to_f2(raw.x), k1 = bf16x2_to_f2(raw.y);
+          const float2 k2 = bf16x2_to_f2(raw.z), k3 = bf16x2_to_f2(raw.w);
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float2 s2 = __fmul2_rn(q2[r][0], k0);
+            s2 = __ffma2_rn(q2[r][1], k1, s2);
+            s2 = __ffma2_rn(q2[r][2], k2, s2);
+            s2 = __ffma2_rn(q2[r][3], k3, s2);
+            part[u * R + r] = s2.x + s2.y;
+          }
+        }
+        float4* rw = reinterpret_cast<float4*>(red + tl * kRedHalf + dl * kRedRow);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) rw[c] = make_float4(part[4 * c], part[4 * c + 1], part[4 * c + 2], part[4 * c + 3]);
+        __syncwarp();
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) s += red[tl * kRedHalf + j * kRedRow + dl];
+        __syncwarp();
+        const int t = b * 2 * NT + tl * NT + dl / R;
+        const bool vis = (t < nt) && (t0 + t <= row_limit);
+        sc[b] = vis ? s : -INFINITY;
+      }
+
+      // ---- online softmax over the stage --------------------------------------
+      float mx = sc[0];
+#pragma unroll
+      for (int b = 1; b < R; ++b) mx = fmaxf(mx, sc[b]);
+#pragma unroll
+      for (int msk = R; msk < 32; msk <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = fast_exp2(m_run - m_use);
+      float psum = 0.f;
+#pragma unroll
+      for (int b = 0; b < R; ++b) {
+        const float pv = fast_exp2(sc[b] - m_use);
+        psum += pv;
+        pb[b * 32 + lane] = pv;
+      }
+#pragma unroll
+      for (int msk = R; msk < 32; msk <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, msk);
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+      if (tl == 0 && dl < R) sm.alpha[w][dl] = alpha;
+      __syncwarp();
+
+      // ---- p.v -------------------------------------------------------------------
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float a = sm.alpha[w][r];
+        acc[r][0] = __fmul2_rn(acc[r][0], make_float2(a, a));
+        acc[r][1] = __fmul2_rn(acc[r][1], make_float2(a, a));
+      }
+#pragma unroll 4
+      for (int t = 0; t < nt; ++t) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * kHeadDim + 4 * lane);
+        const float2 v0 = bf16x2_to_f2(raw.x), v1 = bf16x2_to_f2(raw.y);
+        float pr[R];
+        if constexpr (R >= 4) {
+#pragma unroll
+          for (int c = 0; c < R / 4; ++c) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pb + t * R + 4 * c);
+            pr[4 * c] = p4.x;
+            pr[4 * c + 1] = p4.y;
+            pr[4 * c + 2] = p4.z;
+            pr[4 * c + 3] = p4.w;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < R; ++r) pr[r] = pb[t * R + r];
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float2 pp = make_float2(pr[r], pr[r]);
+          acc[r][0] = __ffma2_rn(pp, v0, acc[r][0]);
+          acc[r][1] = __ffma2_rn(pp, v1, acc[r][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    }
+    stage_n += nst;
+
+    // ---- merge the NW warp states of this item --------------------------------
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      *reinterpret_cast<float4*>(&sm.macc[w][r][4 * lane]) =
+          make_float4(acc[r][0].x, acc[r][0].y, acc[r][1].x, acc[r][1].y);
+    if (tl == 0 && dl < R) {
+      sm.mm[w][dl] = m_run;
+      sm.ml[w][dl] = l_run;
+    }
+    named_bar_sync(1, NW * 32);
+
+    const int rows_valid = q_len * p.group;
+    for (int u = ctid; u < R * 32; u += NW * 32) {
+      const int r = u >> 5, dq = u & 31;
+      float M = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, sm.mm[ww][r]);
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) {
+          const float s = fast_exp2(sm.mm[ww][r] - M);
+          const float4 a = *reinterpret_cast<const float4*>(&sm.macc[ww][r][4 * dq]);
+          L += s * sm.ml[ww][r];
+          O.x += s * a.x;
+          O.y += s * a.y;
+          O.z += s * a.z;
+          O.w += s * a.w;
+        }
+        const float inv = 1.f / L;
+        O.x *= inv;
+        O.y *= inv;
+        O.z *= inv;
+        O.w *= inv;
+      }
+      const float lse2 = (M == -INFINITY) ? -INFINITY : M + fast_log2(L);
+      if (r < rows_valid) {
+        if (slot_out < 0) {
+          const int tok = q_start + r / p.group;
+          const int head = kv_head * p.group + r % p.group;
+          const size_t orow = (size_t)tok * p.hqo + head;
+          uint2 packed;
+          packed.x = f2_to_bf16x2(O.x, O.y);
+          packed.y = f2_to_bf16x2(O.z, O.w);
+          *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
+          if (dq == 0) p.lse[orow] = lse2 * kLn2;
+        } else {
+          const size_t srow = (size_t)slot_out * p.slot_rows + r;
+          *reinterpret_cast<float4*>(p.part_o + srow * kHeadDim + 4 * dq) = O;
+          if (dq == 0) p.part_lse[srow] = lse2;
+        }
+      }
+    }
+
+    if (slot_out >= 0) {
+      // contraction of a split row: the last chunk to finish merges all slots in order
+      named_bar_sync(1, NW * 32);
+      const int unit = __ldg(p.slot_unit + slot_out);
+      if (ctid == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(p.counters + unit, 1u);
+        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+        sm.flag = (prev == uint32_t(n_chunks - 1)) ? 1 : 0;
+        if (sm.flag) __threadfence();
+      }
+      named_bar_sync(1, NW * 32);
+      if (sm.flag) {
+        const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
+        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+        for (int u = ctid; u < R * 32; u += NW * 32) {
+          const int r = u >> 5, dq = u & 31;
+          if (r >= rows_valid) continue;
+          float M = -INFINITY;
+          for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + r));
+          float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+          float L = 0.f;
+          if (M != -INFINITY) {
+            for (int c = 0; c < n_chunks; ++c) {
+              const size_t srow = (size_t)(first + c) * p.slot_rows + r;
+              const float s = fast_exp2(__ldcg(p.part_lse + srow) - M);
+              const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_o + srow * kHeadDim + 4 * dq));
+              L += s;
+              O.x += s * a.x;
+              O.y += s * a.y;
+              O.z += s * a.z;
+              O.w += s * a.w;
+            }
+            const float inv = 1.f / L;
+            O.x *= inv;
+            O.y *= inv;
+            O.z *= inv;
+            O.w *= inv;
+          }
+          const int tok = q_start + r / p.group;
+          const int head = kv_head * p.group + r % p.group;
+          const size_t orow = (size_t)tok * p.hqo + head;
+          uint2 packed;
+          packed.x = f2_to_bf16x2(O.x, O.y);
+          packed.y = f2_to_bf16x2(O.z, O.w);
+          *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
+          if (dq == 0) p.lse[orow] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(L)) * kLn2;
+        }
+        if (ctid == 0) p.counters[unit] = 0u;
+      }
+    }
+    named_bar_sync(1, NW * 32);
+  }
+}
+
+template <int R, int NW, int S>
+__global__ void __launch_bounds__((NW + 1) * 32, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S>*>(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    sm.abort = 0;
+    sm.flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int begin = __ldg(p.cta_indptr + blockIdx.x);
+  const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
+  if (warp == 0) {
+    decode_producer<R, NW, S>(p, sm, begin, end);
+  } else {
+    decode_consumer<R, NW, S>(p, sm, begin, end, warp - 1);
+  }
+}
+
+}  // namespace fi

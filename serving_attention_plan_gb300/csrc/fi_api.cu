@@ -1,0 +1,356 @@
+// C ABI of the library: workspace, plan upload, run, merge, errors.
+//
+// Page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎", 核心机制 7
+// "CUDAGraph 兼容的静态化手段" (paper App. D.1-D.3): the workspace is
+// allocated once at maximum capacity with constant segment offsets; the plan
+// is computed in page-locked host memory and sent to its segments with
+// cudaMemcpyAsync; the persistent kernel has a fixed grid.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "../../include/fi.h"
+#include "decode_kernel.cuh"
+#include "merge_kernel.cuh"
+#include "plan.h"
+#include "prefill_launch.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return FI_ERR_CUDA;
+}
+
+#define FI_CUDA(call)                                        \
+  do {                                                       \
+    cudaError_t e_ = (call);                                 \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);      \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct fi_workspace {
+  int device = 0;
+  int max_batch = 0, max_total_q = 0, max_kv_pages = 0;
+  int hqo = 0, hkv = 0, head_dim = 0, num_ctas = 0;
+  int64_t max_items = 0, max_units = 0, max_slots = 0;
+  fi::CostModel cost;
+
+  // segment byte offsets; [0, plan_bytes) is mirrored in pinned host memory
+  size_t off_header = 0, off_cta = 0, off_items = 0, off_units = 0, off_slot_unit = 0, off_kv = 0, plan_bytes = 0;
+  size_t off_counters = 0, off_err = 0, off_part_lse = 0, off_part_o = 0, dev_bytes = 0;
+  char* dbuf = nullptr;
+  char* hbuf = nullptr;
+  cudaEvent_t copy_done = nullptr;
+  bool copy_pending = false;
+
+  bool has_plan = false;
+  int32_t header[fi::kHeaderLen] = {0};
+  int32_t max_page = -1;
+  int64_t plan_nnz = 0;
+};
+
+namespace {
+
+constexpr int kDecodeWarps = 8;   // consumer warps per decode CTA
+constexpr int kDecodeStages = 8;  // 32-token KV stages in flight per CTA
+
+template <int R>
+int launch_decode(const fi_workspace* ws, const fi::DecodeParams& p, cudaStream_t stream) {
+  using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages>;
+  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
+  });
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(decode)");
+  kernel<<<ws->num_ctas, (kDecodeWarps + 1) * 32, sizeof(Smem), stream>>>(p);
+  FI_CUDA(cudaGetLastError());
+  return FI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fi_status_string(int status) {
+  switch (status) {
+    case FI_OK: return "ok";
+    case FI_ERR_INVALID_ARG: return "invalid argument";
+    case FI_ERR_CAPACITY: return "workspace capacity exceeded";
+    case FI_ERR_UNSUPPORTED: return "unsupported shape";
+    case FI_ERR_CUDA: return "CUDA error";
+    case FI_ERR_DEVICE: return "device-side check failed";
+    case FI_ERR_NO_PLAN: return "no plan";
+    default: return "unknown status";
+  }
+}
+
+const char* fi_last_error_message(void) { return g_last_error.c_str(); }
+
+int fi_device_sm_count(int* out) {
+  if (out == nullptr) return FI_ERR_INVALID_ARG;
+  int dev = 0;
+  FI_CUDA(cudaGetDevice(&dev));
+  FI_CUDA(cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev));
+  return FI_OK;
+}
+
+int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int num_qo_heads, int num_kv_heads,
+                        int head_dim, int num_ctas, fi_workspace** out) {
+  if (out == nullptr) return FI_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (max_batch < 1 || max_total_q < 1 || max_kv_pages < 1 || num_qo_heads < 1 || num_kv_heads < 1 || num_ctas < 0)
+    return FI_ERR_INVALID_ARG;
+  if (head_dim != fi::kHeadDim || num_qo_heads % num_kv_heads != 0) return FI_ERR_UNSUPPORTED;
+  int dev = 0;
+  FI_CUDA(cudaGetDevice(&dev));
+  if (num_ctas == 0) FI_CUDA(cudaDeviceGetAttribute(&num_ctas, cudaDevAttrMultiProcessorCount, dev));
+
+  fi_workspace* ws = new (std::nothrow) fi_workspace();
+  if (ws == nullptr) return FI_ERR_CAPACITY;
+  ws->device = dev;
+  ws->max_batch = max_batch;
+  ws->max_total_q = max_total_q;
+  ws->max_kv_pages = max_kv_pages;
+  ws->hqo = num_qo_heads;
+  ws->hkv = num_kv_heads;
+  ws->head_dim = head_dim;
+  ws->num_ctas = num_ctas;
+  // App. D.3 bound: partial tiles < 2 * #CTA, hence split rows < #CTA.
+  ws->max_slots = 2 * int64_t(num_ctas);
+  ws->max_units = num_ctas;
+  ws->max_items = int64_t(num_kv_heads) * max_total_q + ws->max_slots;
+
+  size_t off = 0;
+  auto seg = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  ws->off_header = seg(sizeof(int32_t) * fi::kHeaderLen);
+  ws->off_cta = seg(sizeof(int32_t) * (num_ctas + 1));
+  ws->off_items = seg(sizeof(int32_t) * fi::kItemFields * ws->max_items);
+  ws->off_units = seg(sizeof(int32_t) * fi::kUnitFields * ws->max_units);
+  ws->off_slot_unit = seg(sizeof(int32_t) * ws->max_slots);
+  ws->off_kv = seg(sizeof(int32_t) * size_t(max_kv_pages));
+  ws->plan_bytes = off;
+  ws->off_counters = seg(sizeof(uint32_t) * ws->max_units);
+  ws->off_err = seg(sizeof(int32_t) * 4);
+  ws->off_part_lse = seg(sizeof(float) * ws->max_slots * fi::kTcRows);
+  ws->off_part_o = seg(sizeof(float) * ws->max_slots * fi::kTcRows * fi::kHeadDim);
+  ws->dev_bytes = off;
+
+  cudaError_t e = cudaMalloc(&ws->dbuf, ws->dev_bytes);
+  if (e == cudaSuccess) e = cudaMemset(ws->dbuf + ws->off_counters, 0, ws->off_part_lse - ws->off_counters);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&ws->hbuf), ws->plan_bytes, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ws->copy_done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    const int st = cuda_fail(e, "fi_workspace_create");
+    fi_workspace_destroy(ws);
+    return st;
+  }
+  *out = ws;
+  return FI_OK;
+}
+
+int fi_workspace_destroy(fi_workspace* ws) {
+  if (ws == nullptr) return FI_OK;
+  if (ws->copy_done != nullptr) {
+    cudaEventSynchronize(ws->copy_done);
+    cudaEventDestroy(ws->copy_done);
+  }
+  if (ws->hbuf != nullptr) cudaFreeHost(ws->hbuf);
+  if (ws->dbuf != nullptr) cudaFree(ws->dbuf);
+  delete ws;
+  return FI_OK;
+}
+
+int fi_workspace_set_cost_model(fi_workspace* ws, int64_t alpha, int64_t beta, int32_t l_min) {
+  if (ws == nullptr || alpha < 0 || beta < 1 || l_min < 1) return FI_ERR_INVALID_ARG;
+  ws->cost.alpha = alpha;
+  ws->cost.beta = beta;
+  ws->cost.l_min = l_min;
+  return FI_OK;
+}
+
+int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+            const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
+            int causal, void* stream) {
+  if (ws == nullptr) return FI_ERR_INVALID_ARG;
+  if (num_qo_heads != ws->hqo || num_kv_heads != ws->hkv || head_dim != ws->head_dim) return FI_ERR_INVALID_ARG;
+  if (batch > ws->max_batch) return FI_ERR_CAPACITY;
+  fi::PlanInput in{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                   causal, ws->num_ctas};
+  int st = fi::validate_input(in);
+  if (st != FI_OK) return st;
+  const int64_t nnz = kv_indptr[batch];
+  if (qo_indptr[batch] > ws->max_total_q || nnz > ws->max_kv_pages) return FI_ERR_CAPACITY;
+  if (nnz > 0 && kv_indices == nullptr) return FI_ERR_INVALID_ARG;
+  int32_t max_page = -1;
+  for (int64_t k = 0; k < nnz; ++k) {
+    if (kv_indices[k] < 0) return FI_ERR_INVALID_ARG;
+    max_page = std::max(max_page, kv_indices[k]);
+  }
+  fi::Plan plan;
+  st = fi::build_plan(in, ws->cost, &plan);
+  if (st != FI_OK) return st;
+  const int64_t n_items = plan.header[fi::H_NUM_ITEMS], n_units = plan.header[fi::H_NUM_UNITS],
+                n_slots = plan.header[fi::H_NUM_SLOTS];
+  if (n_items > ws->max_items || n_units > ws->max_units || n_slots > ws->max_slots) return FI_ERR_CAPACITY;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ws->copy_pending) {
+    FI_CUDA(cudaEventSynchronize(ws->copy_done));
+    ws->copy_pending = false;
+  }
+  char* h = ws->hbuf;
+  std::memcpy(h + ws->off_header, plan.header, sizeof(plan.header));
+  std::memcpy(h + ws->off_cta, plan.cta_indptr.data(), plan.cta_indptr.size() * sizeof(int32_t));
+  if (n_items) std::memcpy(h + ws->off_items, plan.items.data(), plan.items.size() * sizeof(int32_t));
+  if (n_units) std::memcpy(h + ws->off_units, plan.units.data(), plan.units.size() * sizeof(int32_t));
+  if (n_slots) std::memcpy(h + ws->off_slot_unit, plan.slot_unit.data(), plan.slot_unit.size() * sizeof(int32_t));
+  if (nnz) std::memcpy(h + ws->off_kv, kv_indices, size_t(nnz) * sizeof(int32_t));
+
+  struct Seg {
+    size_t off, bytes;
+  } segs[] = {
+      {ws->off_header, sizeof(plan.header)},
+      {ws->off_cta, plan.cta_indptr.size() * sizeof(int32_t)},
+      {ws->off_items, plan.items.size() * sizeof(int32_t)},
+      {ws->off_units, plan.units.size() * sizeof(int32_t)},
+      {ws->off_slot_unit, plan.slot_unit.size() * sizeof(int32_t)},
+      {ws->off_kv, size_t(nnz) * sizeof(int32_t)},
+  };
+  for (const Seg& sg : segs) {
+    if (sg.bytes) FI_CUDA(cudaMemcpyAsync(ws->dbuf + sg.off, h + sg.off, sg.bytes, cudaMemcpyHostToDevice, s));
+  }
+  FI_CUDA(cudaEventRecord(ws->copy_done, s));
+  ws->copy_pending = true;
+  std::memcpy(ws->header, plan.header, sizeof(plan.header));
+  ws->max_page = max_page;
+  ws->plan_nnz = nnz;
+  ws->has_plan = true;
+  return FI_OK;
+}
+
+int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_pages, int num_pages, void* o,
+           float* lse, void* stream) {
+  if (ws == nullptr) return FI_ERR_INVALID_ARG;
+  if (!ws->has_plan) return FI_ERR_NO_PLAN;
+  if (num_pages < 0 || ws->max_page >= num_pages) return FI_ERR_INVALID_ARG;
+  const int32_t* h = ws->header;
+  const bool any_rows = h[fi::H_NUM_ITEMS] > 0;
+  if (any_rows && (q == nullptr || o == nullptr || lse == nullptr)) return FI_ERR_INVALID_ARG;
+  if (ws->plan_nnz > 0 && (k_pages == nullptr || v_pages == nullptr)) return FI_ERR_INVALID_ARG;
+  if (!any_rows) return FI_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int ps = h[fi::H_PAGE_SIZE];
+  const float scale_log2 = fi::kLog2e / std::sqrt(float(ws->head_dim));
+  char* d = ws->dbuf;
+
+  if (h[fi::H_PATH] == fi::kPathDecode) {
+    fi::DecodeParams p;
+    p.cta_indptr = reinterpret_cast<const int32_t*>(d + ws->off_cta);
+    p.items = reinterpret_cast<const int32_t*>(d + ws->off_items);
+    p.units = reinterpret_cast<const int32_t*>(d + ws->off_units);
+    p.slot_unit = reinterpret_cast<const int32_t*>(d + ws->off_slot_unit);
+    p.kv_indices = reinterpret_cast<const int32_t*>(d + ws->off_kv);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k_pages);
+    p.v = static_cast<const __nv_bfloat16*>(v_pages);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.part_o = reinterpret_cast<float*>(d + ws->off_part_o);
+    p.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
+    p.counters = reinterpret_cast<uint32_t*>(d + ws->off_counters);
+    p.err = reinterpret_cast<int32_t*>(d + ws->off_err);
+    p.page_stride = (long long)ws->hkv * ps * fi::kHeadDim;
+    p.head_stride = (long long)ps * fi::kHeadDim;
+    p.num_pages = num_pages;
+    p.page_size = ps;
+    p.hqo = ws->hqo;
+    p.group = h[fi::H_GROUP];
+    p.slot_rows = fi::kTcRows;
+    p.scale_log2 = scale_log2;
+    switch (h[fi::H_ROWS_TILE]) {
+      case 1: return launch_decode<1>(ws, p, s);
+      case 2: return launch_decode<2>(ws, p, s);
+      case 4: return launch_decode<4>(ws, p, s);
+      case 8: return launch_decode<8>(ws, p, s);
+      default: return FI_ERR_UNSUPPORTED;
+    }
+  }
+
+  fi::PrefillArgs a;
+  a.cta_indptr = reinterpret_cast<const int32_t*>(d + ws->off_cta);
+  a.items = reinterpret_cast<const int32_t*>(d + ws->off_items);
+  a.units = reinterpret_cast<const int32_t*>(d + ws->off_units);
+  a.slot_unit = reinterpret_cast<const int32_t*>(d + ws->off_slot_unit);
+  a.kv_indices = reinterpret_cast<const int32_t*>(d + ws->off_kv);
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.o = o;
+  a.lse = lse;
+  a.part_o = reinterpret_cast<float*>(d + ws->off_part_o);
+  a.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
+  a.counters = reinterpret_cast<uint32_t*>(d + ws->off_counters);
+  a.err = reinterpret_cast<int32_t*>(d + ws->off_err);
+  a.num_pages = num_pages;
+  a.page_size = ps;
+  a.hqo = ws->hqo;
+  a.hkv = ws->hkv;
+  a.group = h[fi::H_GROUP];
+  a.tile_tokens = h[fi::H_TILE_TOKENS];
+  a.total_q = ws->max_total_q;
+  a.num_ctas = ws->num_ctas;
+  a.scale_log2 = scale_log2;
+  return fi::launch_prefill(a, s);
+}
+
+int fi_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
+                    int rows, int heads, int head_dim, void* stream) {
+  if (rows < 0 || heads < 1) return FI_ERR_INVALID_ARG;
+  if (head_dim != fi::kHeadDim) return FI_ERR_UNSUPPORTED;
+  if (rows == 0) return FI_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o || !lse) return FI_ERR_INVALID_ARG;
+  const long long n = (long long)rows * heads;
+  int blocks = int(std::min<long long>((n + 7) / 8, 4096));
+  fi::merge_states_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(o_a), lse_a, static_cast<const __nv_bfloat16*>(o_b), lse_b,
+      static_cast<__nv_bfloat16*>(o), lse, n);
+  FI_CUDA(cudaGetLastError());
+  return FI_OK;
+}
+
+int fi_get_error(fi_workspace* ws, int32_t* err_bits) {
+  if (ws == nullptr || err_bits == nullptr) return FI_ERR_INVALID_ARG;
+  FI_CUDA(cudaDeviceSynchronize());
+  int32_t* d = reinterpret_cast<int32_t*>(ws->dbuf + ws->off_err);
+  FI_CUDA(cudaMemcpy(err_bits, d, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  FI_CUDA(cudaMemset(d, 0, sizeof(int32_t)));
+  FI_CUDA(cudaDeviceSynchronize());
+  return FI_OK;
+}
+
+int fi_plan_info(const fi_workspace* ws, int32_t* header16) {
+  if (ws == nullptr || header16 == nullptr) return FI_ERR_INVALID_ARG;
+  if (!ws->has_plan) return FI_ERR_NO_PLAN;
+  std::memcpy(header16, ws->header, sizeof(ws->header));
+  return FI_OK;
+}
+
+}  // extern "C"

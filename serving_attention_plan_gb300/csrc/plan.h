@@ -1,0 +1,70 @@
+// Host planner of the paged serving-attention library (C++17, no CUDA).
+//
+// Builds the per-step work plan described on page "FlashInfer：面向 LLM 推理服务
+// 的高效可定制注意力引擎", 核心机制 6 (paper §3.3.1, Alg. 1) and 核心机制 7
+// (paper App. D.2-D.3).  The rules fixed where the page is silent are listed
+// beside `build_plan`.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+namespace fi {
+
+constexpr int kHeadDim = 128;
+constexpr int kPathDecode = 0;
+constexpr int kPathTensor = 1;
+constexpr int kTcRows = 128;          // rows of a tensor-core tile (tcgen05 M)
+constexpr int kDecodeMaxRows = 8;     // largest tile the CUDA-core decode path takes
+constexpr int32_t kNotCausalDiag = 1 << 30;
+constexpr int32_t kPlanMagic = 0x46495031;
+constexpr int kHeaderLen = 16;
+constexpr int kItemFields = 8;
+constexpr int kUnitFields = 8;
+
+// Header slots.
+enum HeaderSlot {
+  H_MAGIC = 0, H_PATH, H_TILE_TOKENS, H_ROWS_TILE, H_GROUP, H_NUM_CTAS, H_NUM_ITEMS, H_NUM_UNITS,
+  H_NUM_SLOTS, H_LKV, H_PAGE_SIZE, H_CAUSAL, H_HQO, H_HKV, H_HEAD_DIM, H_BATCH
+};
+
+// Item fields: one chunk of one (request, KV head, query tile).
+enum ItemField { I_PAGE_BASE = 0, I_Q_START, I_Q_LEN, I_KV_HEAD, I_KV_LO, I_KV_HI, I_DIAG, I_SLOT };
+// Split-unit fields: the reduction map of one split (request, KV head, query tile).
+enum UnitField { U_FIRST_SLOT = 0, U_N_CHUNKS, U_Q_START, U_Q_LEN, U_KV_HEAD };
+
+struct CostModel {
+  int64_t alpha = 1;
+  int64_t beta = 1;
+  int32_t l_min = 256;
+};
+
+struct PlanInput {
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* last_page_len;
+  int batch;
+  int num_qo_heads;
+  int num_kv_heads;
+  int head_dim;
+  int page_size;
+  int causal;
+  int num_ctas;
+};
+
+struct Plan {
+  int32_t header[kHeaderLen];
+  std::vector<int32_t> cta_indptr;   // [num_ctas + 1]
+  std::vector<int32_t> items;        // [n_items * kItemFields], CTA queue order
+  std::vector<int32_t> units;        // [n_units * kUnitFields]
+  std::vector<int32_t> slot_unit;    // [n_slots]
+  std::vector<int64_t> loads;        // accumulated cost per CTA
+};
+
+// Returns an fi_status code (0 = ok).
+int build_plan(const PlanInput& in, const CostModel& cost, Plan* out);
+
+// Checks that only depend on the inputs (same rules as build_plan's validation).
+int validate_input(const PlanInput& in);
+
+}  // namespace fi

@@ -1,0 +1,39 @@
+// Launch interface of the tensor-core (tcgen05) tile path.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace fi {
+
+struct PrefillArgs {
+  const int32_t* cta_indptr;
+  const int32_t* items;
+  const int32_t* units;
+  const int32_t* slot_unit;
+  const int32_t* kv_indices;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  uint32_t* counters;
+  int32_t* err;
+  int num_pages;
+  int page_size;
+  int hqo;
+  int hkv;
+  int group;
+  int tile_tokens;
+  int total_q;   // rows of q / o (capacity of the workspace)
+  int num_ctas;
+  float scale_log2;
+};
+
+// Returns an fi_status.
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace fi

@@ -115,11 +115,14 @@ def make_paged_batch(
     pool_pages: int | None = None,
     scale: float = 1.0,
     head_dim: int = HEAD_DIM,
+    with_data: bool = True,
 ) -> PagedBatch:
     """Build a paged batch from given lengths: page permutation, then Q, K pool, V pool.
 
     Pages of all requests are a random permutation of the pool (or, with
     `pool_pages` larger than needed, a random subset of it in random order).
+    With with_data=False only the index arrays are drawn (q/k/v are empty);
+    they are identical to the full draw's, since they come first.
     """
     q_lens = np.asarray(q_lens, dtype=np.int64)
     kv_lens = np.asarray(kv_lens, dtype=np.int64)
@@ -131,9 +134,14 @@ def make_paged_batch(
     qo_indptr = np.zeros(q_lens.shape[0] + 1, dtype=np.int32)
     qo_indptr[1:] = np.cumsum(q_lens)
     total_q = int(qo_indptr[-1])
-    q = _bf16_normals(rng, (total_q, num_qo_heads, head_dim), scale)
-    k = _bf16_normals(rng, (pool, num_kv_heads, page_size, head_dim), scale)
-    v = _bf16_normals(rng, (pool, num_kv_heads, page_size, head_dim), scale)
+    if with_data:
+        q = _bf16_normals(rng, (total_q, num_qo_heads, head_dim), scale)
+        k = _bf16_normals(rng, (pool, num_kv_heads, page_size, head_dim), scale)
+        v = _bf16_normals(rng, (pool, num_kv_heads, page_size, head_dim), scale)
+    else:
+        q = np.zeros((0, num_qo_heads, head_dim), np.uint16)
+        k = np.zeros((pool, num_kv_heads, page_size, 0), np.uint16)
+        v = k
     return PagedBatch(
         name=name,
         num_qo_heads=num_qo_heads,
@@ -164,29 +172,33 @@ WORKLOADS = (
 )
 
 
-def tiny_decode() -> PagedBatch:
+def tiny_decode(with_data: bool = True) -> PagedBatch:
     rng = np.random.default_rng(0)
     kv = np.array([37, 128, 255, 512], dtype=np.int64)
-    return make_paged_batch(rng, "tiny_decode", np.ones(4, np.int64), kv, 8, 2, 16, False, pool_pages=128)
+    return make_paged_batch(rng, "tiny_decode", np.ones(4, np.int64), kv, 8, 2, 16, False, pool_pages=128,
+                            with_data=with_data)
 
 
-def llama3_8b_decode(batch: int = 128, max_kv: int = 4096) -> PagedBatch:
+def llama3_8b_decode(batch: int = 128, max_kv: int = 4096, with_data: bool = True) -> PagedBatch:
     rng = np.random.default_rng(1)
     kv = rng.integers(1, max_kv + 1, size=batch)
-    return make_paged_batch(rng, "llama3_8b_decode", np.ones(batch, np.int64), kv, 32, 8, 16, False)
+    return make_paged_batch(rng, "llama3_8b_decode", np.ones(batch, np.int64), kv, 32, 8, 16, False,
+                            with_data=with_data)
 
 
-def skewed_long_decode(long_len: int = 131072, n_short: int = 63) -> PagedBatch:
+def skewed_long_decode(long_len: int = 131072, n_short: int = 63, with_data: bool = True) -> PagedBatch:
     rng = np.random.default_rng(2)
     short = rng.integers(256, 1025, size=n_short)
     kv = np.concatenate([[long_len], short]).astype(np.int64)
-    return make_paged_batch(rng, "skewed_long_decode", np.ones(kv.shape[0], np.int64), kv, 64, 8, 1, False)
+    return make_paged_batch(rng, "skewed_long_decode", np.ones(kv.shape[0], np.int64), kv, 64, 8, 1, False,
+                            with_data=with_data)
 
 
-def ragged_causal_prefill(batch: int = 16, lo: int = 128, hi: int = 4096) -> PagedBatch:
+def ragged_causal_prefill(batch: int = 16, lo: int = 128, hi: int = 4096, with_data: bool = True) -> PagedBatch:
     rng = np.random.default_rng(3)
     lens = rng.integers(lo, hi + 1, size=batch)
-    return make_paged_batch(rng, "ragged_causal_prefill", lens, lens, 32, 8, 16, True, scale=0.5)
+    return make_paged_batch(rng, "ragged_causal_prefill", lens, lens, 32, 8, 16, True, scale=0.5,
+                            with_data=with_data)
 
 
 def shared_prefix_decode(n_req: int = 64, prefix_len: int = 8192, lo: int = 256, hi: int = 1024) -> SharedPrefixBatch:

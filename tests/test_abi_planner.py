@@ -1,0 +1,146 @@
+"""C-ABI library on the CPU: it loads, exports what include/fi.h declares, and its
+host planner equals the oracle's plain restatement bit for bit (no GPU calls)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import planner as P
+from serving_attention_plan_gb300 import binding as B
+from serving_attention_plan_gb300 import build as BLD
+from serving_attention_plan_gb300 import workloads as W
+
+
+@pytest.fixture(scope="module")
+def lib():
+    BLD.build()
+    return B.lib()
+
+
+def test_exports_every_declared_symbol(lib, repo_root):
+    header = open(os.path.join(repo_root, "include", "fi.h")).read()
+    declared = set(re.findall(r"^\s*(?:int|const char\*)\s+(fi_\w+)\s*\(", header, flags=re.M))
+    assert len(declared) >= 12
+    for name in sorted(declared):
+        assert hasattr(lib, name), name
+    assert lib.fi_status_string(0) == b"ok"
+
+
+def _compare(qo, kv, last, hq, hk, ps, causal, n_cta, **kw):
+    got = B.plan_compute(qo, kv, last, hq, hk, ps, causal, n_cta, **kw)
+    ref = P.serialize(P.plan(qo, kv, last, hq, hk, ps, causal, n_cta, **kw))
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    a, b = P.deserialize(got), P.deserialize(ref)
+    for key in ("header", "cta_indptr", "items", "units", "slot_unit"):
+        assert np.array_equal(a[key], b[key]), key
+    return a
+
+
+def _case(rng, ps_choices=(1, 8, 16, 32)):
+    batch = int(rng.integers(1, 40))
+    hk = int(rng.choice([1, 2, 8]))
+    g = int(rng.choice([1, 2, 4, 8]))
+    ps = int(rng.choice(ps_choices))
+    causal = bool(rng.integers(0, 2))
+    prefill = bool(rng.integers(0, 2))
+    lq = rng.integers(0, 700, size=batch) if prefill else rng.integers(0, 2, size=batch)
+    lk = rng.integers(0, 5000, size=batch)
+    if causal:
+        lk = np.maximum(lk, lq)
+    if rng.integers(0, 3) == 0:
+        lk[int(rng.integers(0, batch))] = int(rng.integers(30000, 140000))
+    n_p = (lk + ps - 1) // ps
+    kv = np.concatenate([[0], np.cumsum(n_p)])
+    last = np.where(n_p > 0, lk - (n_p - 1) * ps, 0)
+    qo = np.concatenate([[0], np.cumsum(lq)])
+    return qo, kv, last, hk * g, hk, ps, causal
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_cpp_planner_matches_oracle(lib, seed):
+    rng = np.random.default_rng(500 + seed)
+    qo, kv, last, hq, hk, ps, causal = _case(rng)
+    n_cta = int(rng.choice([1, 7, 148, 152, 304]))
+    g = hq // hk
+    if int(np.diff(qo).max(initial=0)) * g > 8 and (ps % 8 or 128 % ps):
+        with pytest.raises(B.FiError) as ei:
+            B.plan_compute(qo, kv, last, hq, hk, ps, causal, n_cta)
+        assert ei.value.status == 3
+        return
+    _compare(qo, kv, last, hq, hk, ps, causal, n_cta,
+             alpha=int(rng.integers(0, 4)), beta=int(rng.integers(1, 4)), l_min=int(rng.choice([1, 64, 256])))
+
+
+def test_hand_worked_plan_through_abi(lib, repo_root):
+    import json
+    gd = json.load(open(os.path.join(repo_root, "tests", "golden", "plan_hand_worked.json")))
+    a = gd["inputs"]
+    got = P.deserialize(B.plan_compute(a["qo_indptr"], a["kv_indptr"], a["last_page_len"], a["num_qo_heads"],
+                                       a["num_kv_heads"], a["page_size"], a["causal"], a["num_ctas"],
+                                       alpha=a["alpha"], beta=a["beta"], l_min=a["l_min"]))
+    assert got["header"].tolist() == gd["expected"]["header"]
+    assert got["items"].tolist() == gd["expected"]["items"]
+    assert got["cta_indptr"].tolist() == gd["expected"]["cta_indptr"]
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "llama3_8b_decode", "skewed_long_decode", "ragged_causal_prefill"])
+def test_workload_plans_match(lib, name):
+    """The five workloads' plans (lengths only, 152 CTAs) agree between C++ and the restatement."""
+    b = {
+        "tiny_decode": W.tiny_decode,
+        "llama3_8b_decode": W.llama3_8b_decode,
+        "skewed_long_decode": W.skewed_long_decode,
+        "ragged_causal_prefill": W.ragged_causal_prefill,
+    }[name](with_data=False)
+    a = _compare(b.qo_indptr, b.kv_indptr, b.last_page_len, b.num_qo_heads, b.num_kv_heads, b.page_size, b.causal, 152)
+    if name == "skewed_long_decode":
+        assert a["header"][7] == 8          # the long request splits on each of its 8 KV heads
+    if name == "ragged_causal_prefill":
+        assert a["header"][1] == 1 and a["header"][2] == 32
+
+
+def test_shared_prefix_plans_match(lib):
+    sp = W.shared_prefix_decode()
+    for part in (sp.prefix, sp.suffix):
+        _compare(part.qo_indptr, part.kv_indptr, part.last_page_len, part.num_qo_heads, part.num_kv_heads,
+                 part.page_size, part.causal, 152)
+    pre = P.deserialize(B.plan_compute(sp.prefix.qo_indptr, sp.prefix.kv_indptr, sp.prefix.last_page_len, 32, 8, 16,
+                                       False, 152))
+    assert pre["header"][1] == 1 and pre["header"][7] > 0   # tensor-core tiles, split across CTAs
+
+
+def test_plan_ignores_page_ids_and_is_deterministic(lib):
+    rng = np.random.default_rng(3)
+    qo, kv, last, hq, hk, ps, causal = _case(rng, ps_choices=(16,))
+    a = B.plan_compute(qo, kv, last, hq, hk, ps, causal, 152)
+    b = B.plan_compute(qo, kv, last, hq, hk, ps, causal, 152)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("bad", ["qo_not_monotone", "kv_start", "last_zero", "last_big", "head_dim", "heads"])
+def test_invalid_inputs_rejected(lib, bad):
+    qo = np.array([0, 1, 2]); kv = np.array([0, 2, 3]); last = np.array([5, 16]); hq, hk, d = 8, 2, 128
+    expect = 1
+    if bad == "qo_not_monotone":
+        qo = np.array([0, 2, 1])
+    elif bad == "kv_start":
+        kv = np.array([1, 2, 3])
+    elif bad == "last_zero":
+        last = np.array([0, 16])
+    elif bad == "last_big":
+        last = np.array([17, 16])
+    elif bad == "head_dim":
+        d, expect = 64, 3
+    elif bad == "heads":
+        hq, expect = 7, 3
+    with pytest.raises(B.FiError) as ei:
+        B.plan_compute(qo, kv, last, hq, hk, 16, False, 4, head_dim=d)
+    assert ei.value.status == expect
+
+
+def test_tensor_core_path_page_size_rule(lib):
+    qo = np.array([0, 100]); kv = np.array([0, 100]); last = np.array([1])
+    with pytest.raises(B.FiError) as ei:
+        B.plan_compute(qo, kv, last, 8, 2, 1, True, 4)   # 400 rows, page size 1: not tiled by TMA boxes
+    assert ei.value.status == 3

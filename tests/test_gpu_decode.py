@@ -1,0 +1,156 @@
+"""GPU parity of the CUDA-core decode path against the float64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from serving_attention_plan_gb300 import workloads as W
+
+from .gpu_helpers import alloc_out, assert_close, run_library, to_device, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from serving_attention_plan_gb300 import build
+    build.build()
+    torch = torch_mod()
+    assert torch.cuda.is_available()
+
+
+def test_tiny_decode_full():
+    b = W.tiny_decode()
+    o, lse, _ = run_library(b)
+    ro, rl = A.batch_attention(b)
+    assert_close(o, lse, ro, rl)
+
+
+CASES = [
+    # (hq, hk, page_size, q_len range, kv range, causal, num_ctas)
+    (8, 2, 16, (1, 1), (0, 700), False, 0),
+    (8, 2, 16, (1, 1), (0, 700), False, 3),      # few CTAs: long rows split and merged in-kernel
+    (32, 8, 16, (0, 1), (0, 300), False, 5),
+    (64, 8, 1, (1, 1), (0, 900), False, 7),      # page size 1, g = 8
+    (4, 4, 3, (1, 1), (1, 200), True, 2),        # g = 1, odd page size
+    (8, 4, 64, (1, 4), (4, 500), True, 4),       # g = 2, up to 4 query tokens (8 rows), causal
+    (8, 8, 5, (1, 2), (2, 333), True, 9),        # g = 1, 2 query tokens
+    (16, 8, 16, (1, 4), (0, 100), False, 1),     # one CTA does everything
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("seed", [0, 1])
+def test_random_decode_parity(case, seed):
+    hq, hk, ps, qr, kr, causal, n_cta = CASES[case]
+    b = W.random_small_batch(1000 * case + seed, batch=17, num_qo_heads=hq, num_kv_heads=hk, page_size=ps,
+                             causal=causal, q_len_range=qr, kv_len_range=kr, extra_pages=7)
+    o, lse, ws = run_library(b, num_ctas=n_cta)
+    assert ws.info()[1] == 0  # CUDA-core path
+    ro, rl = A.batch_attention(b)
+    assert_close(o, lse, ro, rl)
+
+
+def test_llama3_8b_decode_full():
+    b = W.llama3_8b_decode()
+    o, lse, ws = run_library(b)
+    ro, rl = A.batch_attention(b)
+    assert_close(o, lse, ro, rl)
+
+
+def test_skewed_long_decode_sampled():
+    """Full-size skewed batch in the benchmark's launch configuration; oracle on the long request + 5 others."""
+    b = W.skewed_long_decode()
+    o, lse, ws = run_library(b)
+    h = ws.info()
+    assert h[7] == 8  # the 131072-token request is split on each KV head
+    reqs = [0, 1, 17, 40, 63]
+    ro, rl = A.batch_attention(b, requests=reqs)
+    rows = np.array([int(b.qo_indptr[i]) for i in reqs])
+    assert_close(o, lse, ro, rl, rows=rows)
+
+
+def test_bit_identical_reruns():
+    torch = torch_mod()
+    b = W.random_small_batch(77, batch=33, num_qo_heads=64, num_kv_heads=8, page_size=1, causal=False,
+                             kv_len_range=(0, 4000), extra_pages=3)
+    dev = to_device(b)
+    o1, l1, ws = run_library(b, num_ctas=11, dev=dev)
+    for _ in range(3):
+        o2, l2, _ = run_library(b, ws=ws, dev=dev)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2, equal_nan=True)
+    del torch
+
+
+def test_cuda_graph_replay_matches():
+    """A captured fi_run replays bit-identically and serves a later plan of the same path and tile."""
+    torch = torch_mod()
+    from serving_attention_plan_gb300 import binding as B
+    mk = lambda seed: W.random_small_batch(seed, batch=20, num_qo_heads=32, num_kv_heads=8, page_size=16,
+                                           causal=False, kv_len_range=(1, 3000))
+    b, b2 = mk(78), mk(79)
+    pool = max(b.num_pages, b2.num_pages)
+    q1, k1, v1 = to_device(b)
+    q2, k2, v2 = to_device(b2)
+    q = q1.clone()
+    k = torch.zeros((pool,) + tuple(k1.shape[1:]), dtype=k1.dtype, device=k1.device)
+    v = torch.zeros_like(k)
+    k[: k1.shape[0]].copy_(k1)
+    v[: v1.shape[0]].copy_(v1)
+    ws = B.Workspace(64, 64, 8192, 32, 8, 128, 13)   # capacity for both plans
+    o_ref, l_ref, _ = run_library(b, ws=ws, dev=(q, k, v))
+    o, lse = alloc_out(b)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ws.run(q, k, v, o, lse, stream=s)
+    for _ in range(3):
+        o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(o.float().cpu().numpy(), o_ref)
+        assert np.array_equal(lse.cpu().numpy().astype(np.float64), l_ref)
+    ws.plan(b2.qo_indptr, b2.kv_indptr, b2.kv_indices, b2.last_page_len, 16, False)
+    q.copy_(q2)
+    k[: k2.shape[0]].copy_(k2)
+    v[: v2.shape[0]].copy_(v2)
+    torch.cuda.synchronize()
+    o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    ro, rl = A.batch_attention(b2)
+    assert_close(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl)
+
+
+def test_out_of_range_page_rejected_on_host():
+    from serving_attention_plan_gb300 import binding as B
+    b = W.random_small_batch(80, batch=4, num_qo_heads=8, num_kv_heads=2, page_size=16, causal=False,
+                             kv_len_range=(16, 64), extra_pages=0)
+    q, k, v = to_device(b)
+    o, lse = alloc_out(b)
+    ws = B.Workspace(4, 4, 64, 8, 2)
+    ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 16, False)
+    with pytest.raises(B.FiError) as ei:
+        ws.run(q, k[:-1], v[:-1], o, lse)  # the pool view no longer holds the largest page id
+    assert ei.value.status == 1
+
+
+def test_merge_states_kernel():
+    torch = torch_mod()
+    from serving_attention_plan_gb300 import binding as B
+    rng = np.random.default_rng(5)
+    rows, heads = 37, 6
+    oa = rng.standard_normal((rows, heads, 128)).astype(np.float32)
+    ob = rng.standard_normal((rows, heads, 128)).astype(np.float32)
+    la = (rng.standard_normal((rows, heads)) * 20).astype(np.float32)
+    lb = (rng.standard_normal((rows, heads)) * 20).astype(np.float32)
+    la[0, 0] = -np.inf
+    la[1, :] = lb[1, :] = -np.inf
+    dev = lambda x: torch.from_numpy(x).cuda()
+    ta, tb = dev(oa).bfloat16(), dev(ob).bfloat16()
+    o = torch.empty_like(ta)
+    lse = torch.empty((rows, heads), dtype=torch.float32, device="cuda")
+    B.merge_states(ta, dev(la), tb, dev(lb), o, lse)
+    torch.cuda.synchronize()
+    ro, rl = A.merge_states(ta.float().cpu().numpy(), la, tb.float().cpu().numpy(), lb)
+    assert_close(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl)
