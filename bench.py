@@ -274,6 +274,7 @@ def main():
     ap.add_argument("--config", default=PRIMARY)
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--batch", type=int, default=0, help="smaller batch of the decode workload (profiling captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
@@ -295,7 +296,7 @@ def main():
     from serving_attention_plan_gb300 import workloads as W
 
     hbm_peak, bf16_peak, bf16_sus, peak_src = measured_peaks()
-    b = W.by_name(args.config)
+    b = W.llama3_8b_decode(batch=args.batch) if args.batch and args.config == PRIMARY else W.by_name(args.config)
     case = Case(b, torch, dev)
     nbytes = kv_bytes(b)
     abytes = algorithmic_bytes(b)

@@ -64,8 +64,11 @@ typedef struct fi_workspace fi_workspace;
  *   max_total_q     most query tokens one plan may hold (>= 1)
  *   max_kv_pages    most entries kv_indices may hold (>= 1)
  *   num_qo_heads, num_kv_heads, head_dim   fixed for the workspace
- *   num_ctas        persistent grid size; 0 selects the device's SM count
- *                   (App. D.3 / App. E: #CTA = k * #SM, user-selectable)
+ *   num_sms         SM budget of the attention kernels; 0 selects every SM of
+ *                   the device (App. E: the SMs attention may use are given by
+ *                   the user).  Each path runs k persistent CTAs per SM
+ *                   (App. D.3: #CTA = k * #SM): k = 1 for the CUDA-core decode
+ *                   path, k = 2 for the tensor-core path.
  *   out             receives the handle (owned by the caller; release with
  *                   fi_workspace_destroy)
  *
@@ -74,7 +77,7 @@ typedef struct fi_workspace fi_workspace;
  * segments, on the current device.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
  */
 int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int num_qo_heads, int num_kv_heads,
-                        int head_dim, int num_ctas, fi_workspace** out);
+                        int head_dim, int num_sms, fi_workspace** out);
 
 /* Release a workspace (synchronises with its last plan copy first). NULL is a no-op. */
 int fi_workspace_destroy(fi_workspace* ws);
@@ -187,7 +190,8 @@ int fi_plan_info(const fi_workspace* ws, int32_t* header16);
  * fi_plan_compute -- the planner alone, on the host, with no device work.
  *
  * Same inputs and rules as fi_plan (kv_indices is not an input: plans never
- * depend on it), plus the grid size and cost model.  Writes the plan as one
+ * depend on it), plus the SM budget (num_sms, as for fi_workspace_create) and
+ * the cost model.  Writes the plan as one
  * flat int32 array:
  *   header[16] | cta_indptr[num_ctas + 1] | items[n_items][8] (queue order)
  *   | split rows[n_split][8] | slot_to_split_row[n_slots]
@@ -198,10 +202,10 @@ int fi_plan_info(const fi_workspace* ws, int32_t* header16);
  * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY (out too small; out_len is set).
  */
 int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
-                    int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal, int num_ctas,
+                    int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal, int num_sms,
                     int64_t alpha, int64_t beta, int32_t l_min, int32_t* out, int64_t capacity, int64_t* out_len);
 
-/* Number of SMs of the current device (the default #CTA). Errors: CUDA. */
+/* Number of SMs of the current device (the default SM budget). Errors: CUDA. */
 int fi_device_sm_count(int* out);
 
 /* Static text for a status code. */

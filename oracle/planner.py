@@ -20,6 +20,8 @@ the design notes):
     covering all its query tokens, and rows_tile is the smallest of 1, 2, 4, 8
     that fits; otherwise the tensor-core path with 128-row tiles,
     tile_tokens = 128 // g.
+  * #CTA = k * (SM budget), k = 1 on the decode path and 2 on the tensor-core
+    path (核心机制 7, paper App. D.3: #CTA = k x #SM).
   * KV heads count as separate units in the L_kv sum; L_kv is raised to l_min
     (default 256) and rounded up to a whole number of pages.
   * A unit (request, KV head, query tile) sees e keys: l_kv, or under the causal
@@ -48,6 +50,8 @@ PATH_DECODE = 0
 PATH_TENSOR = 1
 TC_ROWS = 128
 DECODE_MAX_ROWS = 8
+DECODE_CTAS_PER_SM = 1
+TC_CTAS_PER_SM = 2
 NOT_CAUSAL_DIAG = 1 << 30
 PLAN_MAGIC = 0x46495031
 HEADER_LEN = 16
@@ -97,7 +101,7 @@ def choose_path(l_q, group: int):
 
 
 def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, page_size: int,
-         causal: bool, num_ctas: int, head_dim: int = 128, alpha: int = 1, beta: int = 1,
+         causal: bool, num_sms: int, head_dim: int = 128, alpha: int = 1, beta: int = 1,
          l_min: int = 256) -> Plan:
     qo = [int(x) for x in qo_indptr]
     kv = [int(x) for x in kv_indptr]
@@ -114,6 +118,7 @@ def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: i
 
     # a2: path and tile
     path, tile_tokens, rows_tile = choose_path(l_q, g)
+    num_ctas = (TC_CTAS_PER_SM if path == PATH_TENSOR else DECODE_CTAS_PER_SM) * num_sms
 
     # a3: KV chunk bound
     total = 0

@@ -93,7 +93,7 @@ def _dptr(t) -> c_void_p:
     return c_void_p(0 if t is None else t.data_ptr())
 
 
-def plan_compute(qo_indptr, kv_indptr, last_page_len, num_qo_heads, num_kv_heads, page_size, causal, num_ctas,
+def plan_compute(qo_indptr, kv_indptr, last_page_len, num_qo_heads, num_kv_heads, page_size, causal, num_sms,
                  head_dim=128, alpha=1, beta=1, l_min=256) -> np.ndarray:
     """The host planner alone (no GPU): returns the flat int32 plan."""
     L = lib()
@@ -101,12 +101,12 @@ def plan_compute(qo_indptr, kv_indptr, last_page_len, num_qo_heads, num_kv_heads
     batch = qo.shape[0] - 1
     n = c_int64(0)
     st = L.fi_plan_compute(_p32(qo), _p32(kv), _p32(last), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                           int(causal), num_ctas, alpha, beta, l_min, None, 0, ctypes.byref(n))
+                           int(causal), num_sms, alpha, beta, l_min, None, 0, ctypes.byref(n))
     if st not in (FI_OK, 2):
         _check(st, "fi_plan_compute")
     out = np.zeros(max(int(n.value), 1), dtype=np.int32)
     st = L.fi_plan_compute(_p32(qo), _p32(kv), _p32(last), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                           int(causal), num_ctas, alpha, beta, l_min, _p32(out), out.shape[0], ctypes.byref(n))
+                           int(causal), num_sms, alpha, beta, l_min, _p32(out), out.shape[0], ctypes.byref(n))
     _check(st, "fi_plan_compute")
     return out[: n.value]
 
@@ -120,10 +120,10 @@ def device_sm_count() -> int:
 class Workspace:
     """Owns one fi_workspace (device + pinned buffers) at fixed capacity."""
 
-    def __init__(self, max_batch, max_total_q, max_kv_pages, num_qo_heads, num_kv_heads, head_dim=128, num_ctas=0):
+    def __init__(self, max_batch, max_total_q, max_kv_pages, num_qo_heads, num_kv_heads, head_dim=128, num_sms=0):
         self._h = c_void_p(0)
         _check(lib().fi_workspace_create(max_batch, max_total_q, max_kv_pages, num_qo_heads, num_kv_heads, head_dim,
-                                         num_ctas, ctypes.byref(self._h)), "fi_workspace_create")
+                                         num_sms, ctypes.byref(self._h)), "fi_workspace_create")
         self.num_qo_heads, self.num_kv_heads, self.head_dim = num_qo_heads, num_kv_heads, head_dim
 
     def close(self):

@@ -42,7 +42,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct fi_workspace {
   int device = 0;
   int max_batch = 0, max_total_q = 0, max_kv_pages = 0;
-  int hqo = 0, hkv = 0, head_dim = 0, num_ctas = 0;
+  int hqo = 0, hkv = 0, head_dim = 0, num_sms = 0, max_ctas = 0;
   int64_t max_items = 0, max_units = 0, max_slots = 0;
   fi::CostModel cost;
 
@@ -58,6 +58,7 @@ struct fi_workspace {
   int32_t header[fi::kHeaderLen] = {0};
   int32_t max_page = -1;
   int64_t plan_nnz = 0;
+  int32_t plan_total_q = 0;
 };
 
 namespace {
@@ -66,7 +67,7 @@ constexpr int kDecodeWarps = 8;   // consumer warps per decode CTA
 constexpr int kDecodeStages = 8;  // 32-token KV stages in flight per CTA
 
 template <int R>
-int launch_decode(const fi_workspace* ws, const fi::DecodeParams& p, cudaStream_t stream) {
+int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
   using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages>;
   auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages>;
   static std::once_flag once;
@@ -75,7 +76,7 @@ int launch_decode(const fi_workspace* ws, const fi::DecodeParams& p, cudaStream_
     attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(decode)");
-  kernel<<<ws->num_ctas, (kDecodeWarps + 1) * 32, sizeof(Smem), stream>>>(p);
+  kernel<<<grid, (kDecodeWarps + 1) * 32, sizeof(Smem), stream>>>(p);
   FI_CUDA(cudaGetLastError());
   return FI_OK;
 }
@@ -108,15 +109,15 @@ int fi_device_sm_count(int* out) {
 }
 
 int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int num_qo_heads, int num_kv_heads,
-                        int head_dim, int num_ctas, fi_workspace** out) {
+                        int head_dim, int num_sms, fi_workspace** out) {
   if (out == nullptr) return FI_ERR_INVALID_ARG;
   *out = nullptr;
-  if (max_batch < 1 || max_total_q < 1 || max_kv_pages < 1 || num_qo_heads < 1 || num_kv_heads < 1 || num_ctas < 0)
+  if (max_batch < 1 || max_total_q < 1 || max_kv_pages < 1 || num_qo_heads < 1 || num_kv_heads < 1 || num_sms < 0)
     return FI_ERR_INVALID_ARG;
   if (head_dim != fi::kHeadDim || num_qo_heads % num_kv_heads != 0) return FI_ERR_UNSUPPORTED;
   int dev = 0;
   FI_CUDA(cudaGetDevice(&dev));
-  if (num_ctas == 0) FI_CUDA(cudaDeviceGetAttribute(&num_ctas, cudaDevAttrMultiProcessorCount, dev));
+  if (num_sms == 0) FI_CUDA(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
 
   fi_workspace* ws = new (std::nothrow) fi_workspace();
   if (ws == nullptr) return FI_ERR_CAPACITY;
@@ -127,10 +128,11 @@ int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int nu
   ws->hqo = num_qo_heads;
   ws->hkv = num_kv_heads;
   ws->head_dim = head_dim;
-  ws->num_ctas = num_ctas;
+  ws->num_sms = num_sms;
+  ws->max_ctas = std::max(fi::kTcCtasPerSm, fi::kDecodeCtasPerSm) * num_sms;
   // App. D.3 bound: partial tiles < 2 * #CTA, hence split rows < #CTA.
-  ws->max_slots = 2 * int64_t(num_ctas);
-  ws->max_units = num_ctas;
+  ws->max_slots = 2 * int64_t(ws->max_ctas);
+  ws->max_units = ws->max_ctas;
   ws->max_items = int64_t(num_kv_heads) * max_total_q + ws->max_slots;
 
   size_t off = 0;
@@ -140,7 +142,7 @@ int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int nu
     return o;
   };
   ws->off_header = seg(sizeof(int32_t) * fi::kHeaderLen);
-  ws->off_cta = seg(sizeof(int32_t) * (num_ctas + 1));
+  ws->off_cta = seg(sizeof(int32_t) * (ws->max_ctas + 1));
   ws->off_items = seg(sizeof(int32_t) * fi::kItemFields * ws->max_items);
   ws->off_units = seg(sizeof(int32_t) * fi::kUnitFields * ws->max_units);
   ws->off_slot_unit = seg(sizeof(int32_t) * ws->max_slots);
@@ -193,7 +195,7 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   if (num_qo_heads != ws->hqo || num_kv_heads != ws->hkv || head_dim != ws->head_dim) return FI_ERR_INVALID_ARG;
   if (batch > ws->max_batch) return FI_ERR_CAPACITY;
   fi::PlanInput in{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                   causal, ws->num_ctas};
+                   causal, ws->num_sms};
   int st = fi::validate_input(in);
   if (st != FI_OK) return st;
   const int64_t nnz = kv_indptr[batch];
@@ -242,6 +244,7 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   std::memcpy(ws->header, plan.header, sizeof(plan.header));
   ws->max_page = max_page;
   ws->plan_nnz = nnz;
+  ws->plan_total_q = qo_indptr[batch];
   ws->has_plan = true;
   return FI_OK;
 }
@@ -286,10 +289,10 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
     p.slot_rows = fi::kTcRows;
     p.scale_log2 = scale_log2;
     switch (h[fi::H_ROWS_TILE]) {
-      case 1: return launch_decode<1>(ws, p, s);
-      case 2: return launch_decode<2>(ws, p, s);
-      case 4: return launch_decode<4>(ws, p, s);
-      case 8: return launch_decode<8>(ws, p, s);
+      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s);
+      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s);
+      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s);
+      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s);
       default: return FI_ERR_UNSUPPORTED;
     }
   }
@@ -315,8 +318,8 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
   a.hkv = ws->hkv;
   a.group = h[fi::H_GROUP];
   a.tile_tokens = h[fi::H_TILE_TOKENS];
-  a.total_q = ws->max_total_q;
-  a.num_ctas = ws->num_ctas;
+  a.total_q = ws->plan_total_q;
+  a.num_ctas = h[fi::H_NUM_CTAS];
   a.scale_log2 = scale_log2;
   return fi::launch_prefill(a, s);
 }

@@ -22,6 +22,8 @@
 //     number of pages;
 //   * a unit sees e keys (under the causal mask: those of its last token) and is
 //     cut into n = ceil(e / L_kv) chunks of cs = pages(ceil(e / n)) tokens;
+//   * #CTA = k * (SM budget) with k = 1 for the decode path and 2 for the
+//     tensor-core path (two CTAs share an SM's tensor memory and tensor pipe);
 //   * item cost = alpha * rows + beta * chunk length;
 //   * sort by cost descending, ties by enumeration order; the queue pops the
 //     least-loaded CTA, ties to the lowest CTA id.
@@ -47,7 +49,7 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int validate_input(const PlanInput& in) {
   if (in.batch < 0 || in.qo_indptr == nullptr || in.kv_indptr == nullptr) return FI_ERR_INVALID_ARG;
   if (in.batch > 0 && in.last_page_len == nullptr) return FI_ERR_INVALID_ARG;
-  if (in.num_qo_heads <= 0 || in.num_kv_heads <= 0 || in.page_size <= 0 || in.num_ctas <= 0)
+  if (in.num_qo_heads <= 0 || in.num_kv_heads <= 0 || in.page_size <= 0 || in.num_sms <= 0)
     return FI_ERR_INVALID_ARG;
   if (in.causal != 0 && in.causal != 1) return FI_ERR_INVALID_ARG;
   if (in.head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
@@ -98,11 +100,12 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
     tile_tokens = kTcRows / g;
     rows_tile = kTcRows;
   }
+  const int num_ctas = (path == kPathTensor ? kTcCtasPerSm : kDecodeCtasPerSm) * in.num_sms;
 
   // a3: KV chunk bound
   int64_t total = 0;
   for (int i = 0; i < B; ++i) total += int64_t(in.num_kv_heads) * ceil_div(lq[i], tile_tokens) * lkv[i];
-  int64_t l_chunk = std::max<int64_t>(ceil_div(total, in.num_ctas), cm.l_min);
+  int64_t l_chunk = std::max<int64_t>(ceil_div(total, num_ctas), cm.l_min);
   l_chunk = ceil_div(l_chunk, ps) * ps;
   if (l_chunk > (int64_t(1) << 30)) return FI_ERR_UNSUPPORTED;
 
@@ -170,10 +173,10 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
   std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return work[a].cost > work[b].cost; });
   using Entry = std::pair<int64_t, int32_t>;
   std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> queue;
-  for (int32_t c = 0; c < in.num_ctas; ++c) queue.push({0, c});
+  for (int32_t c = 0; c < num_ctas; ++c) queue.push({0, c});
   std::vector<int32_t> cta_of(W);
-  std::vector<int32_t> count(in.num_ctas, 0);
-  std::vector<int64_t> loads(in.num_ctas, 0);
+  std::vector<int32_t> count(num_ctas, 0);
+  std::vector<int64_t> loads(num_ctas, 0);
   for (int32_t k : order) {
     Entry top = queue.top();
     queue.pop();
@@ -184,8 +187,8 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
     queue.push(top);
   }
 
-  out->cta_indptr.assign(in.num_ctas + 1, 0);
-  for (int c = 0; c < in.num_ctas; ++c) out->cta_indptr[c + 1] = out->cta_indptr[c] + count[c];
+  out->cta_indptr.assign(num_ctas + 1, 0);
+  for (int c = 0; c < num_ctas; ++c) out->cta_indptr[c + 1] = out->cta_indptr[c] + count[c];
   out->items.assign(W * kItemFields, 0);
   std::vector<int32_t> fill(out->cta_indptr.begin(), out->cta_indptr.end() - 1);
   for (int32_t k : order) {
@@ -202,7 +205,7 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
   h[H_TILE_TOKENS] = tile_tokens;
   h[H_ROWS_TILE] = rows_tile;
   h[H_GROUP] = g;
-  h[H_NUM_CTAS] = in.num_ctas;
+  h[H_NUM_CTAS] = num_ctas;
   h[H_NUM_ITEMS] = static_cast<int32_t>(W);
   h[H_NUM_UNITS] = static_cast<int32_t>(out->units.size() / kUnitFields);
   h[H_NUM_SLOTS] = static_cast<int32_t>(out->slot_unit.size());
@@ -220,11 +223,11 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
 
 extern "C" int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* last_page_len,
                                int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal,
-                               int num_ctas, int64_t alpha, int64_t beta, int32_t l_min, int32_t* out,
+                               int num_sms, int64_t alpha, int64_t beta, int32_t l_min, int32_t* out,
                                int64_t capacity, int64_t* out_len) {
   if (out_len == nullptr) return FI_ERR_INVALID_ARG;
   fi::PlanInput in{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                   causal, num_ctas};
+                   causal, num_sms};
   fi::CostModel cm;
   cm.alpha = alpha;
   cm.beta = beta;

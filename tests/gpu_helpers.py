@@ -25,13 +25,13 @@ def alloc_out(b):
     return o, lse
 
 
-def run_library(b, num_ctas=0, ws=None, dev=None, out=None):
+def run_library(b, num_sms=0, ws=None, dev=None, out=None):
     """Plan + run through the C ABI; returns (o, lse) as float64 numpy plus the workspace."""
     from serving_attention_plan_gb300 import binding as B
     torch = torch_mod()
     if ws is None:
         ws = B.Workspace(b.batch_size, max(b.total_q, 1), max(int(b.kv_indptr[-1]), 1), b.num_qo_heads,
-                         b.num_kv_heads, b.head_dim, num_ctas)
+                         b.num_kv_heads, b.head_dim, num_sms)
     q, k, v = dev if dev is not None else to_device(b)
     o, lse = out if out is not None else alloc_out(b)
     ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.page_size, b.causal)

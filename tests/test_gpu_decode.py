@@ -44,7 +44,7 @@ def test_random_decode_parity(case, seed):
     hq, hk, ps, qr, kr, causal, n_cta = CASES[case]
     b = W.random_small_batch(1000 * case + seed, batch=17, num_qo_heads=hq, num_kv_heads=hk, page_size=ps,
                              causal=causal, q_len_range=qr, kv_len_range=kr, extra_pages=7)
-    o, lse, ws = run_library(b, num_ctas=n_cta)
+    o, lse, ws = run_library(b, num_sms=n_cta)
     assert ws.info()[1] == 0  # CUDA-core path
     ro, rl = A.batch_attention(b)
     assert_close(o, lse, ro, rl)
@@ -74,7 +74,7 @@ def test_bit_identical_reruns():
     b = W.random_small_batch(77, batch=33, num_qo_heads=64, num_kv_heads=8, page_size=1, causal=False,
                              kv_len_range=(0, 4000), extra_pages=3)
     dev = to_device(b)
-    o1, l1, ws = run_library(b, num_ctas=11, dev=dev)
+    o1, l1, ws = run_library(b, num_sms=11, dev=dev)
     for _ in range(3):
         o2, l2, _ = run_library(b, ws=ws, dev=dev)
         assert np.array_equal(o1, o2) and np.array_equal(l1, l2, equal_nan=True)

@@ -67,7 +67,8 @@ def test_coverage_and_bounds(seed):
         assert p.path == P.PATH_TENSOR and p.tile_tokens * g <= 128 and p.rows_tile == 128
     # chunk bound: a whole number of pages, at least l_min and at least total / #CTA
     total = sum(c["hk"] * -(-int(lq[i]) // p.tile_tokens) * int(lk[i]) for i in range(len(lq)))
-    assert p.l_kv_chunk % c["ps"] == 0 and p.l_kv_chunk >= 256 and p.l_kv_chunk * c["n_cta"] >= total
+    assert p.num_ctas == c["n_cta"] * (2 if p.path == P.PATH_TENSOR else 1)
+    assert p.l_kv_chunk % c["ps"] == 0 and p.l_kv_chunk >= 256 and p.l_kv_chunk * p.num_ctas >= total
     # every (request, kv head, tile) covers its visible keys exactly once with contiguous chunks
     by_unit = {}
     for it in p.items:
@@ -104,7 +105,7 @@ def test_coverage_and_bounds(seed):
                         assert chunks[0]["diag"] + (t - j * p.tile_tokens) == lk[i] - lq[i] + t
     assert sum(1 for _ in by_unit) == n_units
     # partial-output bound (App. D.3): partial tiles < 2 * #CTA
-    assert len(p.slot_unit) < 2 * c["n_cta"] or len(p.slot_unit) == 0
+    assert len(p.slot_unit) < 2 * p.num_ctas or len(p.slot_unit) == 0
     # each item exactly once; queues in non-increasing cost (longest first)
     seen = sorted(k for q in p.queues for k in q)
     assert seen == list(range(len(p.items)))
@@ -114,7 +115,7 @@ def test_coverage_and_bounds(seed):
     # list-scheduling bound: makespan <= sum/m + (1 - 1/m) * max cost
     costs = [it["cost"] for it in p.items]
     if costs:
-        assert max(p.loads) <= sum(costs) / c["n_cta"] + (1 - 1 / c["n_cta"]) * max(costs) + 1e-9
+        assert max(p.loads) <= sum(costs) / p.num_ctas + (1 - 1 / p.num_ctas) * max(costs) + 1e-9
     assert sum(p.loads) == sum(costs)
 
 
