@@ -205,6 +205,38 @@ int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const in
                     int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal, int num_sms,
                     int64_t alpha, int64_t beta, int32_t l_min, int32_t* out, int64_t capacity, int64_t* out_len);
 
+/*
+ * fi_decode_noalloc -- the CUDA-core decode path without any allocation.
+ *
+ * The paper has no counterpart to this call; it exists for callers that
+ * cannot allocate device memory or let a library do so (for example a serving
+ * runtime that hands the whole GPU to its own memory pool up front, or a
+ * plugin host whose allocator the library must not touch).  It plans and runs
+ * one batch like fi_plan + fi_run, but needs no workspace: its plan, page-index
+ * copy, split counters and partial slots live in one file-scope device array
+ * of FI_NOALLOC_SCRATCH_BYTES (4 MiB) that every GPU loading the library holds
+ * until the process exits, and the plan is built in static host storage.  It
+ * calls no cudaMalloc, cudaFree, cudaHostAlloc or other allocating routine.
+ *
+ *   index arrays   HOST int32, as for fi_plan (copied; free on return)
+ *   q, k_pages, v_pages, o, lse   DEVICE, as for fi_run
+ *   stream         the plan copy, the counter reset and the kernel run on it
+ *
+ * All calls share the array: calls that overlap on the GPU (different streams
+ * without ordering) race; host calls are serialised.  The array keeps the last
+ * call's contents, so each call clears its split counters and error word.
+ * The first call on a device looks up the array's device address and sets the
+ * kernel attribute (with that device current); make it before any stream
+ * capture.  Errors: INVALID_ARG, CAPACITY (plan + page indices + slots do not
+ * fit in the array), UNSUPPORTED (the batch needs tensor-core tiles, i.e. some
+ * request has more than 8 rows = query tokens x group size), CUDA.
+ */
+#define FI_NOALLOC_SCRATCH_BYTES (4u << 20)
+int fi_decode_noalloc(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+                      const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                      int page_size, int causal, const void* q, const void* k_pages, const void* v_pages,
+                      int num_pages, void* o, float* lse, void* stream);
+
 /* Number of SMs of the current device (the default SM budget). Errors: CUDA. */
 int fi_device_sm_count(int* out);
 

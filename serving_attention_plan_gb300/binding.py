@@ -54,13 +54,16 @@ def lib() -> ctypes.CDLL:
     L.fi_plan_info.argtypes = [c_void_p, P32]
     L.fi_plan_compute.argtypes = [P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_int64,
                                   c_int32, P32, c_int64, POINTER(c_int64)]
+    L.fi_decode_noalloc.argtypes = [P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                                    c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     L.fi_device_sm_count.argtypes = [POINTER(c_int)]
     L.fi_status_string.argtypes = [c_int]
     L.fi_status_string.restype = ctypes.c_char_p
     L.fi_last_error_message.argtypes = []
     L.fi_last_error_message.restype = ctypes.c_char_p
     for name in ("fi_workspace_create", "fi_workspace_destroy", "fi_workspace_set_cost_model", "fi_plan", "fi_run",
-                 "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count"):
+                 "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count",
+                 "fi_decode_noalloc"):
         getattr(L, name).restype = c_int
     _LIB = L
     return L
@@ -164,6 +167,18 @@ class Workspace:
     @property
     def handle(self) -> int:
         return self._h.value
+
+
+def decode_noalloc(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads, page_size, causal,
+                   q, k_pages, v_pages, o, lse, stream=None, head_dim=128):
+    """Plan and run one decode batch with no workspace (the library's static scratch array)."""
+    qo, kv, idx, last = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)
+    if idx.size == 0:
+        idx = np.zeros(1, np.int32)
+    _check(lib().fi_decode_noalloc(_p32(qo), _p32(kv), _p32(idx), _p32(last), qo.shape[0] - 1, num_qo_heads,
+                                   num_kv_heads, head_dim, page_size, int(causal), _dptr(q), _dptr(k_pages),
+                                   _dptr(v_pages), int(k_pages.shape[0]), _dptr(o), _dptr(lse), _stream_ptr(stream)),
+           "fi_decode_noalloc")
 
 
 def merge_states(o_a, lse_a, o_b, lse_b, o, lse, stream=None):
