@@ -296,7 +296,12 @@ def main():
     from serving_attention_plan_gb300 import workloads as W
 
     hbm_peak, bf16_peak, bf16_sus, peak_src = measured_peaks()
-    b = W.llama3_8b_decode(batch=args.batch) if args.batch and args.config == PRIMARY else W.by_name(args.config)
+    if args.batch and args.config == PRIMARY:
+        b = W.llama3_8b_decode(batch=args.batch)
+    elif args.batch and args.config == "ragged_causal_prefill":
+        b = W.ragged_causal_prefill(batch=args.batch)
+    else:
+        b = W.by_name(args.config)
     case = Case(b, torch, dev)
     nbytes = kv_bytes(b)
     abytes = algorithmic_bytes(b)
@@ -308,6 +313,8 @@ def main():
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
+    hdr = case.ws.info()
+    kernel_name = f"decode_kernel<R={int(hdr[3])}>" if hdr[1] == 0 else "prefill_kernel"
     value = world * nbytes / (ms * 1e-3) / 1e9
     achieved = abytes / (ms * 1e-3) / 1e9
 
@@ -334,7 +341,6 @@ def main():
     for _ in range(e2e_steps):
         e2e_step()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    hdr = case.ws.info()
     plan_bytes = 4 * (16 + int(hdr[5]) + 1 + 8 * int(hdr[6]) + 8 * int(hdr[7]) + int(hdr[8]) + int(b.kv_indptr[-1]))
     h2d = int(b.q.nbytes) + plan_bytes
     d2h = int(o_host.numel() * 2 + lse_host.numel() * 4)
@@ -361,7 +367,7 @@ def main():
         "frac_of_hbm_peak": value / world / hbm_peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_src} hbm_gbs (burst copy)",
-                     "traffic": ncu_traffic(f"decode_kernel/{args.config}"), "kernel": "decode_kernel<4,8,8>",
+                     "traffic": ncu_traffic(f"{kernel_name}/{args.config}"), "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": abytes},
         "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},

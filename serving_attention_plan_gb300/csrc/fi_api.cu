@@ -63,11 +63,19 @@ struct fi_workspace {
 
 namespace {
 
-constexpr int kDecodeWarps = 8;   // consumer warps per decode CTA
-constexpr int kDecodeStages = 8;  // 32-token KV stages in flight per CTA
+// Consumer warps and ring depth of the decode CTA per tile height R.  The ring
+// holds more 32-token stages than there are consumers, so that while every
+// consumer works on one stage the others are still in flight from HBM.
+template <int R>
+struct DecodeConfig {
+  static constexpr int kWarps = R >= 8 ? 6 : 4;
+  static constexpr int kStages = R >= 8 ? 10 : 12;
+};
 
 template <int R>
 int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
+  constexpr int kDecodeWarps = DecodeConfig<R>::kWarps;
+  constexpr int kDecodeStages = DecodeConfig<R>::kStages;
   using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages>;
   auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages>;
   static std::once_flag once;

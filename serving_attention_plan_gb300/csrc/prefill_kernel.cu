@@ -1,9 +1,567 @@
-// Tensor-core tile path (placeholder until the tcgen05 kernel lands).
+// Tensor-core tile path: paged-KV attention for 128-row tiles on tcgen05, fused
+// with the merge of split-KV partial states.
+//
+// Page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎":
+//   核心机制 3-4 (paper §3.2, §3.2.2): query tiles of >= 16 rows run on tensor
+//     cores; scattered KV tiles are gathered into contiguous shared memory
+//     first.  Here the gather is done by TMA: each page of a 128-key tile is one
+//     3-D tensor box (page-head, token in page, dim) landing in a 128-byte
+//     swizzled shared-memory tile (the TMA sparse gather the paper leaves as
+//     future work, 核心机制 8 / App. B).  GQA heads fold into the rows
+//     (术语与记号 "GQA 头组融合", App. A): a tile is 128/g tokens x g heads.
+//   实验与指标 (paper §4.2): causal prefill with the mask aligned to the end of
+//     each request's KV.
+//   核心机制 6-7 (paper §3.3.1, App. D): persistent CTAs walk the plan's queues;
+//     split rows are merged in-kernel by the last chunk to finish, in plan order.
+//
+// CTA = 6 warps, two CTAs per SM (each holds 256 of the SM's 512 TMEM columns):
+//   warps 0-3  softmax + epilogue; thread t owns row t = TMEM lane t
+//   warp 4     TMA producer (Q per item, K and V per 128-key tile)
+//   warp 5     TMEM allocation and MMA issue (one thread)
+// TMEM: S = Q K^T in columns [0,128) (fp32), overwritten in place by P (bf16
+// pairs, columns [0,64)); O accumulates in columns [128,256).
+// Online softmax in base 2 with a lazy rescale: O and l are rescaled only when
+// a row's running maximum grows by more than 8 (a factor 256), which keeps
+// exp2 arguments <= 8 and leaves the result unchanged up to rounding.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
 #include "../../include/fi.h"
+#include "device_common.cuh"
+#include "plan.h"
 #include "prefill_launch.h"
+#include "tcgen05.cuh"
 
 namespace fi {
+namespace {
 
-int launch_prefill(const PrefillArgs&, cudaStream_t) { return FI_ERR_UNSUPPORTED; }
+constexpr int kTile = 128;                  // rows of a Q tile, keys of a KV tile
+constexpr int kHalfBytes = kTile * 128;     // one 64-dim half of a 128-row bf16 tile (16 KB)
+constexpr int kTileBytes = 2 * kHalfBytes;  // full 128 x 128 bf16 tile
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 128;
+constexpr float kRescaleThreshold = 8.0f;
+
+struct PrefillParams {
+  const int32_t* cta_indptr;
+  const int32_t* items;
+  const int32_t* units;
+  const int32_t* slot_unit;
+  const int32_t* kv_indices;
+  __nv_bfloat16* o;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  uint32_t* counters;
+  int32_t* err;
+  int num_pages;
+  int page_size;
+  int hqo;
+  int hkv;
+  int group;
+  int slot_rows;
+  uint32_t q_tile_bytes;  // bytes of one Q tile as TMA writes it (2 halves x rows x 128 B)
+  float scale_log2;
+};
+
+struct PrefillSmem {
+  uint8_t q[kTileBytes];  // [2 halves][128 rows][128 B], 128B-swizzled
+  uint8_t k[kTileBytes];
+  uint8_t v[kTileBytes];
+  uint64_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, o_free;
+  uint32_t tmem_base;
+  int flag;
+  int abort;
+};
+
+struct Item {
+  int page_base, q_start, q_len, kv_head, kv_lo, kv_hi, diag, slot;
+  __device__ __forceinline__ void load(const int32_t* items, int pos) {
+    const int4 a = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields));
+    const int4 b = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields + 4));
+    page_base = a.x;
+    q_start = a.y;
+    q_len = a.z;
+    kv_head = a.w;
+    kv_lo = b.x;
+    kv_hi = b.y;
+    diag = b.z;
+    slot = b.w;
+  }
+  __device__ __forceinline__ int tiles() const { return (kv_hi - kv_lo + kTile - 1) / kTile; }
+};
+
+// ---------------------------------------------------------------------------------------------
+// warp 4: TMA producer
+// ---------------------------------------------------------------------------------------------
+__device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                         const CUtensorMap* tm_v, int begin, int end) {
+  const int lane = threadIdx.x & 31;
+  const int ps = p.page_size;
+  const int ppt = kTile / ps;  // pages per KV tile (<= 16)
+  const int oob_page = p.num_pages * p.hkv;
+  int tt = 0, nq = 0;
+  bool ok = true;
+  for (int pos = begin; pos < end && ok; ++pos) {
+    Item it;
+    it.load(p.items, pos);
+    const int n_tiles = it.tiles();
+    if (n_tiles == 0) continue;
+    if (nq > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_empty, (nq - 1) & 1, p.err, &sm.abort));
+    if (!ok) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&sm.q_full, p.q_tile_bytes);
+      tc::tma_load_3d(sm.q, tm_q, 0, it.kv_head * p.group, it.q_start, &sm.q_full);
+      tc::tma_load_3d(sm.q + kHalfBytes, tm_q, 64, it.kv_head * p.group, it.q_start, &sm.q_full);
+    }
+    for (int t = 0; t < n_tiles; ++t) {
+      const int base = it.kv_lo + t * kTile;
+      int z = oob_page;  // out-of-range page-head coordinate: the box reads as zeros
+      if (lane < ppt) {
+        const int pp = base / ps + lane;
+        if (pp * ps < it.kv_hi) {
+          const int page = __ldg(p.kv_indices + it.page_base + pp);
+          if (page >= 0 && page < p.num_pages) {
+            z = page * p.hkv + it.kv_head;
+          } else {
+            atomicOr(p.err, FI_DEVERR_PAGE_OOB);
+          }
+        }
+      }
+      if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_empty, (tt - 1) & 1, p.err, &sm.abort));
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
+      __syncwarp();
+      if (lane < ppt) {
+        tc::tma_load_3d(sm.k + lane * ps * 128, tm_k, 0, 0, z, &sm.k_full);
+        tc::tma_load_3d(sm.k + kHalfBytes + lane * ps * 128, tm_k, 64, 0, z, &sm.k_full);
+      }
+      if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_empty, (tt - 1) & 1, p.err, &sm.abort));
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
+      __syncwarp();
+      if (lane < ppt) {
+        tc::tma_load_3d(sm.v + lane * ps * 128, tm_v, 0, 0, z, &sm.v_full);
+        tc::tma_load_3d(sm.v + kHalfBytes + lane * ps * 128, tm_v, 64, 0, z, &sm.v_full);
+      }
+      ++tt;
+    }
+    ++nq;
+  }
+  // never leave with tensor copies still landing in this CTA's shared memory
+  if (nq > 0) mbar_wait_bounded(&sm.q_full, (nq - 1) & 1);
+  if (tt > 0) {
+    mbar_wait_bounded(&sm.k_full, (tt - 1) & 1);
+    mbar_wait_bounded(&sm.v_full, (tt - 1) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// warp 5, one thread: MMA issue
+// ---------------------------------------------------------------------------------------------
+__device__ void mma_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kTile, 0, 0);  // A = Q (K-major), B = K (K-major)
+  constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P (TMEM), B = V (MN-major)
+  const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v);
+  int tt = 0, nq = 0;
+  for (int pos = begin; pos < end; ++pos) {
+    Item it;
+    it.load(p.items, pos);
+    const int n_tiles = it.tiles();
+    if (n_tiles == 0) continue;
+    if (!mbar_wait(&sm.q_full, nq & 1, p.err, &sm.abort)) return;
+    for (int t = 0; t < n_tiles; ++t) {
+      if (!mbar_wait(&sm.k_full, tt & 1, p.err, &sm.abort)) return;
+      if (tt > 0 && !mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort)) return;  // S/P columns free
+      tc::fence_after_sync();
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          // K-major, 128B swizzle: a 16-element k step is 32 B inside the 128-B row; 8-row groups 1024 B apart
+          const uint64_t a = tc::smem_desc(q_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
+          const uint64_t b = tc::smem_desc(k_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
+          tc::mma_ss(tmem + kColS, a, b, idesc_qk, (kh | ks) != 0 ? 1u : 0u);
+        }
+      }
+      tc::commit(&sm.s_full);
+      tc::commit(&sm.k_empty);
+      if (t == n_tiles - 1) tc::commit(&sm.q_empty);
+      if (!mbar_wait(&sm.p_full, tt & 1, p.err, &sm.abort)) return;
+      if (!mbar_wait(&sm.v_full, tt & 1, p.err, &sm.abort)) return;
+      if (t == 0 && nq > 0 && !mbar_wait(&sm.o_free, (nq - 1) & 1, p.err, &sm.abort)) return;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        // V as B (K = keys, N = dims), MN-major 128B swizzle: a 16-key step is two 8-row
+        // groups (2048 B); the second 64-dim half is the leading-dimension step (16 KB)
+        const uint64_t b = tc::smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, tc::kLayoutSw128);
+        tc::mma_ts(tmem + kColO, tmem + kColS + ks * 8, b, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+      }
+      tc::commit(&sm.o_done);
+      tc::commit(&sm.v_empty);
+      ++tt;
+    }
+    ++nq;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// warps 0-3: softmax, epilogue and the merge of split rows
+// ---------------------------------------------------------------------------------------------
+
+// Output row of (token, head) for tile row `row`.
+__device__ __forceinline__ size_t out_row(const PrefillParams& p, const Item& it, int row) {
+  return (size_t)(it.q_start + row / p.group) * p.hqo + it.kv_head * p.group + row % p.group;
+}
+
+// 32 normalised output values (dims 32*c .. 32*c+31) of one row -> bf16.
+__device__ __forceinline__ void write_chunk_bf16(__nv_bfloat16* dst_row, int c, const float (&v)[32]) {
+  uint4* dst = reinterpret_cast<uint4*>(dst_row + 32 * c);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = f2_to_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+    w.y = f2_to_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+    w.z = f2_to_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+    w.w = f2_to_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    dst[q] = w;
+  }
+}
+
+__device__ __forceinline__ float lse_out(float lse2) { return (lse2 == -INFINITY) ? -INFINITY : lse2 * kLn2; }
+
+__device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  const int row = threadIdx.x;  // 0..127 == TMEM lane
+  const int warp = row >> 5;
+  const int lane = row & 31;
+  const uint32_t t_lane = tmem + (uint32_t(warp * 32) << 16);
+  const float scale = p.scale_log2;
+  int tt = 0;
+  bool alive = true;
+  for (int pos = begin; pos < end; ++pos) {
+    Item it;
+    it.load(p.items, pos);
+    const int n_tiles = it.tiles();
+    const int rows_valid = it.q_len * p.group;
+    const int u = row / p.group;
+    float m = -INFINITY, l = 0.f;
+
+    for (int t = 0; t < n_tiles; ++t) {
+      const int base = it.kv_lo + t * kTile;
+      const int lim = max(0, min(kTile, min(it.kv_hi - base, it.diag + u + 1 - base)));
+      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.s_full, tt & 1, p.err, &sm.abort));
+      if (alive) {
+        tc::fence_after_sync();
+        uint32_t s[kTile];
+        tc::tmem_ld32(t_lane + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+        tc::tmem_ld32(t_lane + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+        tc::tmem_ld32(t_lane + kColS + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
+        tc::tmem_ld32(t_lane + kColS + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
+        tc::tmem_wait_ld();
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kTile; ++j) {
+          const float x = (j < lim) ? __uint_as_float(s[j]) * scale : -INFINITY;
+          s[j] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m, mx);
+        float alpha = 1.f;
+        bool need = false;
+        if (t == 0) {
+          m = m_new;
+        } else {
+          need = m_new > m + kRescaleThreshold;  // also true when m = -inf and m_new is finite
+          if (need) {
+            alpha = fast_exp2(m - m_new);
+            l *= alpha;
+            m = m_new;
+          }
+        }
+        const float m_use = (m == -INFINITY) ? 0.f : m;
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kTile / 2; ++j) {
+          const float p0 = fast_exp2(__uint_as_float(s[2 * j]) - m_use);
+          const float p1 = fast_exp2(__uint_as_float(s[2 * j + 1]) - m_use);
+          sum += p0 + p1;
+          s[j] = f2_to_bf16x2(p0, p1);  // P overwrites the front of S in place
+        }
+        l += sum;
+        tc::tmem_st32(t_lane + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+        tc::tmem_st32(t_lane + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+        tc::tmem_wait_st();
+        if (__any_sync(0xffffffffu, need)) {
+          // O was last written by the previous tile's P.V: wait for it, then rescale in place
+          alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort));
+          tc::fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(t_lane + kColO + 32 * c, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tc::tmem_st32(t_lane + kColO + 32 * c, o);
+          }
+          tc::tmem_wait_st();
+        }
+        tc::fence_before_sync();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_full);
+      ++tt;
+    }
+
+    // ---- epilogue: O / l and LSE, to the output or to a partial slot --------------------------
+    float lse2 = -INFINITY, inv = 0.f;
+    if (l > 0.f) {
+      lse2 = m + fast_log2(l);
+      inv = 1.f / l;
+    }
+    if (n_tiles > 0) {
+      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort));
+      tc::fence_after_sync();
+    }
+    if (it.slot < 0) {
+      __nv_bfloat16* dst = p.o + out_row(p, it, row) * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        if (n_tiles > 0 && alive) {
+          uint32_t o[32];
+          tc::tmem_ld32(t_lane + kColO + 32 * c, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) * inv;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        if (row < rows_valid) write_chunk_bf16(dst, c, v);
+      }
+      if (row < rows_valid) p.lse[out_row(p, it, row)] = lse_out(lse2);
+    } else {
+      const size_t srow = (size_t)it.slot * p.slot_rows + row;
+      float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kHeadDim);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        if (alive) {
+          tc::tmem_ld32(t_lane + kColO + 32 * c, o);
+          tc::tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+        if (row < rows_valid) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[8 * c + j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                         __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        }
+      }
+      if (row < rows_valid) p.part_lse[srow] = lse2;
+    }
+    if (n_tiles > 0) {
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_free);
+    }
+
+    if (it.slot >= 0) {
+      // contraction of a split row: the last chunk to finish merges all slots in plan order
+      named_bar_sync(1, 128);
+      const int unit = __ldg(p.slot_unit + it.slot);
+      if (row == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(p.counters + unit, 1u);
+        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+        sm.flag = (prev == uint32_t(n_chunks - 1)) ? 1 : 0;
+        if (sm.flag) __threadfence();
+      }
+      named_bar_sync(1, 128);
+      if (sm.flag) {
+        const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
+        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+        if (row < rows_valid) {
+          float M = -INFINITY;
+          for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row));
+          float L = 0.f;
+          if (M != -INFINITY) {
+            for (int c = 0; c < n_chunks; ++c) L += fast_exp2(__ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row) - M);
+          }
+          const float invL = (M != -INFINITY) ? 1.f / L : 0.f;
+          __nv_bfloat16* dst = p.o + out_row(p, it, row) * kHeadDim;
+          for (int dc = 0; dc < 4; ++dc) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            if (M != -INFINITY) {
+              for (int c = 0; c < n_chunks; ++c) {
+                const size_t srow = (size_t)(first + c) * p.slot_rows + row;
+                const float w = fast_exp2(__ldcg(p.part_lse + srow) - M) * invL;
+                const float4* src = reinterpret_cast<const float4*>(p.part_o + srow * kHeadDim + 32 * dc);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 a = __ldcg(src + j);
+                  v[4 * j] += w * a.x;
+                  v[4 * j + 1] += w * a.y;
+                  v[4 * j + 2] += w * a.z;
+                  v[4 * j + 3] += w * a.w;
+                }
+              }
+            }
+            write_chunk_bf16(dst, dc, v);
+          }
+          p.lse[out_row(p, it, row)] = lse_out(M == -INFINITY ? -INFINITY : M + fast_log2(L));
+        }
+        if (row == 0) p.counters[unit] = 0u;
+      }
+      named_bar_sync(1, 128);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+  extern __shared__ unsigned char smem_raw[];
+  // 128B-swizzled tiles want 1024-byte alignment
+  PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.k_full, 1);
+    mbar_init(&sm.k_empty, 1);
+    mbar_init(&sm.v_full, 1);
+    mbar_init(&sm.v_empty, 1);
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 4);
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.o_free, 4);
+    sm.flag = 0;
+    sm.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4 && (threadIdx.x & 31) == 0) {
+    tc::tma_prefetch_desc(&tm_q);
+    tc::tma_prefetch_desc(&tm_k);
+    tc::tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+  const int begin = __ldg(p.cta_indptr + blockIdx.x);
+  const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
+  if ((tmem & 0xFFFFu) + kTmemCols > 512u) {  // not an address this CTA can use: report, do nothing
+    if (threadIdx.x == 0) atomicOr(p.err, FI_DEVERR_TMEM);
+  } else if (warp < 4) {
+    softmax_epilogue(p, sm, tmem, begin, end);
+  } else if (warp == 4) {
+    producer(p, sm, &tm_q, &tm_k, &tm_v, begin, end);
+  } else if ((threadIdx.x & 31) == 0) {
+    mma_issuer(p, sm, tmem, begin, end);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+              uint64_t stride2_bytes, uint32_t box1, uint32_t box2) {
+  const cuuint64_t dims[3] = {uint64_t(kHeadDim), d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {64u, box1, box2};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  if (encode_fn() == nullptr) return FI_ERR_CUDA;
+  if (a.page_size % 8 != 0 || kTile % a.page_size != 0 || a.group > kTile || a.group * a.tile_tokens > kTile)
+    return FI_ERR_UNSUPPORTED;
+  if (a.total_q < 1 || a.num_pages < 1) return FI_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(a.q) % 16 || reinterpret_cast<uintptr_t>(a.k) % 16 ||
+      reinterpret_cast<uintptr_t>(a.v) % 16)
+    return FI_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv;
+  const uint64_t row_bytes = uint64_t(kHeadDim) * 2;
+  // q: (dim, head, token); a box is 64 dims x g heads x (128/g) tokens = up to 128 rows of 128 B
+  if (!make_map(&tq, a.q, uint64_t(a.hqo), uint64_t(a.total_q), row_bytes, row_bytes * a.hqo, uint32_t(a.group),
+                uint32_t(a.tile_tokens)))
+    return FI_ERR_INVALID_ARG;
+  // k, v: (dim, token in page, page * H_kv + head); a box is one page-head half
+  const uint64_t page_heads = uint64_t(a.num_pages) * a.hkv;
+  if (!make_map(&tk, a.k, uint64_t(a.page_size), page_heads, row_bytes, row_bytes * a.page_size,
+                uint32_t(a.page_size), 1u) ||
+      !make_map(&tv, a.v, uint64_t(a.page_size), page_heads, row_bytes, row_bytes * a.page_size,
+                uint32_t(a.page_size), 1u))
+    return FI_ERR_INVALID_ARG;
+
+  PrefillParams p;
+  p.cta_indptr = a.cta_indptr;
+  p.items = a.items;
+  p.units = a.units;
+  p.slot_unit = a.slot_unit;
+  p.kv_indices = a.kv_indices;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  p.counters = a.counters;
+  p.err = a.err;
+  p.num_pages = a.num_pages;
+  p.page_size = a.page_size;
+  p.hqo = a.hqo;
+  p.hkv = a.hkv;
+  p.group = a.group;
+  p.slot_rows = kTcRows;
+  p.q_tile_bytes = uint32_t(2 * 128 * a.group * a.tile_tokens);
+  p.scale_log2 = a.scale_log2;
+
+  const size_t smem = sizeof(PrefillSmem) + 1024;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [&] {
+    attr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  });
+  if (attr != cudaSuccess) return FI_ERR_CUDA;
+  prefill_kernel<<<a.num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
+  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
 
 }  // namespace fi
