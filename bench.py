@@ -309,6 +309,9 @@ def main():
     with ClockSampler(local) as clk:
         ms = time_launches(torch, case.run, args.steps, args.warmup, barrier)
     clocks = clk.summary()
+    device_errors = case.ws.get_error()  # a timed-out pipeline wait or a skipped page would show here
+    if device_errors:
+        print(f"bench: device error bits {device_errors:#x} during the timed launches", file=sys.stderr)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -372,6 +375,7 @@ def main():
         "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps,
+        "device_errors": device_errors,
         "clocks": clocks,
         "plan": {"path": int(hdr[1]), "rows_tile": int(hdr[3]), "num_ctas": int(hdr[5]), "items": int(hdr[6]),
                  "split_rows": int(hdr[7]), "l_kv_chunk": int(hdr[9])},
@@ -411,8 +415,9 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
     c = Case(w, torch, dev)
     ms = time_launches(torch, c.run, steps, warmup)
     hdr = c.ws.info()
+    errs = c.ws.get_error()
     out = {"us_per_batch": ms * 1e3, "path": "tensor-core" if hdr[1] == 1 else "cuda-core",
-           "config": workload_config(name, w)}
+           "config": workload_config(name, w), "device_errors": errs}
     if hdr[1] == 1:
         tf = flops(w) / (ms * 1e-3) / 1e12
         out.update({"tflops": tf, "frac_of_bf16_peak": tf / bf16_peak})

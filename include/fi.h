@@ -67,8 +67,7 @@ typedef struct fi_workspace fi_workspace;
  *   num_sms         SM budget of the attention kernels; 0 selects every SM of
  *                   the device (App. E: the SMs attention may use are given by
  *                   the user).  Each path runs k persistent CTAs per SM
- *                   (App. D.3: #CTA = k * #SM): k = 1 for the CUDA-core decode
- *                   path, k = 2 for the tensor-core path.
+ *                   (App. D.3: #CTA = k * #SM); both paths use k = 1.
  *   out             receives the handle (owned by the caller; release with
  *                   fi_workspace_destroy)
  *

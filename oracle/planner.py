@@ -20,8 +20,8 @@ the design notes):
     covering all its query tokens, and rows_tile is the smallest of 1, 2, 4, 8
     that fits; otherwise the tensor-core path with 128-row tiles,
     tile_tokens = 128 // g.
-  * #CTA = k * (SM budget), k = 1 on the decode path and 2 on the tensor-core
-    path (核心机制 7, paper App. D.3: #CTA = k x #SM).
+  * #CTA = k * (SM budget), k fixed per path, here 1 on both paths
+    (核心机制 7, paper App. D.3: #CTA = k x #SM).
   * KV heads count as separate units in the L_kv sum; L_kv is raised to l_min
     (default 256) and rounded up to a whole number of pages.
   * A unit (request, KV head, query tile) sees e keys: l_kv, or under the causal
@@ -51,7 +51,7 @@ PATH_TENSOR = 1
 TC_ROWS = 128
 DECODE_MAX_ROWS = 8
 DECODE_CTAS_PER_SM = 1
-TC_CTAS_PER_SM = 2
+TC_CTAS_PER_SM = 1
 NOT_CAUSAL_DIAG = 1 << 30
 PLAN_MAGIC = 0x46495031
 HEADER_LEN = 16

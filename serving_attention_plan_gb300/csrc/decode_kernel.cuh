@@ -16,8 +16,15 @@
 //     the slots in the plan's fixed order (an arrival counter only counts; it
 //     never accumulates data), so results are bit-identical run to run.
 //
-// CTA layout: warp 0 = producer (page-index prefetch + bulk copies),
-// warps 1..NW = consumers.  Consumer warps take the CTA's KV stages round-robin
+// CTA layout, two loaders selectable per instantiation (kCopiers):
+//   bulk (kCopiers = 0): warp 0 = producer (page-index prefetch + one bulk async copy per
+//           page-head run);
+//   LDGSTS: warp 0 = page-index warp (4-byte cp.async into an index ring), warps 1..kCopiers =
+//           copiers taking stages round-robin (16-byte cp.async of K/V rows, 512 B per warp
+//           instruction); used when the page size is a power of two.  The bulk engine keeps only a few copies in flight per SM, which
+//           caps a page-sized copy stream well below HBM bandwidth; 16-byte copies do not share
+//           that limit.
+// The remaining NW warps are consumers.  Consumer warps take the CTA's KV stages round-robin
 // (stage n -> warp n % NW); each keeps an online-softmax state, and at the end
 // of a work item the NW states are merged through shared memory in warp order.
 //
@@ -53,6 +60,7 @@ struct DecodeParams {
   long long head_stride;  // elements per page-head (page_size * 128)
   int num_pages;
   int page_size;
+  int page_shift;  // log2(page_size) when it is a power of two (LDGSTS loader), else -1
   int hqo;
   int group;
   int slot_rows;
@@ -60,22 +68,31 @@ struct DecodeParams {
 };
 
 constexpr int kStageTokens = 32;
-constexpr int kIdxDepth = 4;  // page-index prefetch distance (stages)
+constexpr int kIdxDepth = 4;  // page-index prefetch distance of the bulk producer (stages)
+constexpr int kIdxSlots = 8;  // page-index ring of the LDGSTS loader (stages)
 constexpr int kRedHalf = 336; // words between the two halves of the transpose scratch
 constexpr int kRedRow = 20;   // words per lane row of the transpose scratch
 
 template <int R, int NW, int S>
 struct DecodeSmem {
   __nv_bfloat16 kv[S][2][kStageTokens][kHeadDim];  // [stage][K|V][token][dim]
-  float red[NW][2 * kRedHalf];
+  float red[NW][2][2 * kRedHalf];  // per consumer warp: double-buffered transpose scratch
   float pbuf[NW][kStageTokens * R];
   float alpha[NW][8];
   float macc[NW][R][kHeadDim];
   float mm[NW][8];
   float ml[NW][8];
-  int32_t idx[kIdxDepth][32];
+  int32_t idx[kIdxSlots][32];
   uint64_t full[S];
   uint64_t empty[S];
+  uint64_t idx_full[kIdxSlots];
+  uint64_t idx_empty[kIdxSlots];
+  // Stage last consumed from / last issued into each ring slot.  Stages are dealt round-robin to
+  // several consumer (and copier) warps, so the next user of a slot may arrive before the slot's
+  // previous phase has completed; a parity wait would then pass on the phase before.  Waiting
+  // first for the slot's previous stage keeps every parity wait unambiguous.
+  int slot_consumed[S];
+  int slot_filled[S];
   int flag;
   int abort;
 };
@@ -186,6 +203,78 @@ __device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSme
   for (int n = max(0, issued - S); n < issued; ++n) mbar_wait_bounded(&sm.full[n % S], (n / S) & 1);
 }
 
+// LDGSTS loader, warp 0: page ids of each stage into a ring of kIdxSlots x 32 entries.
+template <int R, int NW, int S>
+__device__ __forceinline__ void decode_index_warp(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin,
+                                                  int end) {
+  const int lane = threadIdx.x & 31;
+  StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
+  bool ok = c.load(p.items);
+  for (int n = 0; ok; ++n) {
+    const int slot = n % kIdxSlots, fill = n / kIdxSlots;
+    if (fill > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.idx_empty[slot], (fill - 1) & 1, p.err, &sm.abort))) break;
+    const int t0 = c.tok0();
+    const int first = t0 >> p.page_shift;
+    const int nseg = ((t0 + c.ntok() - 1) >> p.page_shift) - first + 1;
+    if (lane < nseg) cp_async_4(&sm.idx[slot][lane], p.kv_indices + c.page_base + first + lane);
+    cp_async_arrive_noinc(&sm.idx_full[slot]);
+    ok = c.next(p.items);
+  }
+  cp_async_wait_all();
+}
+
+// LDGSTS loader, copier warp `cw` of kCopiers: stages cw, cw + kCopiers, ... -- the stage's K and V
+// rows, 16 bytes per lane per instruction.
+// Copy c (0..1023) of a stage: K/V = c / 512, token = (c % 512) / 16, 16-byte chunk = c % 16,
+// so each warp instruction moves two consecutive 256-byte rows.
+template <int R, int NW, int S, int kCopiers>
+__device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin,
+                                                   int end, int cw) {
+  const int lane = threadIdx.x & 31;
+  const int sh = p.page_shift;
+  const int row_mask = p.page_size - 1;
+  StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
+  bool ok = c.load(p.items);
+  for (int k = 0; k < cw && ok; ++k) ok = c.next(p.items);
+  for (int n = cw; ok; n += kCopiers) {
+    const int islot = n % kIdxSlots;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.idx_full[islot], (n / kIdxSlots) & 1, p.err, &sm.abort))) break;
+    const int t0 = c.tok0();
+    const int nt = c.ntok();
+    const int first = t0 >> sh;
+    const int nseg = ((t0 + nt - 1) >> sh) - first + 1;
+    int pg = (lane < nseg) ? sm.idx[islot][lane] : 0;
+    if (lane < nseg && (pg < 0 || pg >= p.num_pages)) {
+      atomicOr(p.err, FI_DEVERR_PAGE_OOB);
+      pg = -1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.idx_empty[islot]);
+    const int slot = n % S, fill = n / S;
+    if (!__all_sync(0xffffffffu, spin_until_eq(&sm.slot_filled[slot], n - S, p.err, &sm.abort))) break;
+    if (fill > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.empty[slot], (fill - 1) & 1, p.err, &sm.abort))) break;
+    const __nv_bfloat16* kb = p.k + (long long)c.kv_head * p.head_stride;
+    const __nv_bfloat16* vb = p.v + (long long)c.kv_head * p.head_stride;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int tok = 2 * j + (lane >> 4);  // same tokens for the K half (j) and the V half (j + 16)
+      const int pos = t0 + tok;
+      const int seg = min(max((pos >> sh) - first, 0), 31);
+      const int page = __shfl_sync(0xffffffffu, pg, seg);
+      if (tok < nt && page >= 0) {
+        const long long off = (long long)page * p.page_stride + (long long)(pos & row_mask) * kHeadDim + (lane & 15) * 8;
+        cp_async_16(&sm.kv[slot][0][tok][(lane & 15) * 8], kb + off);
+        cp_async_16(&sm.kv[slot][1][tok][(lane & 15) * 8], vb + off);
+      }
+    }
+    cp_async_arrive_noinc(&sm.full[slot]);
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<volatile int*>(&sm.slot_filled[slot]) = n;
+    for (int k = 0; k < kCopiers && ok; ++k) ok = c.next(p.items);
+  }
+  cp_async_wait_all();
+}
+
 template <int R>
 __device__ __forceinline__ void load_q_rows(const DecodeParams& p, int q_start, int q_len, int kv_head, int dl,
                                             float2 (&q2)[R][4]) {
@@ -217,7 +306,7 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
   const int tl = lane >> 4, dl = lane & 15;
   const int my_row = dl % R;
   const int ctid = w * 32 + lane;
-  float* red = sm.red[w];
+
   float* pb = sm.pbuf[w];
   int stage_n = 0;
   bool alive = true;
@@ -243,7 +332,8 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
       if (n % NW != w) continue;
       const int slot = n % S;
       if (!alive) continue;
-      const bool got = mbar_wait(&sm.full[slot], (n / S) & 1, p.err, &sm.abort);
+      const bool got = spin_until_eq(&sm.slot_consumed[slot], n - S, p.err, &sm.abort) &&
+                       mbar_wait(&sm.full[slot], (n / S) & 1, p.err, &sm.abort);
       if (!__all_sync(0xffffffffu, got)) {
         alive = false;  // keep joining the named barriers; outputs of an aborted run are undefined
         continue;
@@ -273,14 +363,19 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
             part[u * R + r] = s2.x + s2.y;
           }
         }
+        // two scratch buffers alternate, so one warp barrier per sub-batch suffices and the sum of
+        // this sub-batch can overlap the products of the next
+        float* red = sm.red[w][b & 1];
         float4* rw = reinterpret_cast<float4*>(red + tl * kRedHalf + dl * kRedRow);
 #pragma unroll
         for (int c = 0; c < 4; ++c) rw[c] = make_float4(part[4 * c], part[4 * c + 1], part[4 * c + 2], part[4 * c + 3]);
         __syncwarp();
-        float s = 0.f;
+        float s4[4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) s += red[tl * kRedHalf + j * kRedRow + dl];
-        __syncwarp();
+        for (int j = 0; j < 4; ++j) s4[j] = red[tl * kRedHalf + j * kRedRow + dl];
+#pragma unroll
+        for (int j = 4; j < 16; ++j) s4[j & 3] += red[tl * kRedHalf + j * kRedRow + dl];
+        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const int t = b * 2 * NT + tl * NT + dl / R;
         const bool vis = (t < nt) && (t0 + t <= row_limit);
         sc[b] = vis ? s : -INFINITY;
@@ -316,6 +411,11 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
         acc[r][0] = __fmul2_rn(acc[r][0], make_float2(a, a));
         acc[r][1] = __fmul2_rn(acc[r][1], make_float2(a, a));
       }
+      // tokens alternate between two accumulator sets (when registers allow) to halve the FMA chain
+      constexpr int kSets = R <= 4 ? 2 : 1;
+      float2 acc2[R][2];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc2[r][0] = acc2[r][1] = make_float2(0.f, 0.f);
 #pragma unroll 4
       for (int t = 0; t < nt; ++t) {
         const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * kHeadDim + 4 * lane);
@@ -334,15 +434,34 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
 #pragma unroll
           for (int r = 0; r < R; ++r) pr[r] = pb[t * R + r];
         }
+        if (kSets == 2 && (t & 1)) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float2 pp = make_float2(pr[r], pr[r]);
+            acc2[r][0] = __ffma2_rn(pp, v0, acc2[r][0]);
+            acc2[r][1] = __ffma2_rn(pp, v1, acc2[r][1]);
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float2 pp = make_float2(pr[r], pr[r]);
+            acc[r][0] = __ffma2_rn(pp, v0, acc[r][0]);
+            acc[r][1] = __ffma2_rn(pp, v1, acc[r][1]);
+          }
+        }
+      }
+      if (kSets == 2) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const float2 pp = make_float2(pr[r], pr[r]);
-          acc[r][0] = __ffma2_rn(pp, v0, acc[r][0]);
-          acc[r][1] = __ffma2_rn(pp, v1, acc[r][1]);
+          acc[r][0] = __fadd2_rn(acc[r][0], acc2[r][0]);
+          acc[r][1] = __fadd2_rn(acc[r][1], acc2[r][1]);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      if (lane == 0) {
+        *reinterpret_cast<volatile int*>(&sm.slot_consumed[slot]) = n;
+        mbar_arrive(&sm.empty[slot]);
+      }
     }
     stage_n += nst;
 
@@ -456,15 +575,24 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
   }
 }
 
-template <int R, int NW, int S>
-__global__ void __launch_bounds__((NW + 1) * 32, 1) decode_kernel(const __grid_constant__ DecodeParams p) {
+template <int R, int NW, int S, int kCopiers = 0>
+__global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr bool kLdgsts = kCopiers > 0;
+  constexpr int kLoaders = kLdgsts ? 1 + kCopiers : 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S>*>(smem_raw);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&sm.full[s], 1);
+      sm.slot_consumed[s] = s - S;
+      sm.slot_filled[s] = s - S;
+      mbar_init(&sm.full[s], kLdgsts ? 32 : 1);  // LDGSTS: one arrival per lane of the stage's copier
       mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < kIdxSlots; ++s) {
+      mbar_init(&sm.idx_full[s], 32);
+      mbar_init(&sm.idx_empty[s], 1);
     }
     sm.abort = 0;
     sm.flag = 0;
@@ -473,10 +601,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) decode_kernel(const __grid_c
   __syncthreads();
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
-  if (warp == 0) {
+  if (warp >= kLoaders) {
+    decode_consumer<R, NW, S>(p, sm, begin, end, warp - kLoaders);
+  } else if (!kLdgsts) {
     decode_producer<R, NW, S>(p, sm, begin, end);
+  } else if (warp == 0) {
+    decode_index_warp<R, NW, S>(p, sm, begin, end);
   } else {
-    decode_consumer<R, NW, S>(p, sm, begin, end, warp - 1);
+    decode_copier_warp<R, NW, S, kCopiers>(p, sm, begin, end, warp - 1);
   }
 }
 

@@ -89,6 +89,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return true;
 }
 
+// Bounded wait until a shared-memory word equals `value` (same error / abort contract as mbar_wait).
+__device__ __forceinline__ bool spin_until_eq(const volatile int* word, int value, int32_t* err,
+                                              volatile int* abort_flag) {
+  if (*word == value) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (*word == value) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(err, FI_DEVERR_WAIT_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // One contiguous global -> shared bulk copy, completion counted in bytes on `bar`.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar,
@@ -116,6 +134,15 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 __device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src_gmem) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
 }
+// 16-byte asynchronous copy global -> shared, bypassing L1 (LDGSTS.128).
+__device__ __forceinline__ void cp_async_16(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has landed (no pending-count increment).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

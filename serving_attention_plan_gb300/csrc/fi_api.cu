@@ -39,6 +39,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+int fi::record_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
 struct fi_workspace {
   int device = 0;
   int max_batch = 0, max_total_q = 0, max_kv_pages = 0;
@@ -63,30 +65,40 @@ struct fi_workspace {
 
 namespace {
 
-// Consumer warps and ring depth of the decode CTA per tile height R.  The ring
-// holds more 32-token stages than there are consumers, so that while every
-// consumer works on one stage the others are still in flight from HBM.
+// Consumer warps, ring depth (32-token stages) and copier warps of the decode CTA per tile
+// height R, from a sweep on the Llama-3-8B-shaped (R = 4) and skewed long-context (R = 8)
+// batches: three copier warps keep ~0.9 of HBM bandwidth in flight; eight consumer warps (two
+// per SM sub-partition) hide the latency of the R <= 4 math; R = 8 needs more registers per
+// thread, so four.
 template <int R>
 struct DecodeConfig {
-  static constexpr int kWarps = R >= 8 ? 6 : 4;
-  static constexpr int kStages = R >= 8 ? 10 : 12;
+  static constexpr int kWarps = R >= 8 ? 4 : 8;
+  static constexpr int kStages = R >= 8 ? 11 : 9;
+  static constexpr int kCopiers = 3;  // copier warps of the 16-byte-copy loader
 };
 
-template <int R>
-int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
+template <int R, int kCopiers>
+int launch_decode_as(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
   constexpr int kDecodeWarps = DecodeConfig<R>::kWarps;
   constexpr int kDecodeStages = DecodeConfig<R>::kStages;
   using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages>;
-  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages>;
+  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages, kCopiers>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
   });
   if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(decode)");
-  kernel<<<grid, (kDecodeWarps + 1) * 32, sizeof(Smem), stream>>>(p);
+  kernel<<<grid, (kDecodeWarps + (kCopiers ? 1 + kCopiers : 1)) * 32, sizeof(Smem), stream>>>(p);
   FI_CUDA(cudaGetLastError());
   return FI_OK;
+}
+
+// Power-of-two page sizes take the 16-byte-copy loader, others the bulk-copy loader.
+template <int R>
+int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
+  return p.page_shift >= 0 ? launch_decode_as<R, DecodeConfig<R>::kCopiers>(grid, p, stream)
+                           : launch_decode_as<R, 0>(grid, p, stream);
 }
 
 }  // namespace
@@ -292,6 +304,7 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
     p.head_stride = (long long)ps * fi::kHeadDim;
     p.num_pages = num_pages;
     p.page_size = ps;
+    p.page_shift = (ps & (ps - 1)) == 0 ? __builtin_ctz(unsigned(ps)) : -1;
     p.hqo = ws->hqo;
     p.group = h[fi::H_GROUP];
     p.slot_rows = fi::kTcRows;

@@ -22,8 +22,8 @@
 //     number of pages;
 //   * a unit sees e keys (under the causal mask: those of its last token) and is
 //     cut into n = ceil(e / L_kv) chunks of cs = pages(ceil(e / n)) tokens;
-//   * #CTA = k * (SM budget) with k = 1 for the decode path and 2 for the
-//     tensor-core path (two CTAs share an SM's tensor memory and tensor pipe);
+//   * #CTA = k * (SM budget) with k fixed per path (kDecodeCtasPerSm,
+//     kTcCtasPerSm; both 1: one persistent CTA per SM);
 //   * item cost = alpha * rows + beta * chunk length;
 //   * sort by cost descending, ties by enumeration order; the queue pops the
 //     least-loaded CTA, ties to the lowest CTA id.

@@ -36,4 +36,7 @@ struct PrefillArgs {
 // Returns an fi_status.
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
+// Records the text of a failed CUDA call for fi_last_error_message; returns FI_ERR_CUDA.
+int record_cuda_error(cudaError_t e, const char* what);
+
 }  // namespace fi

@@ -48,6 +48,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---- register reallocation between warpgroups ---------------------------------------------------
+// Executed by all warps of a warpgroup.  The block's registers are redistributed: the sum over
+// warpgroups of (128 threads x count) must not exceed what the block was launched with.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ---- MMA --------------------------------------------------------------------------------------
 
 // Shared-memory matrix descriptor: start, leading / stride byte offsets (16-byte units),

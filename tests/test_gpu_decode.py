@@ -154,3 +154,20 @@ def test_merge_states_kernel():
     torch.cuda.synchronize()
     ro, rl = A.merge_states(ta.float().cpu().numpy(), la, tb.float().cpu().numpy(), lb)
     assert_close(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl)
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "skewed_long_decode"])
+def test_many_back_to_back_launches(name):
+    """Hundreds of launches in a row: no pipeline wait may time out and every output stays bit-identical."""
+    torch = torch_mod()
+    b = W.by_name(name)
+    dev = to_device(b)
+    o_ref, l_ref, ws = run_library(b, dev=dev)
+    q, k, v = dev
+    o, lse = alloc_out(b)
+    for _ in range(300):
+        ws.run(q, k, v, o, lse)
+    torch.cuda.synchronize()
+    assert ws.get_error() == 0
+    assert np.array_equal(o.float().cpu().numpy(), o_ref)
+    assert np.array_equal(lse.cpu().numpy().astype(np.float64), l_ref)

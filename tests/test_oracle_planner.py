@@ -67,7 +67,7 @@ def test_coverage_and_bounds(seed):
         assert p.path == P.PATH_TENSOR and p.tile_tokens * g <= 128 and p.rows_tile == 128
     # chunk bound: a whole number of pages, at least l_min and at least total / #CTA
     total = sum(c["hk"] * -(-int(lq[i]) // p.tile_tokens) * int(lk[i]) for i in range(len(lq)))
-    assert p.num_ctas == c["n_cta"] * (2 if p.path == P.PATH_TENSOR else 1)
+    assert p.num_ctas == c["n_cta"] * (P.TC_CTAS_PER_SM if p.path == P.PATH_TENSOR else P.DECODE_CTAS_PER_SM)
     assert p.l_kv_chunk % c["ps"] == 0 and p.l_kv_chunk >= 256 and p.l_kv_chunk * p.num_ctas >= total
     # every (request, kv head, tile) covers its visible keys exactly once with contiguous chunks
     by_unit = {}
