@@ -51,7 +51,7 @@ PATH_TENSOR = 1
 TC_ROWS = 128
 DECODE_MAX_ROWS = 8
 DECODE_CTAS_PER_SM = 1
-TC_CTAS_PER_SM = 1
+TC_CTAS_PER_SM = 2
 NOT_CAUSAL_DIAG = 1 << 30
 PLAN_MAGIC = 0x46495031
 HEADER_LEN = 16

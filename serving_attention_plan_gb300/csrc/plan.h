@@ -17,7 +17,7 @@ constexpr int kPathTensor = 1;
 constexpr int kTcRows = 128;          // rows of a tensor-core tile (tcgen05 M)
 constexpr int kDecodeMaxRows = 8;     // largest tile the CUDA-core decode path takes
 constexpr int kDecodeCtasPerSm = 1;   // persistent CTAs per SM of each path (#CTA = k * #SM)
-constexpr int kTcCtasPerSm = 1;
+constexpr int kTcCtasPerSm = 2;
 constexpr int32_t kNotCausalDiag = 1 << 30;
 constexpr int32_t kPlanMagic = 0x46495031;
 constexpr int kHeaderLen = 16;

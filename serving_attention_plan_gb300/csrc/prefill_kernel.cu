@@ -9,28 +9,26 @@
 //     swizzled shared-memory tile (the TMA sparse gather the paper leaves as
 //     future work, 核心机制 8 / App. B).  GQA heads fold into the rows
 //     (术语与记号 "GQA 头组融合", App. A): a tile is 128/g tokens x g heads.
-//   术语与记号 "Attention State 与 ⊕" (paper §2.2): states over disjoint key
-//     sets merge associatively.  Inside a CTA the KV tiles of one work item are
-//     dealt alternately to two softmax warpgroups, each keeping its own state
-//     (S and O buffers in tensor memory); the two states of every row are merged
-//     at the end of the item, so the MMA of one group overlaps the softmax of
-//     the other.
 //   实验与指标 (paper §4.2): causal prefill with the mask aligned to the end of
 //     each request's KV.
 //   核心机制 6-7 (paper §3.3.1, App. D): persistent CTAs walk the plan's queues;
 //     split rows are merged in-kernel by the last chunk to finish, in plan order.
 //
-// One CTA per SM, 12 warps (3 warpgroups):
-//   warps 0-3  softmax group 0 (even KV tiles of an item); thread t owns row t = TMEM lane t
-//   warps 4-7  softmax group 1 (odd KV tiles)
-//   warp 8     TMA producer (Q per item, K and V per 128-key tile through a 2-stage ring)
-//   warp 9     TMEM allocation (all 512 columns) and MMA issue (one thread)
-//   warps 10-11 idle (they complete the third warpgroup, which gives registers back)
-// TMEM columns: S0 [0,128) S1 [128,256) (fp32 scores, overwritten in place by
-// bf16 P pairs in their first 64 columns), O0 [256,384), O1 [384,512).
-// Online softmax in base 2 with a lazy rescale: a group rescales its O and l
-// only when a row's running maximum grows by more than 8 (a factor 256), which
-// keeps exp2 arguments <= 8 and changes the result only by rounding.
+// Two CTAs per SM (each holds 256 of the SM's 512 TMEM columns and ~97 KB of
+// shared memory), 8 warps = 2 warpgroups each:
+//   warps 0-3  softmax + epilogue; thread t owns row t = TMEM lane t
+//   warp 4     TMA producer (Q per item, K and V per 128-key tile)
+//   warp 5     TMEM allocation and MMA issue (one thread)
+//   warps 6-7  idle (they complete the second warpgroup, which hands its registers to the first)
+// The two CTAs of an SM run independent item streams, so one CTA's softmax,
+// epilogue and item changes overlap the other's MMAs.
+// TMEM: S = Q K^T in columns [0,128) (fp32), overwritten in place by P (bf16
+// pairs, columns [0,64)) which is the A operand of O += P V; O accumulates in
+// columns [128,256).  P stays in tensor memory, so P.V reads only V from shared
+// memory (an MMA with both operands in shared memory uses its full bandwidth).
+// Online softmax in base 2 with a lazy rescale: O and l are rescaled only when
+// a row's running maximum grows by more than 8 (a factor 256), which keeps
+// exp2 arguments <= 8 and changes the result only by rounding.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -50,19 +48,15 @@ namespace {
 constexpr int kTile = 128;                  // rows of a Q tile, keys of a KV tile
 constexpr int kHalfBytes = kTile * 128;     // one 64-dim half of a 128-row bf16 tile (16 KB)
 constexpr int kTileBytes = 2 * kHalfBytes;  // full 128 x 128 bf16 tile
-constexpr int kStages = 2;                  // K/V ring depth
-constexpr int kThreads = 384;  // 3 warpgroups: a block's registers are sized per warpgroup
-// Register split after launch (launch: 384 threads x 168): the two softmax warpgroups take
-// 216 each, the producer/MMA warpgroup keeps 56: 2*128*216 + 128*56 = 62464 <= 64512.
-constexpr uint32_t kSoftmaxRegs = 216;
-constexpr uint32_t kControlRegs = 56;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 256;
+// Register split after launch (2 CTAs x 256 threads x 128): the softmax warpgroup takes 184,
+// the producer/MMA warpgroup keeps 72: 128 * 184 + 128 * 72 = 32768 = 256 * 128.
+constexpr uint32_t kSoftmaxRegs = 184;
+constexpr uint32_t kControlRegs = 72;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColO = 128;
 constexpr float kRescaleThreshold = 8.0f;
-
-__device__ __forceinline__ uint32_t col_s(int b) { return uint32_t(b) * 128u; }
-__device__ __forceinline__ uint32_t col_o(int b) { return 256u + uint32_t(b) * 128u; }
 
 struct PrefillParams {
   const int32_t* cta_indptr;
@@ -88,12 +82,9 @@ struct PrefillParams {
 
 struct PrefillSmem {
   uint8_t q[kTileBytes];  // [2 halves][128 rows][128 B], 128B-swizzled
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
-  float ml[2][2][kTile];  // per softmax group: running max, sum (for the end-of-item merge)
-  uint64_t q_full, q_empty, o_free;
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint8_t k[kTileBytes];
+  uint8_t v[kTileBytes];
+  uint64_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, o_free;
   uint32_t tmem_base;
   int flag;
   int abort;
@@ -117,7 +108,7 @@ struct Item {
 };
 
 // ---------------------------------------------------------------------------------------------
-// warp 8: TMA producer
+// warp 4: TMA producer
 // ---------------------------------------------------------------------------------------------
 __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                          const CUtensorMap* tm_v, int begin, int end) {
@@ -125,7 +116,7 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
   const int ps = p.page_size;
   const int ppt = kTile / ps;  // pages per KV tile (<= 16)
   const int oob_page = p.num_pages * p.hkv;
-  int gt = 0, nq = 0;
+  int tt = 0, nq = 0;
   bool ok = true;
   for (int pos = begin; pos < end && ok; ++pos) {
     Item it;
@@ -139,9 +130,7 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
       tc::tma_load_3d(sm.q, tm_q, 0, it.kv_head * p.group, it.q_start, &sm.q_full);
       tc::tma_load_3d(sm.q + kHalfBytes, tm_q, 64, it.kv_head * p.group, it.q_start, &sm.q_full);
     }
-    for (int t = 0; t < n_tiles; ++t, ++gt) {
-      const int st = gt % kStages;
-      const int fill = gt / kStages;
+    for (int t = 0; t < n_tiles; ++t) {
       const int base = it.kv_lo + t * kTile;
       int z = oob_page;  // out-of-range page-head coordinate: the box reads as zeros
       if (lane < ppt) {
@@ -155,116 +144,86 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
           }
         }
       }
-      if (fill > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_empty[st], (fill - 1) & 1, p.err, &sm.abort));
+      if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_empty, (tt - 1) & 1, p.err, &sm.abort));
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
       __syncwarp();
       if (lane < ppt) {
-        tc::tma_load_3d(sm.k[st] + lane * ps * 128, tm_k, 0, 0, z, &sm.k_full[st]);
-        tc::tma_load_3d(sm.k[st] + kHalfBytes + lane * ps * 128, tm_k, 64, 0, z, &sm.k_full[st]);
+        tc::tma_load_3d(sm.k + lane * ps * 128, tm_k, 0, 0, z, &sm.k_full);
+        tc::tma_load_3d(sm.k + kHalfBytes + lane * ps * 128, tm_k, 64, 0, z, &sm.k_full);
       }
-      if (fill > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_empty[st], (fill - 1) & 1, p.err, &sm.abort));
+      if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_empty, (tt - 1) & 1, p.err, &sm.abort));
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
       __syncwarp();
       if (lane < ppt) {
-        tc::tma_load_3d(sm.v[st] + lane * ps * 128, tm_v, 0, 0, z, &sm.v_full[st]);
-        tc::tma_load_3d(sm.v[st] + kHalfBytes + lane * ps * 128, tm_v, 64, 0, z, &sm.v_full[st]);
+        tc::tma_load_3d(sm.v + lane * ps * 128, tm_v, 0, 0, z, &sm.v_full);
+        tc::tma_load_3d(sm.v + kHalfBytes + lane * ps * 128, tm_v, 64, 0, z, &sm.v_full);
       }
+      ++tt;
     }
     ++nq;
   }
   // never leave with tensor copies still landing in this CTA's shared memory
   if (nq > 0) mbar_wait_bounded(&sm.q_full, (nq - 1) & 1);
-  for (int g = gt - 1; g >= 0 && g >= gt - kStages; --g) {
-    mbar_wait_bounded(&sm.k_full[g % kStages], (g / kStages) & 1);
-    mbar_wait_bounded(&sm.v_full[g % kStages], (g / kStages) & 1);
+  if (tt > 0) {
+    mbar_wait_bounded(&sm.k_full, (tt - 1) & 1);
+    mbar_wait_bounded(&sm.v_full, (tt - 1) & 1);
   }
 }
 
 // ---------------------------------------------------------------------------------------------
-// warp 9, one thread: MMA issue.  Order per item: QK(0), then for each tile t:
-// QK(t+1) into the other S buffer, PV(t) -- so S(t+1) is computed while P(t) is.
+// warp 5, one thread: MMA issue
 // ---------------------------------------------------------------------------------------------
-struct MmaState {
-  int gt;      // global KV tile counter (ring stage / phase)
-  int use[2];  // uses of S/O buffer b so far (QK and PV each count once per use)
-};
-
-__device__ __forceinline__ bool issue_qk(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, MmaState& ms, int t,
-                                         bool last, int gt_item) {
-  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kTile, 0, 0);  // A = Q (K-major), B = K (K-major)
-  const int b = t & 1;
-  const int g = gt_item + t;
-  const int st = g % kStages;
-  const int u = ms.use[b] + (t >> 1);  // use index of buffer b for this tile
-  if (!mbar_wait(&sm.k_full[st], (g / kStages) & 1, p.err, &sm.abort)) return false;
-  if (u > 0 && !mbar_wait(&sm.pv_done[b], (u - 1) & 1, p.err, &sm.abort)) return false;  // S[b]/P[b] free
-  tc::fence_after_sync();
-  const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k[st]);
-#pragma unroll
-  for (int kh = 0; kh < 2; ++kh) {
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      // K-major, 128B swizzle: a 16-element k step is 32 B inside the 128-B row; 8-row groups 1024 B apart
-      const uint64_t a = tc::smem_desc(q_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
-      const uint64_t bd = tc::smem_desc(k_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
-      tc::mma_ss(tmem + col_s(b), a, bd, idesc_qk, (kh | ks) != 0 ? 1u : 0u);
-    }
-  }
-  tc::commit(&sm.s_full[b]);
-  tc::commit(&sm.k_empty[st]);
-  if (last) tc::commit(&sm.q_empty);
-  return true;
-}
-
-__device__ __forceinline__ bool issue_pv(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, MmaState& ms, int t,
-                                         int gt_item, int nq) {
-  constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P (TMEM), B = V (MN-major)
-  const int b = t & 1;
-  const int g = gt_item + t;
-  const int st = g % kStages;
-  const int u = ms.use[b] + (t >> 1);
-  if (!mbar_wait(&sm.p_full[b], u & 1, p.err, &sm.abort)) return false;
-  if (!mbar_wait(&sm.v_full[st], (g / kStages) & 1, p.err, &sm.abort)) return false;
-  if (t == 0 && nq > 0 && !mbar_wait(&sm.o_free, (nq - 1) & 1, p.err, &sm.abort)) return false;
-  tc::fence_after_sync();
-  const uint32_t v_addr = smem_u32(sm.v[st]);
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    // V as B (K = keys, N = dims), MN-major 128B swizzle: a 16-key step is two 8-row
-    // groups (2048 B); the second 64-dim half is the leading-dimension step (16 KB)
-    const uint64_t bd = tc::smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, tc::kLayoutSw128);
-    tc::mma_ts(tmem + col_o(b), tmem + col_s(b) + ks * 8, bd, idesc_pv, (t >= 2 || ks > 0) ? 1u : 0u);
-  }
-  tc::commit(&sm.pv_done[b]);
-  tc::commit(&sm.v_empty[st]);
-  return true;
-}
-
 __device__ void mma_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
-  MmaState ms{0, {0, 0}};
-  int nq = 0;
+  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kTile, 0, 0);  // A = Q (K-major), B = K (K-major)
+  constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P (TMEM), B = V (MN-major)
+  const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v);
+  int tt = 0, nq = 0;
   for (int pos = begin; pos < end; ++pos) {
     Item it;
     it.load(p.items, pos);
-    const int n = it.tiles();
-    if (n == 0) continue;
+    const int n_tiles = it.tiles();
+    if (n_tiles == 0) continue;
     if (!mbar_wait(&sm.q_full, nq & 1, p.err, &sm.abort)) return;
-    if (!issue_qk(p, sm, tmem, ms, 0, n == 1, ms.gt)) return;
-    for (int t = 0; t < n; ++t) {
-      if (t + 1 < n && !issue_qk(p, sm, tmem, ms, t + 1, t + 1 == n - 1, ms.gt)) return;
-      if (!issue_pv(p, sm, tmem, ms, t, ms.gt, nq)) return;
+    for (int t = 0; t < n_tiles; ++t) {
+      if (!mbar_wait(&sm.k_full, tt & 1, p.err, &sm.abort)) return;
+      if (tt > 0 && !mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort)) return;  // S/P columns free
+      tc::fence_after_sync();
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          // K-major, 128B swizzle: a 16-element k step is 32 B inside the 128-B row; 8-row groups 1024 B apart
+          const uint64_t a = tc::smem_desc(q_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
+          const uint64_t b = tc::smem_desc(k_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
+          tc::mma_ss(tmem + kColS, a, b, idesc_qk, (kh | ks) != 0 ? 1u : 0u);
+        }
+      }
+      tc::commit(&sm.s_full);
+      tc::commit(&sm.k_empty);
+      if (t == n_tiles - 1) tc::commit(&sm.q_empty);
+      if (!mbar_wait(&sm.p_full, tt & 1, p.err, &sm.abort)) return;
+      if (!mbar_wait(&sm.v_full, tt & 1, p.err, &sm.abort)) return;
+      if (t == 0 && nq > 0 && !mbar_wait(&sm.o_free, (nq - 1) & 1, p.err, &sm.abort)) return;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        // V as B (K = keys, N = dims), MN-major 128B swizzle: a 16-key step is two 8-row
+        // groups (2048 B); the second 64-dim half is the leading-dimension step (16 KB)
+        const uint64_t b = tc::smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, tc::kLayoutSw128);
+        tc::mma_ts(tmem + kColO, tmem + kColS + ks * 8, b, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+      }
+      tc::commit(&sm.o_done);
+      tc::commit(&sm.v_empty);
+      ++tt;
     }
-    ms.use[0] += (n + 1) / 2;
-    ms.use[1] += n / 2;
-    ms.gt += n;
     ++nq;
   }
 }
 
 // ---------------------------------------------------------------------------------------------
-// warps 0-7: softmax (two groups), end-of-item state merge, epilogue, merge of split rows
+// warps 0-3: softmax, epilogue and the merge of split rows
 // ---------------------------------------------------------------------------------------------
 
 // Output row of (token, head) for tile row `row`.
@@ -288,16 +247,16 @@ __device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst_ptr, const floa
 
 __device__ __forceinline__ float lse_out(float lse2) { return (lse2 == -INFINITY) ? -INFINITY : lse2 * kLn2; }
 
-// One KV tile of one softmax group: scores -> mask -> online-softmax update -> P into TMEM.
+// One KV tile: scores -> mask -> online-softmax update -> P into the S columns of TMEM.
 template <bool kMasked>
-__device__ __forceinline__ void softmax_tile(const uint32_t t_s, const uint32_t t_o, int lim, float scale, float& m,
-                                             float& l, bool first, PrefillSmem& sm, int b, int u,
-                                             const PrefillParams& p, bool& alive) {
+__device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lim, float scale, float& m, float& l,
+                                             bool first, PrefillSmem& sm, int tt, const PrefillParams& p,
+                                             bool& alive) {
   uint32_t s[kTile];
-  tc::tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
-  tc::tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-  tc::tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
-  tc::tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
+  tc::tmem_ld32(t_lane + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+  tc::tmem_ld32(t_lane + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+  tc::tmem_ld32(t_lane + kColS + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
+  tc::tmem_ld32(t_lane + kColS + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
   tc::tmem_wait_ld();
   // row maximum of the raw scores with 8 independent partial maxima
   float mx8[8];
@@ -339,37 +298,33 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_s, const uint32_t 
   const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
   const float2 s0123 = __fadd2_rn(s01, s23);
   l += s0123.x + s0123.y;
-  tc::tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
-  tc::tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+  tc::tmem_st32(t_lane + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+  tc::tmem_st32(t_lane + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
   tc::tmem_wait_st();
   if (__any_sync(0xffffffffu, need)) {
-    // O[b] was last written by this group's previous P.V: wait for it, then rescale in place
-    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[b], (u - 1) & 1, p.err, &sm.abort));
+    // O was last written by the previous tile's P.V: wait for it, then rescale in place
+    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort));
     tc::fence_after_sync();
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
-      tc::tmem_ld32(t_o + 32 * c, o);
+      tc::tmem_ld32(t_lane + kColO + 32 * c, o);
       tc::tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-      tc::tmem_st32(t_o + 32 * c, o);
+      tc::tmem_st32(t_lane + kColO + 32 * c, o);
     }
     tc::tmem_wait_st();
   }
 }
 
-__device__ void softmax_group(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
-  const int b = threadIdx.x >> 7;    // softmax group 0 or 1
-  const int row = threadIdx.x & 127;  // TMEM lane
-  const int lane = threadIdx.x & 31;
-  const uint32_t lane_off = uint32_t(row & ~31) << 16;
-  const uint32_t t_s = tmem + lane_off + col_s(b);
-  const uint32_t t_o = tmem + lane_off + col_o(b);
-  const uint32_t t_o0 = tmem + lane_off + col_o(0);
-  const uint32_t t_o1 = tmem + lane_off + col_o(1);
+__device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  const int row = threadIdx.x;  // 0..127 == TMEM lane
+  const int warp = row >> 5;
+  const int lane = row & 31;
+  const uint32_t t_lane = tmem + (uint32_t(warp * 32) << 16);
   const float scale = p.scale_log2;
-  int use = 0;  // uses of this group's S/O buffer so far
+  int tt = 0;
   bool alive = true;
   for (int pos = begin; pos < end; ++pos) {
     Item it;
@@ -378,139 +333,127 @@ __device__ void softmax_group(const PrefillParams& p, PrefillSmem& sm, uint32_t 
     const int rows_valid = it.q_len * p.group;
     const int u = row / p.group;
     float m = -INFINITY, l = 0.f;
-    int mine = 0;  // tiles of this item handled by this group
-    for (int t = b; t < n_tiles; t += 2, ++mine) {
+
+    for (int t = 0; t < n_tiles; ++t) {
       const int base = it.kv_lo + t * kTile;
       const int lim = max(0, min(kTile, min(it.kv_hi - base, it.diag + u + 1 - base)));
-      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.s_full[b], (use + mine) & 1, p.err, &sm.abort));
+      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.s_full, tt & 1, p.err, &sm.abort));
       if (alive) {
         tc::fence_after_sync();
         if (__all_sync(0xffffffffu, lim >= kTile)) {
-          softmax_tile<false>(t_s, t_o, lim, scale, m, l, mine == 0, sm, b, use + mine, p, alive);
+          softmax_tile<false>(t_lane, lim, scale, m, l, t == 0, sm, tt, p, alive);
         } else {
-          softmax_tile<true>(t_s, t_o, lim, scale, m, l, mine == 0, sm, b, use + mine, p, alive);
+          softmax_tile<true>(t_lane, lim, scale, m, l, t == 0, sm, tt, p, alive);
         }
         tc::fence_before_sync();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[b]);
+      if (lane == 0) mbar_arrive(&sm.p_full);
+      ++tt;
     }
-    use += mine;
 
-    // ---- end of item: merge the two groups' states, write O / LSE or a partial slot ----------
-    if (mine > 0) {
-      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.pv_done[b], (use - 1) & 1, p.err, &sm.abort));
+    // ---- epilogue: O / l and LSE, to the output or to a partial slot --------------------------
+    float lse2 = -INFINITY, inv = 0.f;
+    if (l > 0.f) {
+      lse2 = m + fast_log2(l);
+      inv = 1.f / l;
     }
-    sm.ml[b][0][row] = m;
-    sm.ml[b][1][row] = l;
-    named_bar_sync(1, 256);
-    tc::fence_after_sync();
-    const float m0 = sm.ml[0][0][row], l0 = sm.ml[0][1][row];
-    const float m1 = sm.ml[1][0][row], l1 = sm.ml[1][1][row];
-    const float M = fmaxf(m0, m1);
-    const float w0 = (l0 > 0.f) ? fast_exp2(m0 - M) : 0.f;
-    const float w1 = (l1 > 0.f) ? fast_exp2(m1 - M) : 0.f;
-    const float L = w0 * l0 + w1 * l1;
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    const float lse2 = (L > 0.f) ? M + fast_log2(L) : -INFINITY;
-    const float c0 = w0 * inv, c1 = w1 * inv;
-    // group b writes dims [64b, 64b + 64) of the merged row
+    uint32_t o[kHeadDim];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint32_t col = uint32_t(64 * b + 32 * c);
-      uint32_t x0[32], x1[32];
-      float v[32];
-      if (n_tiles > 0 && alive) {
-        tc::tmem_ld32(t_o0 + col, x0);
-        tc::tmem_ld32(t_o1 + col, x1);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float a0 = (c0 != 0.f) ? c0 * __uint_as_float(x0[j]) : 0.f;  // never read a group's unused O
-          const float a1 = (c1 != 0.f) ? c1 * __uint_as_float(x1[j]) : 0.f;
-          v[j] = a0 + a1;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-      }
-      if (row < rows_valid) {
-        if (it.slot < 0) {
-          store_bf16_32(p.o + out_row(p, it, row) * kHeadDim + col, v);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + ((size_t)it.slot * p.slot_rows + row) * kHeadDim + col);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        }
-      }
-    }
-    if (b == 0 && row < rows_valid) {
-      if (it.slot < 0) {
-        p.lse[out_row(p, it, row)] = lse_out(lse2);
-      } else {
-        p.part_lse[(size_t)it.slot * p.slot_rows + row] = lse2;
-      }
-    }
+    for (int j = 0; j < kHeadDim; ++j) o[j] = 0u;
     if (n_tiles > 0) {
+      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort));
+      if (alive) {
+        tc::fence_after_sync();
+        tc::tmem_ld32(t_lane + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(o + 0));
+        tc::tmem_ld32(t_lane + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+        tc::tmem_ld32(t_lane + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
+        tc::tmem_ld32(t_lane + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
+        tc::tmem_wait_ld();
+      }
+      // O is in registers: the next item's first P.V may overwrite it while this one is written out
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.o_free);
     }
+    if (row < rows_valid) {
+      if (it.slot < 0) {
+        __nv_bfloat16* dst = p.o + out_row(p, it, row) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[32 * c + j]) * inv;
+          store_bf16_32(dst + 32 * c, v);
+        }
+        p.lse[out_row(p, it, row)] = lse_out(lse2);
+      } else {
+        const size_t srow = (size_t)it.slot * p.slot_rows + row;
+        float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kHeadDim);
+#pragma unroll
+        for (int j = 0; j < kHeadDim / 4; ++j)
+          dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                               __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        p.part_lse[srow] = lse2;
+      }
+    }
 
     if (it.slot >= 0) {
       // contraction of a split row: the last chunk to finish merges all slots in plan order
-      named_bar_sync(1, 256);
+      named_bar_sync(1, 128);
       const int unit = __ldg(p.slot_unit + it.slot);
-      if (threadIdx.x == 0) {
+      if (row == 0) {
         __threadfence();
         const uint32_t prev = atomicAdd(p.counters + unit, 1u);
         const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
         sm.flag = (prev == uint32_t(n_chunks - 1)) ? 1 : 0;
         if (sm.flag) __threadfence();
       }
-      named_bar_sync(1, 256);
-      if (sm.flag && row < rows_valid) {
-        const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
-        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
-        float Mc = -INFINITY;
-        for (int c = 0; c < n_chunks; ++c) Mc = fmaxf(Mc, __ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row));
-        float Lc = 0.f;
-        if (Mc != -INFINITY) {
-          for (int c = 0; c < n_chunks; ++c) Lc += fast_exp2(__ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row) - Mc);
-        }
-        const float invL = (Mc != -INFINITY) ? 1.f / Lc : 0.f;
-        __nv_bfloat16* dst = p.o + out_row(p, it, row) * kHeadDim;
-        for (int dc = 2 * b; dc < 2 * b + 2; ++dc) {  // group b merges dims [64b, 64b + 64)
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      named_bar_sync(1, 128);
+      if (sm.flag) {
+        if (row < rows_valid) {
+          const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
+          const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+          float Mc = -INFINITY;
+          for (int c = 0; c < n_chunks; ++c) Mc = fmaxf(Mc, __ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row));
+          float Lc = 0.f;
           if (Mc != -INFINITY) {
-            for (int c = 0; c < n_chunks; ++c) {
-              const size_t srow = (size_t)(first + c) * p.slot_rows + row;
-              const float w = fast_exp2(__ldcg(p.part_lse + srow) - Mc) * invL;
-              const float4* src = reinterpret_cast<const float4*>(p.part_o + srow * kHeadDim + 32 * dc);
+            for (int c = 0; c < n_chunks; ++c)
+              Lc += fast_exp2(__ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row) - Mc);
+          }
+          const float invL = (Mc != -INFINITY) ? 1.f / Lc : 0.f;
+          __nv_bfloat16* dst = p.o + out_row(p, it, row) * kHeadDim;
+          for (int dc = 0; dc < 4; ++dc) {
+            float v[32];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 a = __ldcg(src + j);
-                v[4 * j] += w * a.x;
-                v[4 * j + 1] += w * a.y;
-                v[4 * j + 2] += w * a.z;
-                v[4 * j + 3] += w * a.w;
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            if (Mc != -INFINITY) {
+              for (int c = 0; c < n_chunks; ++c) {
+                const size_t srow = (size_t)(first + c) * p.slot_rows + row;
+                const float w = fast_exp2(__ldcg(p.part_lse + srow) - Mc) * invL;
+                const float4* src = reinterpret_cast<const float4*>(p.part_o + srow * kHeadDim + 32 * dc);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 a = __ldcg(src + j);
+                  v[4 * j] += w * a.x;
+                  v[4 * j + 1] += w * a.y;
+                  v[4 * j + 2] += w * a.z;
+                  v[4 * j + 3] += w * a.w;
+                }
               }
             }
+            store_bf16_32(dst + 32 * dc, v);
           }
-          store_bf16_32(dst + 32 * dc, v);
+          p.lse[out_row(p, it, row)] = lse_out(Mc == -INFINITY ? -INFINITY : Mc + fast_log2(Lc));
         }
-        if (b == 0) p.lse[out_row(p, it, row)] = lse_out(Mc == -INFINITY ? -INFINITY : Mc + fast_log2(Lc));
+        if (row == 0) p.counters[unit] = 0u;
       }
-      named_bar_sync(1, 256);
-      if (threadIdx.x == 0 && sm.flag) p.counters[unit] = 0u;
+      named_bar_sync(1, 128);
     }
-    named_bar_sync(1, 256);  // sm.ml and sm.flag are reused by the next item
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ unsigned char smem_raw[];
@@ -520,28 +463,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    mbar_init(&sm.o_free, 8);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
-      mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.p_full[b], 4);
-      mbar_init(&sm.pv_done[b], 1);
-    }
+    mbar_init(&sm.k_full, 1);
+    mbar_init(&sm.k_empty, 1);
+    mbar_init(&sm.v_full, 1);
+    mbar_init(&sm.v_empty, 1);
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 4);
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.o_free, 4);
     sm.flag = 0;
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == kProducerWarp && (threadIdx.x & 31) == 0) {
+  if (warp == 4 && (threadIdx.x & 31) == 0) {
     tc::tma_prefetch_desc(&tm_q);
     tc::tma_prefetch_desc(&tm_k);
     tc::tma_prefetch_desc(&tm_v);
   }
-  if (warp == kMmaWarp) {
+  if (warp == 5) {
     tc::tmem_alloc(&sm.tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -551,22 +490,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
-  if ((tmem & 0xFFFFu) != 0u) {  // not an address this CTA can use: report, do nothing
+  if ((tmem & 0xFFFFu) + kTmemCols > 512u) {  // not an address this CTA can use: report, do nothing
     if (threadIdx.x == 0) atomicOr(p.err, FI_DEVERR_TMEM);
-  } else if (warp < 8) {
+  } else if (warp < 4) {
     tc::regs_increase<kSoftmaxRegs>();
-    softmax_group(p, sm, tmem, begin, end);
+    softmax_epilogue(p, sm, tmem, begin, end);
   } else {
     tc::regs_decrease<kControlRegs>();
-    if (warp == kProducerWarp) {
+    if (warp == 4) {
       producer(p, sm, &tm_q, &tm_k, &tm_v, begin, end);
-    } else if (warp == kMmaWarp && (threadIdx.x & 31) == 0) {
+    } else if (warp == 5 && (threadIdx.x & 31) == 0) {
       mma_issuer(p, sm, tmem, begin, end);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == 5) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
