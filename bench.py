@@ -235,6 +235,8 @@ def reference_arm(args):
     if rank != 0:
         return
     b = W.by_name(args.config)
+    if hasattr(b, "flat"):
+        b = b.flat
     for _ in range(args.warmup):
         cpu_oracle_sample(b, budget_s=2.0)
     vals = []
@@ -247,12 +249,28 @@ def reference_arm(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.config},
+        "config": dict(workload_config(args.config, b), parallelism="host cores (CPU oracle)"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": samples + " per step, float64 NumPy oracle"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest replica sets the whole job's time); identity at N = 1."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, seconds: float, world: int) -> float:
+    """Whole-job throughput of `world` independent replicas: all ranks' units over the slowest rank's time."""
+    return world * units_per_rank / seconds
 
 
 def workload_config(name, b):
@@ -312,13 +330,10 @@ def main():
     device_errors = case.ws.get_error()  # a timed-out pipeline wait or a skipped page would show here
     if device_errors:
         print(f"bench: device error bits {device_errors:#x} during the timed launches", file=sys.stderr)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     hdr = case.ws.info()
     kernel_name = f"decode_kernel<R={int(hdr[3])}>" if hdr[1] == 0 else "prefill_kernel"
-    value = world * nbytes / (ms * 1e-3) / 1e9
+    value = replica_throughput(nbytes, ms * 1e-3, world) / 1e9
     achieved = abytes / (ms * 1e-3) / 1e9
 
     # end to end through the C ABI from host buffers
