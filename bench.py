@@ -431,7 +431,7 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
     ms = time_launches(torch, c.run, steps, warmup)
     hdr = c.ws.info()
     errs = c.ws.get_error()
-    out = {"us_per_batch": ms * 1e3, "path": "tensor-core" if hdr[1] == 1 else "cuda-core",
+    out = {"us_per_batch": ms * 1e3, "path": path_name(w, hdr),
            "config": workload_config(name, w), "device_errors": errs}
     if hdr[1] == 1:
         tf = flops(w) / (ms * 1e-3) / 1e12
@@ -440,6 +440,15 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
         gbs = kv_bytes(w) / (ms * 1e-3) / 1e9
         out.update({"kv_gbs": gbs, "frac_of_hbm_peak": gbs / hbm_peak})
     return out
+
+
+def path_name(w, hdr) -> str:
+    """Which kernel body the plan runs: 128-row tiles on tcgen05, or <= 8-row decode tiles whose
+    consumer is warp-level MMA (16-byte-copy loader, power-of-two pages) or CUDA cores (bulk loader)."""
+    if hdr[1] == 1:
+        return "128-row tiles, tcgen05"
+    ps = int(w.page_size)
+    return f"{int(hdr[3])}-row tiles, " + ("mma.sync" if ps & (ps - 1) == 0 else "CUDA cores")
 
 
 if __name__ == "__main__":

@@ -1,15 +1,17 @@
-// Persistent CUDA-core decode kernel: paged-KV attention for tiles of <= 8 rows,
-// fused with the merge of split-KV partial states.
+// Persistent decode kernel: paged-KV attention for tiles of <= 8 rows, fused with the merge of
+// split-KV partial states.
 //
 // Page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎":
 //   核心机制 3 (paper §3.2): scattered KV tiles are gathered into contiguous
 //     shared memory, after which sparse and dense KV share one kernel body.
-//     Here each page-head run (page_size x 256 B, contiguous in the HND pool)
-//     is one bulk async copy into a 32-token shared-memory stage; a ring of
-//     stages keeps many copies in flight.
-//   核心机制 4 (paper §3.2.2): query tile 1 runs on CUDA cores, since MMA
-//     needs >= 16 rows; GQA heads of one KV head fold into the rows
+//     Each 32-token stage of a page-head run lands in a ring of shared-memory
+//     stages that keeps many copies in flight.
+//   核心机制 4 (paper §3.2.2): the pages run query tile 1 on CUDA cores, since
+//     an MMA needs >= 16 rows; GQA heads of one KV head fold into the rows
 //     (术语与记号 "GQA 头组融合", paper App. A), so one KV load serves g rows.
+//     Here the tensor-core consumer puts the stage's KV tokens on the MMA's
+//     16-row side instead (S^T = K Q^T, O^T = V^T P^T), which lifts that limit
+//     for 1..8 rows.
 //   核心机制 6-7 (paper §3.3.1, App. D): one persistent CTA per queue of the
 //     plan; attention and the contraction of partial outputs in one kernel;
 //     a split row is merged by whichever of its chunks finishes last, reading
@@ -18,22 +20,21 @@
 //
 // CTA layout, two loaders selectable per instantiation (kCopiers):
 //   bulk (kCopiers = 0): warp 0 = producer (page-index prefetch + one bulk async copy per
-//           page-head run);
+//           page-head run); any page size;
 //   LDGSTS: warp 0 = page-index warp (4-byte cp.async into an index ring), warps 1..kCopiers =
 //           copiers taking stages round-robin (16-byte cp.async of K/V rows, 512 B per warp
-//           instruction); used when the page size is a power of two.  The bulk engine keeps only a few copies in flight per SM, which
-//           caps a page-sized copy stream well below HBM bandwidth; 16-byte copies do not share
-//           that limit.
+//           instruction); power-of-two page sizes.  The bulk engine keeps only a few copies in
+//           flight per SM, which caps a page-sized copy stream well below HBM bandwidth; 16-byte
+//           copies do not share that limit.
 // The remaining NW warps are consumers.  Consumer warps take the CTA's KV stages round-robin
 // (stage n -> warp n % NW); each keeps an online-softmax state, and at the end
 // of a work item the NW states are merged through shared memory in warp order.
-//
-// Consumer lane mapping per 32-token stage, R rows (R = 1, 2, 4, 8):
-//   q.k: lane = (half tl, dim-lane dl); dl owns dims 8*dl..8*dl+7, tl owns
-//        tokens; partial dots of 16 (token, row) pairs are transposed through
-//        shared memory and summed, leaving one score per lane.
-//   p.v: lane owns dims 4*lane..4*lane+3 of all R accumulator rows.
-// Scores are kept in the log2 domain (q is pre-scaled by scale * log2 e).
+// Two consumer bodies:
+//   tensor-core (kMma, with the LDGSTS loader): warp-level m16n8k16 MMA, see decode_consumer_mma;
+//   CUDA cores (with the bulk loader): lane = (half tl, dim-lane dl) for q.k, dl owning dims
+//     8*dl..8*dl+7 and tl tokens, partial dots of 16 (token, row) pairs transposed through
+//     shared memory and summed; for p.v a lane owns dims 4*lane..4*lane+3 of all R rows.
+// Scores are kept in the log2 domain.
 #pragma once
 
 #include "device_common.cuh"
@@ -73,11 +74,12 @@ constexpr int kIdxSlots = 8;  // page-index ring of the LDGSTS loader (stages)
 constexpr int kRedHalf = 336; // words between the two halves of the transpose scratch
 constexpr int kRedRow = 20;   // words per lane row of the transpose scratch
 
-template <int R, int NW, int S>
+// kMma: the tensor-core consumer needs neither the transpose scratch nor the probability buffer.
+template <int R, int NW, int S, bool kMma = false>
 struct DecodeSmem {
   __nv_bfloat16 kv[S][2][kStageTokens][kHeadDim];  // [stage][K|V][token][dim]
-  float red[NW][2][2 * kRedHalf];  // per consumer warp: double-buffered transpose scratch
-  float pbuf[NW][kStageTokens * R];
+  float red[kMma ? 1 : NW][2][2 * kRedHalf];  // per consumer warp: double-buffered transpose scratch
+  float pbuf[kMma ? 1 : NW][kStageTokens * R];
   float alpha[NW][8];
   float macc[NW][R][kHeadDim];
   float mm[NW][8];
@@ -127,8 +129,8 @@ struct StageCursor {
   __device__ __forceinline__ int ntok() const { return min(kStageTokens, kv_hi - tok0()); }
 };
 
-template <int R, int NW, int S>
-__device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin, int end) {
+template <int R, int NW, int S, bool kMs>
+__device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin, int end) {
   const int lane = threadIdx.x & 31;
   const int ps = p.page_size;
   const uint64_t policy = policy_evict_first();
@@ -204,8 +206,8 @@ __device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSme
 }
 
 // LDGSTS loader, warp 0: page ids of each stage into a ring of kIdxSlots x 32 entries.
-template <int R, int NW, int S>
-__device__ __forceinline__ void decode_index_warp(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin,
+template <int R, int NW, int S, bool kMs>
+__device__ __forceinline__ void decode_index_warp(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
                                                   int end) {
   const int lane = threadIdx.x & 31;
   StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
@@ -227,8 +229,8 @@ __device__ __forceinline__ void decode_index_warp(const DecodeParams& p, DecodeS
 // rows, 16 bytes per lane per instruction.
 // Copy c (0..1023) of a stage: K/V = c / 512, token = (c % 512) / 16, 16-byte chunk = c % 16,
 // so each warp instruction moves two consecutive 256-byte rows.
-template <int R, int NW, int S, int kCopiers>
-__device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin,
+template <int R, int NW, int S, int kCopiers, bool kSwizzle, bool kMs>
+__device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
                                                    int end, int cw) {
   const int lane = threadIdx.x & 31;
   const int sh = p.page_shift;
@@ -263,8 +265,9 @@ __device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, Decode
       const int page = __shfl_sync(0xffffffffu, pg, seg);
       if (tok < nt && page >= 0) {
         const long long off = (long long)page * p.page_stride + (long long)(pos & row_mask) * kHeadDim + (lane & 15) * 8;
-        cp_async_16(&sm.kv[slot][0][tok][(lane & 15) * 8], kb + off);
-        cp_async_16(&sm.kv[slot][1][tok][(lane & 15) * 8], vb + off);
+        const int chunk = kSwizzle ? ((lane & 15) ^ (tok & 7)) : (lane & 15);
+        cp_async_16(&sm.kv[slot][0][tok][chunk * 8], kb + off);
+        cp_async_16(&sm.kv[slot][1][tok][chunk * 8], vb + off);
       }
     }
     cp_async_arrive_noinc(&sm.full[slot]);
@@ -298,8 +301,111 @@ __device__ __forceinline__ void load_q_rows(const DecodeParams& p, int q_start, 
   }
 }
 
-template <int R, int NW, int S>
-__device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSmem<R, NW, S>& sm, int begin, int end,
+// End of a work item, all NW consumer warps: merge their (O, m, l) states from shared memory in
+// warp order, then write the row (single chunk) or its partial state, and if this chunk is the
+// last of a split row to finish, contract all of the row's slots in plan order.
+template <int R, int NW, int S, bool kMs>
+__device__ __forceinline__ void decode_finish_item(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int ctid,
+                                                   int q_start, int kv_head, int rows_valid, int slot_out) {
+  for (int u = ctid; u < R * 32; u += NW * 32) {
+    const int r = u >> 5, dq = u & 31;
+    float M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, sm.mm[ww][r]);
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int ww = 0; ww < NW; ++ww) {
+        const float s = fast_exp2(sm.mm[ww][r] - M);
+        const float4 a = *reinterpret_cast<const float4*>(&sm.macc[ww][r][4 * dq]);
+        L += s * sm.ml[ww][r];
+        O.x += s * a.x;
+        O.y += s * a.y;
+        O.z += s * a.z;
+        O.w += s * a.w;
+      }
+      const float inv = 1.f / L;
+      O.x *= inv;
+      O.y *= inv;
+      O.z *= inv;
+      O.w *= inv;
+    }
+    const float lse2 = (M == -INFINITY) ? -INFINITY : M + fast_log2(L);
+    if (r < rows_valid) {
+      if (slot_out < 0) {
+        const int tok = q_start + r / p.group;
+        const int head = kv_head * p.group + r % p.group;
+        const size_t orow = (size_t)tok * p.hqo + head;
+        uint2 packed;
+        packed.x = f2_to_bf16x2(O.x, O.y);
+        packed.y = f2_to_bf16x2(O.z, O.w);
+        *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
+        if (dq == 0) p.lse[orow] = lse2 * kLn2;
+      } else {
+        const size_t srow = (size_t)slot_out * p.slot_rows + r;
+        *reinterpret_cast<float4*>(p.part_o + srow * kHeadDim + 4 * dq) = O;
+        if (dq == 0) p.part_lse[srow] = lse2;
+      }
+    }
+  }
+
+  if (slot_out >= 0) {
+    // contraction of a split row: the last chunk to finish merges all slots in order
+    named_bar_sync(1, NW * 32);
+    const int unit = __ldg(p.slot_unit + slot_out);
+    if (ctid == 0) {
+      __threadfence();
+      const uint32_t prev = atomicAdd(p.counters + unit, 1u);
+      const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+      sm.flag = (prev == uint32_t(n_chunks - 1)) ? 1 : 0;
+      if (sm.flag) __threadfence();
+    }
+    named_bar_sync(1, NW * 32);
+    if (sm.flag) {
+      const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
+      const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+      for (int u = ctid; u < R * 32; u += NW * 32) {
+        const int r = u >> 5, dq = u & 31;
+        if (r >= rows_valid) continue;
+        float M = -INFINITY;
+        for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + r));
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
+        if (M != -INFINITY) {
+          for (int c = 0; c < n_chunks; ++c) {
+            const size_t srow = (size_t)(first + c) * p.slot_rows + r;
+            const float s = fast_exp2(__ldcg(p.part_lse + srow) - M);
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_o + srow * kHeadDim + 4 * dq));
+            L += s;
+            O.x += s * a.x;
+            O.y += s * a.y;
+            O.z += s * a.z;
+            O.w += s * a.w;
+          }
+          const float inv = 1.f / L;
+          O.x *= inv;
+          O.y *= inv;
+          O.z *= inv;
+          O.w *= inv;
+        }
+        const int tok = q_start + r / p.group;
+        const int head = kv_head * p.group + r % p.group;
+        const size_t orow = (size_t)tok * p.hqo + head;
+        uint2 packed;
+        packed.x = f2_to_bf16x2(O.x, O.y);
+        packed.y = f2_to_bf16x2(O.z, O.w);
+        *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
+        if (dq == 0) p.lse[orow] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(L)) * kLn2;
+      }
+      if (ctid == 0) p.counters[unit] = 0u;
+    }
+  }
+  named_bar_sync(1, NW * 32);
+}
+
+template <int R, int NW, int S, bool kMs>
+__device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin, int end,
                                                 int w) {
   constexpr int NT = 16 / R;  // tokens per half per sub-batch
   const int lane = threadIdx.x & 31;
@@ -475,113 +581,205 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
       sm.ml[w][dl] = l_run;
     }
     named_bar_sync(1, NW * 32);
-
-    const int rows_valid = q_len * p.group;
-    for (int u = ctid; u < R * 32; u += NW * 32) {
-      const int r = u >> 5, dq = u & 31;
-      float M = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, sm.mm[ww][r]);
-      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-      float L = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int ww = 0; ww < NW; ++ww) {
-          const float s = fast_exp2(sm.mm[ww][r] - M);
-          const float4 a = *reinterpret_cast<const float4*>(&sm.macc[ww][r][4 * dq]);
-          L += s * sm.ml[ww][r];
-          O.x += s * a.x;
-          O.y += s * a.y;
-          O.z += s * a.z;
-          O.w += s * a.w;
-        }
-        const float inv = 1.f / L;
-        O.x *= inv;
-        O.y *= inv;
-        O.z *= inv;
-        O.w *= inv;
-      }
-      const float lse2 = (M == -INFINITY) ? -INFINITY : M + fast_log2(L);
-      if (r < rows_valid) {
-        if (slot_out < 0) {
-          const int tok = q_start + r / p.group;
-          const int head = kv_head * p.group + r % p.group;
-          const size_t orow = (size_t)tok * p.hqo + head;
-          uint2 packed;
-          packed.x = f2_to_bf16x2(O.x, O.y);
-          packed.y = f2_to_bf16x2(O.z, O.w);
-          *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
-          if (dq == 0) p.lse[orow] = lse2 * kLn2;
-        } else {
-          const size_t srow = (size_t)slot_out * p.slot_rows + r;
-          *reinterpret_cast<float4*>(p.part_o + srow * kHeadDim + 4 * dq) = O;
-          if (dq == 0) p.part_lse[srow] = lse2;
-        }
-      }
-    }
-
-    if (slot_out >= 0) {
-      // contraction of a split row: the last chunk to finish merges all slots in order
-      named_bar_sync(1, NW * 32);
-      const int unit = __ldg(p.slot_unit + slot_out);
-      if (ctid == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(p.counters + unit, 1u);
-        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
-        sm.flag = (prev == uint32_t(n_chunks - 1)) ? 1 : 0;
-        if (sm.flag) __threadfence();
-      }
-      named_bar_sync(1, NW * 32);
-      if (sm.flag) {
-        const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
-        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
-        for (int u = ctid; u < R * 32; u += NW * 32) {
-          const int r = u >> 5, dq = u & 31;
-          if (r >= rows_valid) continue;
-          float M = -INFINITY;
-          for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + r));
-          float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-          float L = 0.f;
-          if (M != -INFINITY) {
-            for (int c = 0; c < n_chunks; ++c) {
-              const size_t srow = (size_t)(first + c) * p.slot_rows + r;
-              const float s = fast_exp2(__ldcg(p.part_lse + srow) - M);
-              const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_o + srow * kHeadDim + 4 * dq));
-              L += s;
-              O.x += s * a.x;
-              O.y += s * a.y;
-              O.z += s * a.z;
-              O.w += s * a.w;
-            }
-            const float inv = 1.f / L;
-            O.x *= inv;
-            O.y *= inv;
-            O.z *= inv;
-            O.w *= inv;
-          }
-          const int tok = q_start + r / p.group;
-          const int head = kv_head * p.group + r % p.group;
-          const size_t orow = (size_t)tok * p.hqo + head;
-          uint2 packed;
-          packed.x = f2_to_bf16x2(O.x, O.y);
-          packed.y = f2_to_bf16x2(O.z, O.w);
-          *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
-          if (dq == 0) p.lse[orow] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(L)) * kLn2;
-        }
-        if (ctid == 0) p.counters[unit] = 0u;
-      }
-    }
-    named_bar_sync(1, NW * 32);
+    decode_finish_item<R, NW, S>(p, sm, ctid, q_start, kv_head, q_len * p.group, slot_out);
   }
 }
 
-template <int R, int NW, int S, int kCopiers = 0>
+// Tensor-core consumer (warp-level m16n8k16 MMA, bf16 in, fp32 accumulate), used with the
+// LDGSTS loader.  With R = 8 rows the CUDA-core body needs 8 FMAs per K/V element pair, which
+// at HBM rate is most of the SM's FP32 issue; here one stage of 32 tokens is 32 MMAs.
+//   S^T[token][row] = K Q^T  : A = K tile (ldmatrix), B = Q^T held in registers for the item;
+//   O^T[dim][row]  += V^T P^T : A = V^T (ldmatrix.trans), B = P^T, obtained from the S^T
+//                               accumulator fragment by a packed bf16 8x8 transpose (movmatrix).
+// Rows R < 8 are padded with zero queries.  The loader stores 16-byte chunk c of token t at
+// chunk position c ^ (t & 7), so the eight row addresses of every ldmatrix hit distinct banks.
+// Lane l holds query rows 2(l%4), 2(l%4)+1; a row's running max is reduced over the 8 lanes
+// that share it; its running sum stays per lane until the end of the item.
+template <int R, int NW, int S, bool kMs>
+__device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
+                                                    int end, int w) {
+  const int lane = threadIdx.x & 31;
+  const int qd = lane & 3;   // row pair 2*qd, 2*qd+1 of the score / output fragments
+  const int gq = lane >> 2;  // token (scores) / dim (output) index within an 8-block
+  const int ctid = w * 32 + lane;
+  // ldmatrix row addresses (element offsets within a stage's K or V tile), swizzled chunks
+  const int lk_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lk_chunk = lane >> 4;  // K: m = token, k = dim
+  const int lv_tok = (lane & 7) + (lane >> 4) * 8, lv_chunk = (lane >> 3) & 1;  // V^T: m = dim, k = token
+
+  int stage_n = 0;
+  bool alive = true;
+
+  for (int pos = begin; pos < end; ++pos) {
+    const int4 ia = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields));
+    const int4 ib = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields + 4));
+    const int q_start = ia.y, q_len = ia.z, kv_head = ia.w;
+    const int kv_lo = ib.x, kv_hi = ib.y, diag = ib.z, slot_out = ib.w;
+    const int nst = (kv_hi - kv_lo + kStageTokens - 1) / kStageTokens;
+    const int rows_valid = q_len * p.group;
+
+    // B fragments of Q^T: row gq, dims 16ks + 2qd (+1) and 16ks + 8 + 2qd (+1)
+    uint32_t qb[8][2];
+    {
+      const int r = gq;
+      if (r < R && r < rows_valid) {
+        const int tok = q_start + r / p.group;
+        const int head = kv_head * p.group + r % p.group;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((size_t)tok * p.hqo + head) * kHeadDim);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          qb[ks][0] = __ldg(qrow + 8 * ks + qd);
+          qb[ks][1] = __ldg(qrow + 8 * ks + 4 + qd);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+      }
+    }
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    const int lim0 = diag + (2 * qd) / p.group, lim1 = diag + (2 * qd + 1) / p.group;
+
+    for (int st = 0; st < nst; ++st) {
+      const int n = stage_n + st;
+      if (n % NW != w) continue;
+      const int slot = n % S;
+      if (!alive) continue;
+      const bool got = spin_until_eq(&sm.slot_consumed[slot], n - S, p.err, &sm.abort) &&
+                       mbar_wait(&sm.full[slot], (n / S) & 1, p.err, &sm.abort);
+      if (!__all_sync(0xffffffffu, got)) {
+        alive = false;  // keep joining the named barriers; outputs of an aborted run are undefined
+        continue;
+      }
+      const int t0 = kv_lo + st * kStageTokens;
+      const int nt = min(kStageTokens, kv_hi - t0);
+      const int n_mt = nt > 16 ? 2 : 1;  // 16-token halves that hold any key of this stage
+      const __nv_bfloat16* Ks = &sm.kv[slot][0][0][0];
+      const __nv_bfloat16* Vs = &sm.kv[slot][1][0][0];
+
+      // ---- S^T = K Q^T -----------------------------------------------------------
+      float s[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+        if (mt < n_mt) {
+          const int tok = 16 * mt + lk_tok;
+          const __nv_bfloat16* row = Ks + tok * kHeadDim;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, row + (((2 * ks + lk_chunk) ^ (tok & 7)) * 8));
+            mma_16816(s[mt], a, qb[ks][0], qb[ks][1]);
+          }
+        }
+      }
+      // ---- online softmax (log2 domain) ------------------------------------------
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = 16 * mt + 8 * h + gq;
+          const bool in = t < nt;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool vis = in && (t0 + t <= (e ? lim1 : lim0));
+            const float v = vis ? s[mt][2 * h + e] * p.scale_log2 : -INFINITY;
+            s[mt][2 * h + e] = v;
+            mx[e] = fmaxf(mx[e], v);
+          }
+        }
+      }
+      float alpha[2], m_use[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+        const float m_new = fmaxf(m_run[e], mx[e]);
+        m_use[e] = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[e] = fast_exp2(m_run[e] - m_use[e]);
+        m_run[e] = m_new;
+        l_run[e] *= alpha[e];
+      }
+      uint32_t pb[2][2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float p0 = fast_exp2(s[mt][2 * h] - m_use[0]);
+          const float p1 = fast_exp2(s[mt][2 * h + 1] - m_use[1]);
+          l_run[0] += p0;
+          l_run[1] += p1;
+          pb[mt][h] = movmatrix_trans(f2_to_bf16x2(p0, p1));
+        }
+      }
+      // ---- O^T += V^T P^T -----------------------------------------------------------
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0];
+        o[mt][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        if (kt < n_mt) {
+          const int tok = 16 * kt + lv_tok;
+          const __nv_bfloat16* row = Vs + tok * kHeadDim;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, row + (((2 * mt + lv_chunk) ^ (tok & 7)) * 8));
+            mma_16816(o[mt], a, pb[kt][0], pb[kt][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        *reinterpret_cast<volatile int*>(&sm.slot_consumed[slot]) = n;
+        mbar_arrive(&sm.empty[slot]);
+      }
+    }
+    stage_n += nst;
+
+    // ---- merge the NW warp states of this item --------------------------------
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 4);
+      l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 8);
+      l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 16);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 2 * qd + e;
+      if (r < R) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          sm.macc[w][r][16 * mt + gq] = o[mt][e];
+          sm.macc[w][r][16 * mt + 8 + gq] = o[mt][2 + e];
+        }
+        if (gq == 0) {
+          sm.mm[w][r] = m_run[e];
+          sm.ml[w][r] = l_run[e];
+        }
+      }
+    }
+    named_bar_sync(1, NW * 32);
+    decode_finish_item<R, NW, S>(p, sm, ctid, q_start, kv_head, rows_valid, slot_out);
+  }
+}
+
+// kMma selects the tensor-core consumer (LDGSTS loader only, whose copies it swizzles).
+template <int R, int NW, int S, int kCopiers = 0, bool kMma = false>
 __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
+  static_assert(!kMma || kCopiers > 0, "the tensor-core consumer reads swizzled LDGSTS stages");
   constexpr bool kLdgsts = kCopiers > 0;
   constexpr int kLoaders = kLdgsts ? 1 + kCopiers : 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S>*>(smem_raw);
+  auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S, kMma>*>(smem_raw);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -598,17 +796,28 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
     sm.flag = 0;
     fence_mbar_init();
   }
+  if constexpr (kMma) {
+    // Rows past the end of a short stage are read by the P.V MMA with weight 0: they must hold
+    // finite values, so the V ring starts zeroed (later it holds earlier stages' V rows).
+    for (int i = threadIdx.x; i < S * kStageTokens * kHeadDim / 8; i += blockDim.x) {
+      const int st = i / (kStageTokens * kHeadDim / 8), rem = i % (kStageTokens * kHeadDim / 8);
+      reinterpret_cast<uint4*>(&sm.kv[st][1][0][0])[rem] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   __syncthreads();
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp >= kLoaders) {
-    decode_consumer<R, NW, S>(p, sm, begin, end, warp - kLoaders);
+    if constexpr (kMma)
+      decode_consumer_mma<R, NW, S>(p, sm, begin, end, warp - kLoaders);
+    else
+      decode_consumer<R, NW, S>(p, sm, begin, end, warp - kLoaders);
   } else if (!kLdgsts) {
     decode_producer<R, NW, S>(p, sm, begin, end);
   } else if (warp == 0) {
     decode_index_warp<R, NW, S>(p, sm, begin, end);
   } else {
-    decode_copier_warp<R, NW, S, kCopiers>(p, sm, begin, end, warp - 1);
+    decode_copier_warp<R, NW, S, kCopiers, kMma>(p, sm, begin, end, warp - 1);
   }
 }
 

@@ -65,24 +65,30 @@ struct fi_workspace {
 
 namespace {
 
-// Consumer warps, ring depth (32-token stages) and copier warps of the decode CTA per tile
-// height R, from a sweep on the Llama-3-8B-shaped (R = 4) and skewed long-context (R = 8)
-// batches: three copier warps keep ~0.9 of HBM bandwidth in flight; eight consumer warps (two
-// per SM sub-partition) hide the latency of the R <= 4 math; R = 8 needs more registers per
-// thread, so four.
-template <int R>
+// Consumer warps and ring depth (32-token stages) of the decode CTA, per tile height R and
+// consumer kind, from sweeps on GB300.  The 16-byte-copy loader (power-of-two page sizes) feeds
+// tensor-core consumers, which spend little issue per stage and keep no transpose scratch,
+// leaving the shared memory to a 12-stage ring; four of them hide the stage latency (two fall
+// behind).  Against the CUDA-core consumers they raised the Llama-3-8B-shaped batch (R = 4) from
+// 0.75 to 0.99 of the measured copy bandwidth, the skewed batch (R = 8) from 0.35 to 0.85, and
+// g = 1 / g = 2 batches of the same lengths from 0.96 / 0.90 to 1.00 / 0.99.  The bulk loader
+// (other page sizes) feeds CUDA-core consumers: eight warps hide the latency of the R <= 4 math;
+// R = 8 needs more registers per thread, so four.
+constexpr int kDecodeCopiers = 3;  // copier warps of the 16-byte-copy loader: ~0.9 of HBM in flight
+template <int R, bool kMma>
 struct DecodeConfig {
-  static constexpr int kWarps = R >= 8 ? 4 : 8;
-  static constexpr int kStages = R >= 8 ? 11 : 9;
-  static constexpr int kCopiers = 3;  // copier warps of the 16-byte-copy loader
+  static constexpr int kWarps = kMma ? 4 : (R >= 8 ? 4 : 8);
+  static constexpr int kStages = kMma ? 12 : (R >= 8 ? 11 : 9);
 };
 
 template <int R, int kCopiers>
 int launch_decode_as(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
-  constexpr int kDecodeWarps = DecodeConfig<R>::kWarps;
-  constexpr int kDecodeStages = DecodeConfig<R>::kStages;
-  using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages>;
-  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages, kCopiers>;
+  constexpr bool kMma = kCopiers > 0;
+  constexpr int kDecodeWarps = DecodeConfig<R, kMma>::kWarps;
+  constexpr int kDecodeStages = DecodeConfig<R, kMma>::kStages;
+  using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages, kMma>;
+  static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages, kCopiers, kMma>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -97,7 +103,7 @@ int launch_decode_as(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
 // Power-of-two page sizes take the 16-byte-copy loader, others the bulk-copy loader.
 template <int R>
 int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
-  return p.page_shift >= 0 ? launch_decode_as<R, DecodeConfig<R>::kCopiers>(grid, p, stream)
+  return p.page_shift >= 0 ? launch_decode_as<R, kDecodeCopiers>(grid, p, stream)
                            : launch_decode_as<R, 0>(grid, p, stream);
 }
 

@@ -1,4 +1,4 @@
-"""GPU parity of the CUDA-core decode path against the float64 oracle, through the C ABI."""
+"""GPU parity of the decode path (<= 8-row tiles) against the float64 oracle, through the C ABI."""
 import numpy as np
 import pytest
 
@@ -35,6 +35,10 @@ CASES = [
     (8, 4, 64, (1, 4), (4, 500), True, 4),       # g = 2, up to 4 query tokens (8 rows), causal
     (8, 8, 5, (1, 2), (2, 333), True, 9),        # g = 1, 2 query tokens
     (16, 8, 16, (1, 4), (0, 100), False, 1),     # one CTA does everything
+    (16, 4, 32, (1, 2), (2, 600), True, 6),      # g = 4, 2 query tokens: 8-row tiles, tensor-core consumer
+    (8, 8, 8, (1, 8), (8, 400), True, 3),        # g = 1, up to 8 query tokens: one causal limit per row
+    (32, 8, 24, (1, 1), (0, 700), False, 4),     # g = 4, page 24: bulk loader, CUDA-core consumer
+    (64, 8, 12, (1, 1), (0, 900), True, 5),      # g = 8, page 12: bulk loader, CUDA-core consumer
 ]
 
 
@@ -45,7 +49,7 @@ def test_random_decode_parity(case, seed):
     b = W.random_small_batch(1000 * case + seed, batch=17, num_qo_heads=hq, num_kv_heads=hk, page_size=ps,
                              causal=causal, q_len_range=qr, kv_len_range=kr, extra_pages=7)
     o, lse, ws = run_library(b, num_sms=n_cta)
-    assert ws.info()[1] == 0  # CUDA-core path
+    assert ws.info()[1] == 0  # decode path
     ro, rl = A.batch_attention(b)
     assert_close(o, lse, ro, rl)
 
