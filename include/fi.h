@@ -67,7 +67,8 @@ typedef struct fi_workspace fi_workspace;
  *   num_sms         SM budget of the attention kernels; 0 selects every SM of
  *                   the device (App. E: the SMs attention may use are given by
  *                   the user).  Each path runs k persistent CTAs per SM
- *                   (App. D.3: #CTA = k * #SM); both paths use k = 1.
+ *                   (App. D.3: #CTA = k * #SM): k = 1 for decode tiles, k = 2
+ *                   for 128-row tensor-core tiles.
  *   out             receives the handle (owned by the caller; release with
  *                   fi_workspace_destroy)
  *
@@ -131,8 +132,11 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
  * of partial outputs run in one persistent kernel of fixed grid; partial
  * states of a split row go to workspace slots and are merged in the order
  * the plan fixed (no atomic aggregation), so outputs are bit-identical from
- * run to run.  Decode tiles (<= 8 rows) run on CUDA cores; larger tiles run on
- * tcgen05 tensor cores (核心机制 4, paper §3.2.2).
+ * run to run.  Decode tiles (<= 8 rows) run warp-level MMAs with the KV tokens
+ * on the MMA's 16-row side (power-of-two page sizes) or CUDA cores (other page
+ * sizes); 128-row tiles run on tcgen05 tensor cores (核心机制 4, paper §3.2.2).
+ * A split row is merged by the last of its chunks to finish, summing the
+ * chunks in the plan's slot order.
  *
  *   q          DEVICE bf16 [total_q, num_qo_heads, 128]
  *   k_pages    DEVICE bf16 [num_pages, num_kv_heads, page_size, 128]
@@ -144,7 +148,9 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
  * Every row of o/lse that the plan covers is written; a row that sees no key
  * gets o = 0, lse = -inf.  Asynchronous on `stream`; capturable in a CUDA
  * graph, and a captured launch stays valid for later plans of the same
- * workspace that keep the same path and tile (fi_plan_info header[1..3]).
+ * workspace that keep the same path and tile (fi_plan_info header[1..3]); on
+ * the tensor-core path they must also keep the total query count (the launch
+ * holds a TMA descriptor of q whose extent is the plan's total_q).
  * Calls that share a workspace must not overlap on the GPU.
  * Errors: NO_PLAN, INVALID_ARG (null pointers, page id >= num_pages), CUDA.
  */

@@ -16,12 +16,12 @@ Readings (the algorithm listing itself is not on the page; these are listed in
 the design notes):
   * Path / tile (核心机制 4, paper §3.2.2): rows of a tile are (query token, query
     head in group) pairs.  If every request has l_q * g <= 8 rows, the whole
-    batch takes the CUDA-core decode path with one tile per (request, KV head)
+    batch takes the decode path with one tile per (request, KV head)
     covering all its query tokens, and rows_tile is the smallest of 1, 2, 4, 8
     that fits; otherwise the tensor-core path with 128-row tiles,
     tile_tokens = 128 // g.
-  * #CTA = k * (SM budget), k fixed per path, here 1 on both paths
-    (核心机制 7, paper App. D.3: #CTA = k x #SM).
+  * #CTA = k * (SM budget), k fixed per path: 1 for decode tiles, 2 for
+    tensor-core tiles (核心机制 7, paper App. D.3: #CTA = k x #SM).
   * KV heads count as separate units in the L_kv sum; L_kv is raised to l_min
     (default 256) and rounded up to a whole number of pages.
   * A unit (request, KV head, query tile) sees e keys: l_kv, or under the causal
@@ -87,7 +87,7 @@ class Plan:
 
 
 def choose_path(l_q, group: int):
-    """Tile choice (核心机制 4, paper §3.2.2): CUDA cores for tiny row counts, tensor cores otherwise."""
+    """Tile choice (核心机制 4, paper §3.2.2): decode tiles for <= 8 rows, 128-row tensor-core tiles otherwise."""
     max_rows = int(max((int(x) for x in l_q), default=0)) * group
     if max_rows <= DECODE_MAX_ROWS:
         tile_tokens = max(1, int(max((int(x) for x in l_q), default=1)))

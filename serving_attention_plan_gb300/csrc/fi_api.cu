@@ -337,7 +337,7 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
   a.lse = lse;
   a.part_o = reinterpret_cast<float*>(d + ws->off_part_o);
   a.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
-  a.counters = reinterpret_cast<uint32_t*>(d + ws->off_counters);
+  a.header = reinterpret_cast<const int32_t*>(d + ws->off_header);
   a.err = reinterpret_cast<int32_t*>(d + ws->off_err);
   a.num_pages = num_pages;
   a.page_size = ps;

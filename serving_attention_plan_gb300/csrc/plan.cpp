@@ -9,8 +9,9 @@
 //   核心机制 7 (paper App. D.2): only work longer than the chunk bound is split;
 //     the rest writes the final output directly.  App. D.3: partial outputs
 //     stay below 2 * #CTA tiles.
-//   核心机制 4 (paper §3.2.2): tiny query tiles run on CUDA cores (tensor-core
-//     MMA needs at least 16 rows), larger ones on tensor cores.
+//   核心机制 4 (paper §3.2.2): tiles of at most 8 rows take the decode kernel
+//     (the page runs them on CUDA cores, since an MMA needs at least 16 query
+//     rows), larger ones 128-row tensor-core tiles.
 //
 // Rules fixed where the page is silent (the same ones the test-side
 // restatement uses, so the two must agree bit for bit):
@@ -22,8 +23,8 @@
 //     number of pages;
 //   * a unit sees e keys (under the causal mask: those of its last token) and is
 //     cut into n = ceil(e / L_kv) chunks of cs = pages(ceil(e / n)) tokens;
-//   * #CTA = k * (SM budget) with k fixed per path (kDecodeCtasPerSm,
-//     kTcCtasPerSm; both 1: one persistent CTA per SM);
+//   * #CTA = k * (SM budget) with k fixed per path (kDecodeCtasPerSm = 1,
+//     kTcCtasPerSm = 2: two tensor-core CTAs share an SM);
 //   * item cost = alpha * rows + beta * chunk length;
 //   * sort by cost descending, ties by enumeration order; the queue pops the
 //     least-loaded CTA, ties to the lowest CTA id.

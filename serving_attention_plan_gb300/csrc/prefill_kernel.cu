@@ -11,8 +11,16 @@
 //     (术语与记号 "GQA 头组融合", App. A): a tile is 128/g tokens x g heads.
 //   实验与指标 (paper §4.2): causal prefill with the mask aligned to the end of
 //     each request's KV.
-//   核心机制 6-7 (paper §3.3.1, App. D): persistent CTAs walk the plan's queues;
-//     split rows are merged in-kernel by the last chunk to finish, in plan order.
+//   核心机制 6-7 (paper §3.3.1, App. D): persistent CTAs walk the plan's queues
+//     and write the partial states of split rows to workspace slots; the
+//     contraction follows in a second kernel chained by programmatic dependent
+//     launch, so its launch overlaps the attention tail and every SM shares it,
+//     each row summing its chunks in the plan's slot order.  (A 128-row partial
+//     state is 64 KB: merged by the last chunk's CTA alone, as the decode kernel
+//     does with its <= 8-row states, a row cut into 19 chunks took ~70 us.  An
+//     in-kernel grid barrier would need a cooperative launch, which the driver
+//     refuses for this grid: it counts one TMEM-allocating CTA per SM, although
+//     two run side by side.)
 //
 // Two CTAs per SM (each holds 256 of the SM's 512 TMEM columns and ~97 KB of
 // shared memory), 8 warps = 2 warpgroups each:
@@ -68,7 +76,6 @@ struct PrefillParams {
   float* lse;
   float* part_o;
   float* part_lse;
-  uint32_t* counters;
   int32_t* err;
   int num_pages;
   int page_size;
@@ -86,7 +93,6 @@ struct PrefillSmem {
   uint8_t v[kTileBytes];
   uint64_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, o_free;
   uint32_t tmem_base;
-  int flag;
   int abort;
 };
 
@@ -398,58 +404,6 @@ __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32
       }
     }
 
-    if (it.slot >= 0) {
-      // contraction of a split row: the last chunk to finish merges all slots in plan order
-      named_bar_sync(1, 128);
-      const int unit = __ldg(p.slot_unit + it.slot);
-      if (row == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(p.counters + unit, 1u);
-        const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
-        sm.flag = (prev == uint32_t(n_chunks - 1)) ? 1 : 0;
-        if (sm.flag) __threadfence();
-      }
-      named_bar_sync(1, 128);
-      if (sm.flag) {
-        if (row < rows_valid) {
-          const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
-          const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
-          float Mc = -INFINITY;
-          for (int c = 0; c < n_chunks; ++c) Mc = fmaxf(Mc, __ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row));
-          float Lc = 0.f;
-          if (Mc != -INFINITY) {
-            for (int c = 0; c < n_chunks; ++c)
-              Lc += fast_exp2(__ldcg(p.part_lse + (size_t)(first + c) * p.slot_rows + row) - Mc);
-          }
-          const float invL = (Mc != -INFINITY) ? 1.f / Lc : 0.f;
-          __nv_bfloat16* dst = p.o + out_row(p, it, row) * kHeadDim;
-          for (int dc = 0; dc < 4; ++dc) {
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            if (Mc != -INFINITY) {
-              for (int c = 0; c < n_chunks; ++c) {
-                const size_t srow = (size_t)(first + c) * p.slot_rows + row;
-                const float w = fast_exp2(__ldcg(p.part_lse + srow) - Mc) * invL;
-                const float4* src = reinterpret_cast<const float4*>(p.part_o + srow * kHeadDim + 32 * dc);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float4 a = __ldcg(src + j);
-                  v[4 * j] += w * a.x;
-                  v[4 * j + 1] += w * a.y;
-                  v[4 * j + 2] += w * a.z;
-                  v[4 * j + 3] += w * a.w;
-                }
-              }
-            }
-            store_bf16_32(dst + 32 * dc, v);
-          }
-          p.lse[out_row(p, it, row)] = lse_out(Mc == -INFINITY ? -INFINITY : Mc + fast_log2(Lc));
-        }
-        if (row == 0) p.counters[unit] = 0u;
-      }
-      named_bar_sync(1, 128);
-    }
   }
 }
 
@@ -457,6 +411,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ unsigned char smem_raw[];
+  // the contraction kernel that follows may be scheduled as soon as every CTA has started; it
+  // waits for this grid to complete before it reads a partial state
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // 128B-swizzled tiles want 1024-byte alignment
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -471,7 +428,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&sm.p_full, 4);
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.o_free, 4);
-    sm.flag = 0;
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -508,6 +464,85 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 5) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// contraction of split rows: a second kernel, chained by programmatic dependent launch
+// ---------------------------------------------------------------------------------------------
+// One warp per (unit, tile row); lane l owns dims 4l..4l+3, so each load of a partial row is one
+// coalesced 512-byte access.  A row's chunks are summed in slot (plan) order with up to
+// kContractUnroll loads in flight: the result does not depend on which warp runs the task, so
+// reruns are bit-identical.  The number of split units is read from the plan in device memory,
+// so a captured launch follows later plans.
+struct ContractParams {
+  const int32_t* header;
+  const int32_t* units;
+  const float* part_o;
+  const float* part_lse;
+  __nv_bfloat16* o;
+  float* lse;
+  int hqo;
+  int group;
+  int slot_rows;
+};
+
+constexpr int kContractThreads = 256;
+constexpr int kContractUnroll = 8;
+
+__global__ void __launch_bounds__(kContractThreads) contract_kernel(const __grid_constant__ ContractParams p) {
+  // the attention grid has completed and its partial states are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int n_warps = gridDim.x * (kContractThreads / 32);
+  const int tasks = __ldg(p.header + H_NUM_UNITS) * kTcRows;
+  for (int t = blockIdx.x * (kContractThreads / 32) + (threadIdx.x >> 5); t < tasks; t += n_warps) {
+    const int unit = t / kTcRows, row = t % kTcRows;
+    const int4 u = __ldg(reinterpret_cast<const int4*>(p.units + unit * kUnitFields));
+    const int first = u.x, n = u.y, q_start = u.z;
+    if (row >= u.w * p.group) continue;  // rows of the tile beyond its query tokens
+    const int kv_head = __ldg(p.units + unit * kUnitFields + U_KV_HEAD);
+    const float* lse_col = p.part_lse + (size_t)first * p.slot_rows + row;
+    float mx = -INFINITY;
+    for (int c = lane; c < n; c += 32) mx = fmaxf(mx, __ldcg(lse_col + (size_t)c * p.slot_rows));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float m_use = (mx == -INFINITY) ? 0.f : mx;
+    float sum = 0.f;
+    for (int c = lane; c < n; c += 32) sum += fast_exp2(__ldcg(lse_col + (size_t)c * p.slot_rows) - m_use);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float inv_l = (mx == -INFINITY) ? 0.f : 1.f / sum;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + ((size_t)first * p.slot_rows + row) * kHeadDim) + lane;
+    const size_t chunk_stride = (size_t)p.slot_rows * kHeadDim / 4;  // float4s between slots
+    for (int cb = 0; cb < n; cb += 32) {
+      const int c = cb + lane;
+      const float wl = (c < n) ? fast_exp2(__ldcg(lse_col + (size_t)c * p.slot_rows) - m_use) * inv_l : 0.f;
+      const int nb = min(32, n - cb);
+      for (int j = 0; j < nb; j += kContractUnroll) {
+        float4 a[kContractUnroll];
+#pragma unroll
+        for (int k = 0; k < kContractUnroll; ++k)
+          a[k] = (j + k < nb) ? __ldcg(src + (size_t)(cb + j + k) * chunk_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kContractUnroll; ++k) {
+          const float w = __shfl_sync(0xffffffffu, wl, (j + k) & 31);
+          if (j + k < nb) {
+            acc.x += w * a[k].x;
+            acc.y += w * a[k].y;
+            acc.z += w * a[k].z;
+            acc.w += w * a[k].w;
+          }
+        }
+      }
+    }
+    const size_t orow = (size_t)(q_start + row / p.group) * p.hqo + kv_head * p.group + row % p.group;
+    uint2 packed;
+    packed.x = f2_to_bf16x2(acc.x, acc.y);
+    packed.y = f2_to_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * lane) = packed;
+    if (lane == 0) p.lse[orow] = lse_out(mx == -INFINITY ? -INFINITY : mx + fast_log2(sum));
   }
 }
 
@@ -570,7 +605,6 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.lse = a.lse;
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
-  p.counters = a.counters;
   p.err = a.err;
   p.num_pages = a.num_pages;
   p.page_size = a.page_size;
@@ -589,8 +623,35 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   });
   if (attr != cudaSuccess) return record_cuda_error(attr, "cudaFuncSetAttribute(prefill_kernel)");
   prefill_kernel<<<a.num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
-  const cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) return FI_OK;
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    // the contraction of split rows; launched for every plan of this path (it reads the number
+    // of split units from the plan), so a captured pair stays valid across plans
+    ContractParams c;
+    c.header = a.header;
+    c.units = a.units;
+    c.part_o = a.part_o;
+    c.part_lse = a.part_lse;
+    c.o = p.o;
+    c.lse = a.lse;
+    c.hqo = a.hqo;
+    c.group = a.group;
+    c.slot_rows = kTcRows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(a.num_ctas));
+    cfg.blockDim = dim3(unsigned(kContractThreads));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, contract_kernel, c);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e == cudaSuccess) return FI_OK;
+    return record_cuda_error(e, "contract_kernel launch");
+  }
   cudaFuncAttributes fa;
   char what[256] = "prefill_kernel launch";
   if (cudaFuncGetAttributes(&fa, prefill_kernel) == cudaSuccess)

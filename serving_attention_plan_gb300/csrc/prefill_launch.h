@@ -20,7 +20,7 @@ struct PrefillArgs {
   float* lse;
   float* part_o;
   float* part_lse;
-  uint32_t* counters;
+  const int32_t* header;  // the plan's header in device memory
   int32_t* err;
   int num_pages;
   int page_size;

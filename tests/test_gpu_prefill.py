@@ -5,7 +5,7 @@ import pytest
 from oracle import attention as A
 from serving_attention_plan_gb300 import workloads as W
 
-from .gpu_helpers import assert_close, run_library, to_device, torch_mod
+from .gpu_helpers import alloc_out, assert_close, run_library, to_device, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -97,3 +97,45 @@ def test_shared_prefix_composable():
     torch.cuda.synchronize()
     ro, rl = A.batch_attention(sp.flat)
     assert_close(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl)
+
+
+def test_graph_replay_with_split_rows():
+    """A captured tensor-core launch replays bit-identically and follows re-plans of the same total_q,
+    with and without split rows (the split count is read from the plan, the launch is cooperative)."""
+    torch = torch_mod()
+    from serving_attention_plan_gb300 import binding as B
+    mk = lambda seed, kr: W.random_small_batch(seed, batch=3, num_qo_heads=8, num_kv_heads=2, page_size=16,
+                                               causal=True, q_len_range=(40, 40), kv_len_range=kr, scale=0.5)
+    plans = [mk(2200, (1500, 3000)), mk(2201, (40, 200)), mk(2202, (2000, 4000))]
+    pool = max(b.num_pages for b in plans)
+    devs = [to_device(b) for b in plans]
+    q = devs[0][0].clone()
+    k = torch.zeros((pool,) + tuple(devs[0][1].shape[1:]), dtype=devs[0][1].dtype, device="cuda")
+    v = torch.zeros_like(k)
+    ws = B.Workspace(4, 120, pool, 8, 2, 128, 16)   # 32 CTAs: long rows split into 3-4 chunks
+    o, lse = alloc_out(plans[0])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = None
+    for i, b in enumerate(plans):
+        qi, ki, vi = devs[i]
+        q.copy_(qi)
+        k[: ki.shape[0]].copy_(ki)
+        v[: vi.shape[0]].copy_(vi)
+        ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 16, True)
+        assert ws.info()[1] == 1 and (ws.info()[7] > 0) == (i != 1)
+        torch.cuda.synchronize()
+        if g is None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                ws.run(q, k, v, o, lse, stream=s)
+        outs = []
+        for _ in range(2):
+            o.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            outs.append((o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)))
+        assert ws.get_error() == 0
+        assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+        ro, rl = A.batch_attention(b)
+        assert_close(outs[0][0], outs[0][1], ro, rl)
