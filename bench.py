@@ -417,15 +417,22 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
         suf.plan()
         o, lse = torch.empty_like(pre.o), torch.empty_like(pre.lse)
 
+        def suffix_merged():
+            # suffix attention, each row written as prefix state ⊕ suffix state (fi_run_merge)
+            suf.ws.run_merge(suf.q, suf.k, suf.v, pre.o, pre.lse, o, lse)
+
         def step():
             pre.run()
-            suf.run()
-            B.merge_states(pre.o, pre.lse, suf.o, suf.lse, o, lse)
+            suffix_merged()
 
         ms = time_launches(torch, step, steps, warmup)
+        parts = {"prefix_attention_and_contraction": time_launches(torch, pre.run, steps, warmup) * 1e3,
+                 "suffix_decode_merged": time_launches(torch, suffix_merged, steps, warmup) * 1e3,
+                 "suffix_decode_alone": time_launches(torch, suf.run, steps, warmup) * 1e3}
         nbytes = kv_bytes(w.prefix) + kv_bytes(w.suffix)
         return {"us_per_batch": ms * 1e3, "kv_gbs_unique": nbytes / (ms * 1e-3) / 1e9,
                 "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "launches_per_step": 3,
+                "us_each_alone": parts,
                 "prefix_plan": pre.ws.info().tolist()[:10], "suffix_plan": suf.ws.info().tolist()[:10]}
     c = Case(w, torch, dev)
     ms = time_launches(torch, c.run, steps, warmup)

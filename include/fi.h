@@ -158,6 +158,27 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
            float* lse, void* stream);
 
 /*
+ * fi_run_merge -- fi_run, with each output row merged (⊕) into a given state.
+ *
+ * Source: 核心机制 2 "可组合格式" (paper §3.1.2, Fig. 3) and 术语与记号
+ * "Attention State 与 ⊕" (paper §2.2): the attention of one block-sparse
+ * sub-matrix (e.g. per-request suffixes, Br = 1) is combined with the state of
+ * another over a disjoint key set (e.g. the shared prefix, Br = #requests).
+ * Here the combination is done by the kernel that writes the rows, so no
+ * separate merge launch runs.
+ *
+ *   o_prev    DEVICE bf16 [total_q, num_qo_heads, 128]: the other state's O
+ *   lse_prev  DEVICE float32 [total_q, num_qo_heads]: its LSE (natural log;
+ *             -inf for a row that saw no key)
+ *   o, lse    written with (state of this plan) ⊕ (o_prev, lse_prev); they may
+ *             be the same buffers as o_prev / lse_prev (in place)
+ * Other arguments, behaviour and errors as fi_run; o_prev and lse_prev are
+ * both null (plain fi_run) or both set (else INVALID_ARG).
+ */
+int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const void* v_pages, int num_pages,
+                 const void* o_prev, const float* lse_prev, void* o, float* lse, void* stream);
+
+/*
  * fi_merge_states -- (O, LSE) of two disjoint KV sets merged into one.
  *
  * Source: 术语与记号 "Attention State 与 ⊕" (paper §2.2) and 核心机制 2

@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
     L.fi_workspace_set_cost_model.argtypes = [c_void_p, c_int64, c_int64, c_int32]
     L.fi_plan.argtypes = [c_void_p, P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]
     L.fi_run.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
+    L.fi_run_merge.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                               c_void_p]
     L.fi_merge_states.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                   c_void_p]
     L.fi_get_error.argtypes = [c_void_p, P32]
@@ -62,7 +64,7 @@ def lib() -> ctypes.CDLL:
     L.fi_last_error_message.argtypes = []
     L.fi_last_error_message.restype = ctypes.c_char_p
     for name in ("fi_workspace_create", "fi_workspace_destroy", "fi_workspace_set_cost_model", "fi_plan", "fi_run",
-                 "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count",
+                 "fi_run_merge", "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count",
                  "fi_decode_noalloc"):
         getattr(L, name).restype = c_int
     _LIB = L
@@ -153,6 +155,12 @@ class Workspace:
     def run(self, q, k_pages, v_pages, o, lse, stream=None):
         _check(lib().fi_run(self._h, _dptr(q), _dptr(k_pages), _dptr(v_pages), int(k_pages.shape[0]), _dptr(o),
                             _dptr(lse), _stream_ptr(stream)), "fi_run")
+
+    def run_merge(self, q, k_pages, v_pages, o_prev, lse_prev, o, lse, stream=None):
+        """fi_run with each output row merged (⊕) into the state (o_prev, lse_prev); o may be o_prev."""
+        _check(lib().fi_run_merge(self._h, _dptr(q), _dptr(k_pages), _dptr(v_pages), int(k_pages.shape[0]),
+                                  _dptr(o_prev), _dptr(lse_prev), _dptr(o), _dptr(lse), _stream_ptr(stream)),
+               "fi_run_merge")
 
     def info(self) -> np.ndarray:
         h = np.zeros(16, np.int32)

@@ -53,6 +53,8 @@ struct DecodeParams {
   const __nv_bfloat16* v;
   __nv_bfloat16* o;
   float* lse;
+  const __nv_bfloat16* o_prev;  // optional state of the same rows over other keys, merged into o / lse
+  const float* lse_prev;
   float* part_o;    // [slots][slot_rows][128] fp32, normalised O
   float* part_lse;  // [slots][slot_rows] fp32, log2 domain
   uint32_t* counters;
@@ -337,11 +339,14 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, Decode
         const int tok = q_start + r / p.group;
         const int head = kv_head * p.group + r % p.group;
         const size_t orow = (size_t)tok * p.hqo + head;
+        float lse_w = lse2;
+        if (p.o_prev)
+          merge_prev4(O, lse_w, *reinterpret_cast<const uint2*>(p.o_prev + orow * kHeadDim + 4 * dq), p.lse_prev[orow]);
         uint2 packed;
         packed.x = f2_to_bf16x2(O.x, O.y);
         packed.y = f2_to_bf16x2(O.z, O.w);
         *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
-        if (dq == 0) p.lse[orow] = lse2 * kLn2;
+        if (dq == 0) p.lse[orow] = lse_w * kLn2;
       } else {
         const size_t srow = (size_t)slot_out * p.slot_rows + r;
         *reinterpret_cast<float4*>(p.part_o + srow * kHeadDim + 4 * dq) = O;
@@ -392,11 +397,14 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, Decode
         const int tok = q_start + r / p.group;
         const int head = kv_head * p.group + r % p.group;
         const size_t orow = (size_t)tok * p.hqo + head;
+        float lse_w = (M == -INFINITY) ? -INFINITY : M + fast_log2(L);
+        if (p.o_prev)
+          merge_prev4(O, lse_w, *reinterpret_cast<const uint2*>(p.o_prev + orow * kHeadDim + 4 * dq), p.lse_prev[orow]);
         uint2 packed;
         packed.x = f2_to_bf16x2(O.x, O.y);
         packed.y = f2_to_bf16x2(O.z, O.w);
         *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * dq) = packed;
-        if (dq == 0) p.lse[orow] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(L)) * kLn2;
+        if (dq == 0) p.lse[orow] = lse_w * kLn2;
       }
       if (ctid == 0) p.counters[unit] = 0u;
     }

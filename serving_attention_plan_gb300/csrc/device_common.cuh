@@ -204,4 +204,22 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// ---- ⊕ with a state given in output form ----------------------------------------------------------
+// (O, lse2) of a row (normalised O, log2-domain LSE) merged with the state of the same row over a
+// disjoint key set, given as bf16 O (raw: dims d..d+3) and natural-log LSE; identity (0, -inf).
+__device__ __forceinline__ void merge_prev4(float4& O, float& lse2, uint2 prev_raw, float prev_lse) {
+  const float p2 = prev_lse * kLog2e;
+  const float m = fmaxf(lse2, p2);
+  if (m == -INFINITY) {
+    O = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const float wa = fast_exp2(lse2 - m), wb = fast_exp2(p2 - m);
+  const float z = wa + wb;
+  const float ia = wa / z, ib = wb / z;
+  const float2 b0 = bf16x2_to_f2(prev_raw.x), b1 = bf16x2_to_f2(prev_raw.y);
+  O = make_float4(ia * O.x + ib * b0.x, ia * O.y + ib * b0.y, ia * O.z + ib * b1.x, ia * O.w + ib * b1.y);
+  lse2 = m + fast_log2(z);
+}
+
 }  // namespace fi

@@ -277,7 +277,13 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
 
 int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_pages, int num_pages, void* o,
            float* lse, void* stream) {
+  return fi_run_merge(ws, q, k_pages, v_pages, num_pages, nullptr, nullptr, o, lse, stream);
+}
+
+int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const void* v_pages, int num_pages,
+                 const void* o_prev, const float* lse_prev, void* o, float* lse, void* stream) {
   if (ws == nullptr) return FI_ERR_INVALID_ARG;
+  if ((o_prev == nullptr) != (lse_prev == nullptr)) return FI_ERR_INVALID_ARG;
   if (!ws->has_plan) return FI_ERR_NO_PLAN;
   if (num_pages < 0 || ws->max_page >= num_pages) return FI_ERR_INVALID_ARG;
   const int32_t* h = ws->header;
@@ -291,7 +297,7 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
   char* d = ws->dbuf;
 
   if (h[fi::H_PATH] == fi::kPathDecode) {
-    fi::DecodeParams p;
+    fi::DecodeParams p{};
     p.cta_indptr = reinterpret_cast<const int32_t*>(d + ws->off_cta);
     p.items = reinterpret_cast<const int32_t*>(d + ws->off_items);
     p.units = reinterpret_cast<const int32_t*>(d + ws->off_units);
@@ -302,6 +308,8 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
     p.v = static_cast<const __nv_bfloat16*>(v_pages);
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
+    p.o_prev = static_cast<const __nv_bfloat16*>(o_prev);
+    p.lse_prev = lse_prev;
     p.part_o = reinterpret_cast<float*>(d + ws->off_part_o);
     p.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
     p.counters = reinterpret_cast<uint32_t*>(d + ws->off_counters);
@@ -324,7 +332,7 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
     }
   }
 
-  fi::PrefillArgs a;
+  fi::PrefillArgs a{};
   a.cta_indptr = reinterpret_cast<const int32_t*>(d + ws->off_cta);
   a.items = reinterpret_cast<const int32_t*>(d + ws->off_items);
   a.units = reinterpret_cast<const int32_t*>(d + ws->off_units);
@@ -335,6 +343,8 @@ int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_p
   a.v = v_pages;
   a.o = o;
   a.lse = lse;
+  a.o_prev = o_prev;
+  a.lse_prev = lse_prev;
   a.part_o = reinterpret_cast<float*>(d + ws->off_part_o);
   a.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
   a.header = reinterpret_cast<const int32_t*>(d + ws->off_header);

@@ -318,7 +318,7 @@ extern "C" int fi_decode_noalloc(const int32_t* qo_indptr, const int32_t* kv_ind
   if (cudaMemcpyAsync(d, h, staged, cudaMemcpyHostToDevice, s) != cudaSuccess) return FI_ERR_CUDA;
   if (cudaMemsetAsync(d + L.counters, 0, L.part_lse - L.counters, s) != cudaSuccess) return FI_ERR_CUDA;
 
-  fi::DecodeParams p;
+  fi::DecodeParams p{};  // value-initialised: optional fields (o_prev, lse_prev) stay null
   p.cta_indptr = reinterpret_cast<const int32_t*>(d + L.cta);
   p.items = reinterpret_cast<const int32_t*>(d + L.items);
   p.units = reinterpret_cast<const int32_t*>(d + L.units);

@@ -74,6 +74,8 @@ struct PrefillParams {
   const int32_t* kv_indices;
   __nv_bfloat16* o;
   float* lse;
+  const __nv_bfloat16* o_prev;  // optional state of the same rows over other keys, merged into o / lse
+  const float* lse_prev;
   float* part_o;
   float* part_lse;
   int32_t* err;
@@ -384,15 +386,43 @@ __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32
     }
     if (row < rows_valid) {
       if (it.slot < 0) {
-        __nv_bfloat16* dst = p.o + out_row(p, it, row) * kHeadDim;
+        const size_t orow = out_row(p, it, row);
+        __nv_bfloat16* dst = p.o + orow * kHeadDim;
+        float wa = inv, wb = 0.f;  // weights of this state (unnormalised O) and of the given one
+        if (p.o_prev) {
+          const float p2 = p.lse_prev[orow] * kLog2e;
+          const float m2 = fmaxf(lse2, p2);
+          if (m2 == -INFINITY) {
+            wa = 0.f;
+          } else {
+            const float a = fast_exp2(lse2 - m2), b = fast_exp2(p2 - m2);
+            wa = a * inv / (a + b);
+            wb = b / (a + b);
+            lse2 = m2 + fast_log2(a + b);
+          }
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[32 * c + j]) * inv;
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[32 * c + j]) * wa;
+          if (wb != 0.f) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.o_prev + orow * kHeadDim + 32 * c);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint4 raw = src[q4];
+              const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float2 f = bf16x2_to_f2(w4[h]);
+                v[8 * q4 + 2 * h] += wb * f.x;
+                v[8 * q4 + 2 * h + 1] += wb * f.y;
+              }
+            }
+          }
           store_bf16_32(dst + 32 * c, v);
         }
-        p.lse[out_row(p, it, row)] = lse_out(lse2);
+        p.lse[orow] = lse_out(lse2);
       } else {
         const size_t srow = (size_t)it.slot * p.slot_rows + row;
         float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kHeadDim);
@@ -482,6 +512,8 @@ struct ContractParams {
   const float* part_lse;
   __nv_bfloat16* o;
   float* lse;
+  const __nv_bfloat16* o_prev;
+  const float* lse_prev;
   int hqo;
   int group;
   int slot_rows;
@@ -538,11 +570,14 @@ __global__ void __launch_bounds__(kContractThreads) contract_kernel(const __grid
       }
     }
     const size_t orow = (size_t)(q_start + row / p.group) * p.hqo + kv_head * p.group + row % p.group;
+    float lse2 = (mx == -INFINITY) ? -INFINITY : mx + fast_log2(sum);
+    if (p.o_prev)
+      merge_prev4(acc, lse2, *reinterpret_cast<const uint2*>(p.o_prev + orow * kHeadDim + 4 * lane), p.lse_prev[orow]);
     uint2 packed;
     packed.x = f2_to_bf16x2(acc.x, acc.y);
     packed.y = f2_to_bf16x2(acc.z, acc.w);
     *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * lane) = packed;
-    if (lane == 0) p.lse[orow] = lse_out(mx == -INFINITY ? -INFINITY : mx + fast_log2(sum));
+    if (lane == 0) p.lse[orow] = lse_out(lse2);
   }
 }
 
@@ -595,7 +630,7 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
                 uint32_t(a.page_size), 1u))
     return FI_ERR_INVALID_ARG;
 
-  PrefillParams p;
+  PrefillParams p{};
   p.cta_indptr = a.cta_indptr;
   p.items = a.items;
   p.units = a.units;
@@ -603,6 +638,8 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.kv_indices = a.kv_indices;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.lse = a.lse;
+  p.o_prev = static_cast<const __nv_bfloat16*>(a.o_prev);
+  p.lse_prev = a.lse_prev;
   p.part_o = a.part_o;
   p.part_lse = a.part_lse;
   p.err = a.err;
@@ -627,13 +664,15 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (e == cudaSuccess) {
     // the contraction of split rows; launched for every plan of this path (it reads the number
     // of split units from the plan), so a captured pair stays valid across plans
-    ContractParams c;
+    ContractParams c{};
     c.header = a.header;
     c.units = a.units;
     c.part_o = a.part_o;
     c.part_lse = a.part_lse;
     c.o = p.o;
     c.lse = a.lse;
+    c.o_prev = p.o_prev;
+    c.lse_prev = a.lse_prev;
     c.hqo = a.hqo;
     c.group = a.group;
     c.slot_rows = kTcRows;

@@ -18,6 +18,8 @@ struct PrefillArgs {
   const void* v;
   void* o;
   float* lse;
+  const void* o_prev;      // optional: state of the same rows over a disjoint key set, merged in
+  const float* lse_prev;
   float* part_o;
   float* part_lse;
   const int32_t* header;  // the plan's header in device memory
