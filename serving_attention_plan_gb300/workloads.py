@@ -245,7 +245,43 @@ def shared_prefix_decode(n_req: int = 64, prefix_len: int = 8192, lo: int = 256,
     return SharedPrefixBatch(prefix, suffix, flat)
 
 
+# ---------------------------------------------------------------------------
+# Kernel-level length distributions (batch 16; constant / uniform / Zipf)
+# ---------------------------------------------------------------------------
+
+KERNEL_DISTS = ("constant", "uniform", "zipf")
+KERNEL_DIST_WORKLOADS = tuple(f"kernel_{d}_{m}" for m in ("decode", "prefill") for d in KERNEL_DISTS)
+
+
+def kernel_dist_lengths(rng: np.random.Generator, dist: str, batch: int = 16) -> np.ndarray:
+    """constant: 1024; uniform: U[512, 1024]; zipf: 512 * k, k ~ Zipf(2.5), capped at 16384 (mean ~1000)."""
+    if dist == "constant":
+        return np.full(batch, 1024, np.int64)
+    if dist == "uniform":
+        return rng.integers(512, 1025, size=batch).astype(np.int64)
+    if dist == "zipf":
+        return np.minimum(512 * rng.zipf(2.5, size=batch), 16384).astype(np.int64)
+    raise ValueError(dist)
+
+
+def kernel_dist(dist: str, mode: str, batch: int = 16, with_data: bool = True) -> PagedBatch:
+    """Batch 16, 32/8 heads, page 16: decode (one query token) or causal prefill (q = kv) over the lengths."""
+    seed = 10 + KERNEL_DIST_WORKLOADS.index(f"kernel_{dist}_{mode}")
+    rng = np.random.default_rng(seed)
+    lens = kernel_dist_lengths(rng, dist, batch)
+    if mode == "decode":
+        return make_paged_batch(rng, f"kernel_{dist}_decode", np.ones(batch, np.int64), lens, 32, 8, 16, False,
+                                with_data=with_data)
+    if mode == "prefill":
+        return make_paged_batch(rng, f"kernel_{dist}_prefill", lens, lens, 32, 8, 16, True, scale=0.5,
+                                with_data=with_data)
+    raise ValueError(mode)
+
+
 def by_name(name: str):
+    if name.startswith("kernel_"):
+        _, dist, mode = name.split("_")
+        return kernel_dist(dist, mode)
     return {
         "tiny_decode": tiny_decode,
         "llama3_8b_decode": llama3_8b_decode,

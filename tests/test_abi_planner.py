@@ -100,6 +100,38 @@ def test_workload_plans_match(lib, name):
         assert a["header"][1] == 1 and a["header"][2] == 32
 
 
+@pytest.mark.parametrize("name", W.KERNEL_DIST_WORKLOADS)
+def test_kernel_distribution_plans_match(lib, name):
+    """Kernel-level batches (16 requests; constant / uniform / Zipf lengths): C++ plan == restatement."""
+    dist, mode = name.split("_")[1:]
+    b = W.kernel_dist(dist, mode, with_data=False)
+    a = _compare(b.qo_indptr, b.kv_indptr, b.last_page_len, b.num_qo_heads, b.num_kv_heads, b.page_size, b.causal, 152)
+    assert a["header"][1] == (1 if mode == "prefill" else 0)
+
+
+def test_kernel_distribution_lengths():
+    """Lengths follow the stated distributions and are reproducible from the seed."""
+    import numpy as np
+    for name in W.KERNEL_DIST_WORKLOADS:
+        dist, mode = name.split("_")[1:]
+        b1 = W.kernel_dist(dist, mode, with_data=False)
+        b2 = W.kernel_dist(dist, mode, with_data=False)
+        assert np.array_equal(b1.kv_indptr, b2.kv_indptr) and np.array_equal(b1.last_page_len, b2.last_page_len)
+        n_p = np.diff(b1.kv_indptr)
+        lkv = (n_p - 1) * b1.page_size + b1.last_page_len
+        assert b1.batch_size == 16
+        if dist == "constant":
+            assert np.all(lkv == 1024)
+        elif dist == "uniform":
+            assert lkv.min() >= 512 and lkv.max() <= 1024
+        else:
+            assert np.all(lkv % 512 == 0) and lkv.min() >= 512 and lkv.max() <= 16384
+        if mode == "prefill":
+            assert np.array_equal(np.diff(b1.qo_indptr), lkv) and b1.causal
+        else:
+            assert np.all(np.diff(b1.qo_indptr) == 1) and not b1.causal
+
+
 def test_shared_prefix_plans_match(lib):
     sp = W.shared_prefix_decode()
     for part in (sp.prefix, sp.suffix):
