@@ -27,6 +27,14 @@ Readings where the pages are silent (each listed in the design notes):
   * Causal masks are aligned to the end of each request's KV: query token t
     (0-based within its request) sees keys j <= l_kv - l_q + t.
   * Page layout "HND" is [pages, H_kv, page_size, D]; "NHD" is [pages, page_size, H_kv, D].
+
+Attention variants (问题背景 挑战二 names sliding-window masks and Grok's logit
+soft-cap among the variants a serving library must carry; 核心机制 5, paper
+§3.2.3, treats them as logits transforms and masks of one template):
+  * Sliding window, read with causal masks: query token t, aligned at position
+    p = l_kv - l_q + t, sees keys p - window_left .. p (window_left + 1 keys).
+  * Logit soft-cap: the scaled logit x = scale * q.k becomes cap * tanh(x / cap)
+    before the softmax, so every logit lies in (-cap, cap).
 """
 from __future__ import annotations
 
@@ -83,39 +91,56 @@ def visible_counts(l_q: int, l_kv: int, causal: bool) -> np.ndarray:
     return np.clip(l_kv - l_q + t + 1, 0, l_kv)
 
 
-def attention_state(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, n_visible, scale: float):
-    """State (O, LSE) of each query row over its first n_visible[r] keys, in float64.
+def window_starts(l_q: int, l_kv: int, window_left: int) -> np.ndarray:
+    """First key each query token sees under a sliding window (0 without one): max(0, p - window_left)."""
+    t = np.arange(l_q, dtype=np.int64)
+    if window_left < 0:
+        return np.zeros(l_q, dtype=np.int64)
+    return np.maximum(0, l_kv - l_q + t - window_left)
 
-    s_j = scale * q . k_j ;  M = max_j s_j ;  LSE = M + log sum_j exp(s_j - M) ;
-    O = sum_j exp(s_j - LSE) v_j .  A row with no visible key gets (0, -inf).
+
+def attention_state(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, n_visible, scale: float, first=0,
+                    soft_cap: float = 0.0):
+    """State (O, LSE) of each query row over keys first[r] .. n_visible[r]-1, in float64.
+
+    s_j = scale * q . k_j (then cap * tanh(s_j / cap) when soft_cap > 0) ;  M = max_j s_j ;
+    LSE = M + log sum_j exp(s_j - M) ;  O = sum_j exp(s_j - LSE) v_j .
+    A row with no visible key gets (0, -inf).
     """
     q_rows = np.asarray(q_rows, dtype=np.float64)
     n_rows, d = q_rows.shape
     o = np.zeros((n_rows, v.shape[1] if v.ndim == 2 else d), dtype=np.float64)
     lse = np.full(n_rows, NEG_INF, dtype=np.float64)
     n_visible = np.broadcast_to(np.asarray(n_visible, dtype=np.int64), (n_rows,))
+    first = np.broadcast_to(np.asarray(first, dtype=np.int64), (n_rows,))
     if k.shape[0] == 0:
         return o, lse
     s = scale * (q_rows @ k.T)
+    if soft_cap > 0:
+        s = soft_cap * np.tanh(s / soft_cap)
     for r in range(n_rows):
-        n = int(n_visible[r])
-        if n <= 0:
+        lo, n = int(first[r]), int(n_visible[r])
+        if n <= lo:
             continue
-        sr = s[r, :n]
+        sr = s[r, lo:n]
         m = sr.max()
         w = np.exp(sr - m)
         z = w.sum()
         lse[r] = m + np.log(z)
-        o[r] = (w @ v[:n]) / z
+        o[r] = (w @ v[lo:n]) / z
     return o, lse
 
 
-def batch_attention(b, layout: str = "HND", requests=None, scale: float | None = None):
+def batch_attention(b, layout: str = "HND", requests=None, scale: float | None = None, window_left: int = -1,
+                    soft_cap: float = 0.0):
     """O [total_q, H_qo, D] and LSE [total_q, H_qo] (float64) for a paged batch.
 
     `b` carries the library's input arrays (see serving_attention_plan_gb300.workloads.PagedBatch).
-    Rows of requests not in `requests` (when given) are left as (0, -inf).
+    Rows of requests not in `requests` (when given) are left as (0, -inf).  A sliding window
+    (window_left >= 0) needs a causal batch.
     """
+    if window_left >= 0 and not b.causal:
+        raise ValueError("the sliding window is read with causal masks")
     d = b.head_dim
     scale = 1.0 / np.sqrt(d) if scale is None else scale
     g = b.num_qo_heads // b.num_kv_heads
@@ -129,19 +154,23 @@ def batch_attention(b, layout: str = "HND", requests=None, scale: float | None =
         if nq == 0:
             continue
         vis = visible_counts(nq, nk, b.causal)
+        lo = window_starts(nq, nk, window_left)
         for hk in range(b.num_kv_heads):
             k = gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, hk, layout)
             v = gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, hk, layout)
             for h in range(hk * g, (hk + 1) * g):
                 qr = bf16_to_f64(b.q[q0:q0 + nq, h])
-                oo, ll = attention_state(qr, k, v, vis, scale)
+                oo, ll = attention_state(qr, k, v, vis, scale, lo, soft_cap)
                 o[q0:q0 + nq, h] = oo
                 lse[q0:q0 + nq, h] = ll
     return o, lse
 
 
-def attention_rows(b, i: int, h: int, tokens, layout: str = "HND", scale: float | None = None):
+def attention_rows(b, i: int, h: int, tokens, layout: str = "HND", scale: float | None = None,
+                   window_left: int = -1, soft_cap: float = 0.0):
     """State of selected query tokens (0-based within request i) of query head h."""
+    if window_left >= 0 and not b.causal:
+        raise ValueError("the sliding window is read with causal masks")
     d = b.head_dim
     scale = 1.0 / np.sqrt(d) if scale is None else scale
     g = b.num_qo_heads // b.num_kv_heads
@@ -149,10 +178,11 @@ def attention_rows(b, i: int, h: int, tokens, layout: str = "HND", scale: float 
     nq, nk = int(l_q[i]), int(l_kv[i])
     tokens = np.asarray(tokens, dtype=np.int64)
     vis = visible_counts(nq, nk, b.causal)[tokens]
+    lo = window_starts(nq, nk, window_left)[tokens]
     k = gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, h // g, layout)
     v = gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, h // g, layout)
     qr = bf16_to_f64(b.q[int(b.qo_indptr[i]) + tokens, h])
-    return attention_state(qr, k, v, vis, scale)
+    return attention_state(qr, k, v, vis, scale, lo, soft_cap)
 
 
 def merge_states(o_a, lse_a, o_b, lse_b):

@@ -20,7 +20,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 TOL = 1e-12
 
 
-def _brute_force(b, scale):
+def _brute_force(b, scale, window_left=-1, soft_cap=0.0):
     """Explicit loops, Python floats, math.exp: the attention definition element by element."""
     d = b.head_dim
     g = b.num_qo_heads // b.num_kv_heads
@@ -44,11 +44,15 @@ def _brute_force(b, scale):
                 row = int(b.qo_indptr[i]) + t
                 q = [float(x) for x in A.bf16_to_f64(b.q[row, h])]
                 allowed = [j for j in range(lk) if (not b.causal) or j <= lk - lq + t]
+                if window_left >= 0:
+                    allowed = [j for j in allowed if j >= lk - lq + t - window_left]
                 if not allowed:
                     out_o[(row, h)] = [0.0] * d
                     out_l[(row, h)] = -math.inf
                     continue
                 s = {j: scale * sum(q[c] * keys[j][c] for c in range(d)) for j in allowed}
+                if soft_cap > 0:
+                    s = {j: soft_cap * math.tanh(x / soft_cap) for j, x in s.items()}
                 m = max(s.values())
                 z = sum(math.exp(s[j] - m) for j in allowed)
                 out_l[(row, h)] = m + math.log(z)
@@ -298,3 +302,104 @@ def test_workload_shapes():
     lq, lk = A.request_lengths(b.qo_indptr, b.kv_indptr, b.last_page_len, b.page_size)
     assert lk.tolist() == [37, 128, 255, 512] and lq.tolist() == [1, 1, 1, 1]
     assert b.k_pages.shape == (128, 2, 16, 128) and len(set(b.kv_indices.tolist())) == 59
+
+
+# ---- attention variants: sliding window and logit soft-cap (问题背景 挑战二; 核心机制 5, paper §3.2.3)
+
+@pytest.mark.parametrize("seed", range(4))
+def test_variants_brute_force_tiny(seed):
+    rng = np.random.default_rng(700 + seed)
+    b = W.random_small_batch(700 + seed, batch=3, num_qo_heads=4, num_kv_heads=2, page_size=3, causal=True,
+                             q_len_range=(1, 6), kv_len_range=(1, 14), head_dim=4)
+    w = int(rng.integers(0, 6))
+    cap = float(rng.choice([0.0, 0.7, 3.0]))
+    scale = 1.0 / math.sqrt(b.head_dim)
+    o, l = A.batch_attention(b, window_left=w, soft_cap=cap)
+    bo, bl = _brute_force(b, scale, window_left=w, soft_cap=cap)
+    for (row, h), val in bo.items():
+        np.testing.assert_allclose(o[row, h], val, atol=TOL)
+        if math.isinf(bl[(row, h)]):
+            assert np.isneginf(l[row, h])
+        else:
+            assert abs(l[row, h] - bl[(row, h)]) <= TOL
+
+
+def test_sliding_window_special_cases():
+    b = W.random_small_batch(720, batch=5, num_qo_heads=4, num_kv_heads=2, page_size=4, causal=True,
+                             q_len_range=(1, 7), kv_len_range=(1, 40), head_dim=8)
+    o, l = A.batch_attention(b)
+    # a window at least as long as every KV changes nothing
+    o2, l2 = A.batch_attention(b, window_left=64)
+    assert np.array_equal(o, o2) and np.array_equal(l, l2)
+    # window 0: each token sees only the key at its own position: O = v_p, LSE = scale q.k_p
+    o0, l0 = A.batch_attention(b, window_left=0)
+    scale = 1.0 / math.sqrt(b.head_dim)
+    lq, lk = A.request_lengths(b.qo_indptr, b.kv_indptr, b.last_page_len, b.page_size)
+    g = b.num_qo_heads // b.num_kv_heads
+    for i in range(b.batch_size):
+        for h in range(b.num_qo_heads):
+            k = A.gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, int(lk[i]), b.page_size, i, h // g)
+            v = A.gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, int(lk[i]), b.page_size, i, h // g)
+            for t in range(int(lq[i])):
+                row, pos = int(b.qo_indptr[i]) + t, int(lk[i] - lq[i] + t)
+                if pos < 0:
+                    assert np.isneginf(l0[row, h]) and np.all(o0[row, h] == 0)
+                    continue
+                q = A.bf16_to_f64(b.q[row, h])
+                np.testing.assert_allclose(o0[row, h], v[pos], atol=TOL)
+                assert abs(l0[row, h] - scale * float(q @ k[pos])) <= TOL
+
+
+def test_sliding_window_is_attention_over_the_window():
+    """Windowed state == plain state over the contiguous slice of keys p - w .. p."""
+    b = W.random_small_batch(721, batch=4, num_qo_heads=2, num_kv_heads=1, page_size=5, causal=True,
+                             q_len_range=(1, 9), kv_len_range=(5, 60), head_dim=8)
+    w = 7
+    o, l = A.batch_attention(b, window_left=w)
+    scale = 1.0 / math.sqrt(b.head_dim)
+    lq, lk = A.request_lengths(b.qo_indptr, b.kv_indptr, b.last_page_len, b.page_size)
+    for i in range(b.batch_size):
+        for h in range(b.num_qo_heads):
+            k = A.gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, int(lk[i]), b.page_size, i, 0)
+            v = A.gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, int(lk[i]), b.page_size, i, 0)
+            for t in range(int(lq[i])):
+                row, pos = int(b.qo_indptr[i]) + t, int(lk[i] - lq[i] + t)
+                lo = max(0, pos - w)
+                ks, vs = k[lo:pos + 1], v[lo:pos + 1]
+                oo, ll = A.attention_state(A.bf16_to_f64(b.q[row:row + 1, h]), ks, vs, ks.shape[0], scale)
+                np.testing.assert_allclose(o[row, h], oo[0], atol=TOL)
+                assert abs(l[row, h] - ll[0]) <= TOL or (np.isneginf(l[row, h]) and np.isneginf(ll[0]))
+
+
+def test_soft_cap_closed_forms_and_bounds():
+    rng = np.random.default_rng(722)
+    d, n = 16, 11
+    scale = 1.0 / math.sqrt(d)
+    q = 3.0 * rng.standard_normal((5, d))
+    k = 3.0 * rng.standard_normal((n, d))
+    v = rng.standard_normal((n, d))
+    # an enormous cap is the plain softmax
+    o, l = A.attention_state(q, k, v, n, scale)
+    o1, l1 = A.attention_state(q, k, v, n, scale, soft_cap=1e9)
+    np.testing.assert_allclose(o1, o, atol=1e-9)
+    np.testing.assert_allclose(l1, l, atol=1e-9)
+    for cap in (0.5, 2.0, 30.0):
+        # identical keys: weights stay uniform; LSE = log n + cap tanh(scale q.k / cap)
+        kk = np.tile(k[0], (n, 1))
+        oc, lc = A.attention_state(q, kk, v, n, scale, soft_cap=cap)
+        np.testing.assert_allclose(oc, np.tile(v.mean(0), (5, 1)), atol=TOL)
+        np.testing.assert_allclose(lc, math.log(n) + cap * np.tanh(scale * (q @ k[0]) / cap), atol=TOL)
+        # single key: O = v, LSE = cap tanh(scale q.k / cap)
+        o1k, l1k = A.attention_state(q, k[:1], v[:1], 1, scale, soft_cap=cap)
+        np.testing.assert_allclose(o1k, np.tile(v[0], (5, 1)), atol=TOL)
+        np.testing.assert_allclose(l1k, cap * np.tanh(scale * (q @ k[0]) / cap), atol=TOL)
+        # every capped logit lies in (-cap, cap): log n - cap < LSE < log n + cap
+        _, lb = A.attention_state(q, k, v, n, scale, soft_cap=cap)
+        assert np.all(lb < math.log(n) + cap) and np.all(lb > math.log(n) - cap)
+
+
+def test_window_needs_causal():
+    b = W.random_small_batch(723, batch=2, num_qo_heads=2, num_kv_heads=1, page_size=4, causal=False,
+                             kv_len_range=(1, 10), head_dim=8)
+    with pytest.raises(ValueError):
+        A.batch_attention(b, window_left=3)
