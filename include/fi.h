@@ -45,6 +45,10 @@ typedef enum fi_status {
   FI_ERR_NO_PLAN = 6      /* fi_run before a successful fi_plan on this workspace */
 } fi_status;
 
+/* Page layouts of k_pages / v_pages (fi_workspace_set_variant). */
+#define FI_KV_LAYOUT_HND 0 /* [num_pages, num_kv_heads, page_size, head_dim] */
+#define FI_KV_LAYOUT_NHD 1 /* [num_pages, page_size, num_kv_heads, head_dim] */
+
 /* Device-side error bits reported by fi_get_error. */
 #define FI_DEVERR_PAGE_OOB 0x1     /* a page index >= num_pages was skipped */
 #define FI_DEVERR_WAIT_TIMEOUT 0x2 /* a pipeline wait gave up after its iteration limit */
@@ -91,6 +95,29 @@ int fi_workspace_destroy(fi_workspace* ws);
  * next fi_plan.  Errors: INVALID_ARG (alpha < 0, beta < 1, l_min < 1).
  */
 int fi_workspace_set_cost_model(fi_workspace* ws, int64_t alpha, int64_t beta, int32_t l_min);
+
+/*
+ * fi_workspace_set_variant -- attention variant for the following fi_plan.
+ *
+ * Source: 问题背景 挑战二 (paper §1) names sliding-window masks and Grok's logit
+ * soft-cap among the variants a serving library must carry, and 核心机制 5
+ * (paper §3.2-3.2.3) treats masks, logits transforms and the KV layout as
+ * inputs of one attention template.
+ *
+ *   window_left      -1 for none; else a causal plan's query token t, aligned
+ *                    at key position p = l_kv - l_q + t, sees keys p - window_left
+ *                    .. p.  The plan reads only the keys windows reach.
+ *   logits_soft_cap  0 for none; else the scaled logit x = scale * q.k becomes
+ *                    cap * tanh(x / cap) before the softmax.
+ *   kv_layout        FI_KV_LAYOUT_HND or FI_KV_LAYOUT_NHD.
+ *
+ * The variant is fixed into the plan at fi_plan; fi_run uses the plan's.  A
+ * window on a non-causal batch makes fi_plan return UNSUPPORTED; so does NHD
+ * decode with a page size or a KV-head count that is not a power of two.  A captured fi_run keeps
+ * the variant it was captured with.  Default: none, none, HND.
+ * Errors: INVALID_ARG.
+ */
+int fi_workspace_set_variant(fi_workspace* ws, int32_t window_left, float logits_soft_cap, int32_t kv_layout);
 
 /*
  * fi_plan -- inspector step: compute the work plan for one batch on the CPU.
@@ -203,7 +230,7 @@ int fi_get_error(fi_workspace* ws, int32_t* err_bits);
 
 /*
  * fi_plan_info -- copy the current plan's 16-int32 header to host memory:
- *   [0] magic 0x46495031  [1] path (0 CUDA-core decode, 1 tensor core)
+ *   [0] magic 0x46495031  [1] path (0 decode tiles, 1 tensor-core tiles)
  *   [2] tokens per tile   [3] rows per tile  [4] group size g  [5] #CTA
  *   [6] work items  [7] split rows  [8] partial slots  [9] L_kv (tokens)
  *   [10] page_size  [11] causal  [12] num_qo_heads  [13] num_kv_heads
@@ -216,8 +243,9 @@ int fi_plan_info(const fi_workspace* ws, int32_t* header16);
  * fi_plan_compute -- the planner alone, on the host, with no device work.
  *
  * Same inputs and rules as fi_plan (kv_indices is not an input: plans never
- * depend on it), plus the SM budget (num_sms, as for fi_workspace_create) and
- * the cost model.  Writes the plan as one
+ * depend on it), plus the SM budget (num_sms, as for fi_workspace_create), the
+ * cost model and the sliding window (window_left, as for
+ * fi_workspace_set_variant; -1 for none).  Writes the plan as one
  * flat int32 array:
  *   header[16] | cta_indptr[num_ctas + 1] | items[n_items][8] (queue order)
  *   | split rows[n_split][8] | slot_to_split_row[n_slots]
@@ -229,7 +257,8 @@ int fi_plan_info(const fi_workspace* ws, int32_t* header16);
  */
 int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* last_page_len, int batch,
                     int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal, int num_sms,
-                    int64_t alpha, int64_t beta, int32_t l_min, int32_t* out, int64_t capacity, int64_t* out_len);
+                    int64_t alpha, int64_t beta, int32_t l_min, int32_t window_left, int32_t* out,
+                    int64_t capacity, int64_t* out_len);
 
 /*
  * fi_decode_noalloc -- the CUDA-core decode path without any allocation.

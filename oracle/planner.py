@@ -102,7 +102,11 @@ def choose_path(l_q, group: int):
 
 def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, page_size: int,
          causal: bool, num_sms: int, head_dim: int = 128, alpha: int = 1, beta: int = 1,
-         l_min: int = 256) -> Plan:
+         l_min: int = 256, window_left: int = -1) -> Plan:
+    """window_left >= 0: sliding window (causal plans only); each tile reads only the keys its
+    tokens' windows reach, from the first token's window start rounded down to a page."""
+    if window_left >= 0 and not causal:
+        raise ValueError("the sliding window is read with causal masks")
     qo = [int(x) for x in qo_indptr]
     kv = [int(x) for x in kv_indptr]
     last = [int(x) for x in last_page_len]
@@ -120,10 +124,27 @@ def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: i
     path, tile_tokens, rows_tile = choose_path(l_q, g)
     num_ctas = (TC_CTAS_PER_SM if path == PATH_TENSOR else DECODE_CTAS_PER_SM) * num_sms
 
-    # a3: KV chunk bound
+    def extent(i, q0, qn):
+        """Keys [lo, e) that tile rows q0 .. q0+qn-1 of request i can see."""
+        if not causal:
+            return 0, l_kv[i]
+        e = min(max(l_kv[i] - l_q[i] + q0 + qn, 0), l_kv[i])
+        lo = 0
+        if window_left >= 0:
+            lo = max(0, l_kv[i] - l_q[i] + q0 - window_left) // page_size * page_size
+            lo = min(lo, e)
+        return lo, e
+
+    # a3: KV chunk bound (with a window: the keys each tile reads, which is all a window touches)
     total = 0
     for i in range(batch):
-        total += num_kv_heads * _ceil_div(l_q[i], tile_tokens) * l_kv[i]
+        if window_left < 0:
+            total += num_kv_heads * _ceil_div(l_q[i], tile_tokens) * l_kv[i]
+        else:
+            for j in range(_ceil_div(l_q[i], tile_tokens)):
+                q0 = j * tile_tokens
+                lo, e = extent(i, q0, min(tile_tokens, l_q[i] - q0))
+                total += num_kv_heads * (e - lo)
     l_chunk = max(_ceil_div(total, num_ctas), l_min)
     l_chunk = _ceil_div(l_chunk, page_size) * page_size
 
@@ -135,18 +156,14 @@ def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: i
             for j in range(n_tiles):
                 q0 = j * tile_tokens
                 qn = min(tile_tokens, l_q[i] - q0)
-                if causal:
-                    e = min(max(l_kv[i] - l_q[i] + q0 + qn, 0), l_kv[i])
-                    diag = l_kv[i] - l_q[i] + q0
-                else:
-                    e = l_kv[i]
-                    diag = NOT_CAUSAL_DIAG
-                if e == 0:
+                lo_e, e = extent(i, q0, qn)
+                diag = l_kv[i] - l_q[i] + q0 if causal else NOT_CAUSAL_DIAG
+                if e - lo_e == 0:
                     n, cs = 1, 0
                 else:
-                    n = _ceil_div(e, l_chunk)
-                    cs = _ceil_div(_ceil_div(e, n), page_size) * page_size
-                    n = _ceil_div(e, cs)
+                    n = _ceil_div(e - lo_e, l_chunk)
+                    cs = _ceil_div(_ceil_div(e - lo_e, n), page_size) * page_size
+                    n = _ceil_div(e - lo_e, cs)
                 unit = -1
                 if n > 1:
                     unit = len(units)
@@ -154,7 +171,7 @@ def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: i
                                       kv_head=h))
                     slot_unit.extend([unit] * n)
                 for c in range(n):
-                    lo, hi = c * cs, min(e, (c + 1) * cs)
+                    lo, hi = lo_e + c * cs, min(e, lo_e + (c + 1) * cs)
                     items.append(dict(
                         request=i, kv_head=h, tile=j, chunk=c,
                         page_base=kv[i], q_start=qo[i] + q0, q_len=qn, kv_lo=lo, kv_hi=hi, diag=diag,

@@ -46,6 +46,7 @@ def lib() -> ctypes.CDLL:
     L.fi_workspace_create.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int, c_int, POINTER(c_void_p)]
     L.fi_workspace_destroy.argtypes = [c_void_p]
     L.fi_workspace_set_cost_model.argtypes = [c_void_p, c_int64, c_int64, c_int32]
+    L.fi_workspace_set_variant.argtypes = [c_void_p, c_int32, ctypes.c_float, c_int32]
     L.fi_plan.argtypes = [c_void_p, P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]
     L.fi_run.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     L.fi_run_merge.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -55,7 +56,7 @@ def lib() -> ctypes.CDLL:
     L.fi_get_error.argtypes = [c_void_p, P32]
     L.fi_plan_info.argtypes = [c_void_p, P32]
     L.fi_plan_compute.argtypes = [P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_int64,
-                                  c_int32, P32, c_int64, POINTER(c_int64)]
+                                  c_int32, c_int32, P32, c_int64, POINTER(c_int64)]
     L.fi_decode_noalloc.argtypes = [P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                                     c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     L.fi_device_sm_count.argtypes = [POINTER(c_int)]
@@ -63,7 +64,8 @@ def lib() -> ctypes.CDLL:
     L.fi_status_string.restype = ctypes.c_char_p
     L.fi_last_error_message.argtypes = []
     L.fi_last_error_message.restype = ctypes.c_char_p
-    for name in ("fi_workspace_create", "fi_workspace_destroy", "fi_workspace_set_cost_model", "fi_plan", "fi_run",
+    for name in ("fi_workspace_create", "fi_workspace_destroy", "fi_workspace_set_cost_model",
+                 "fi_workspace_set_variant", "fi_plan", "fi_run",
                  "fi_run_merge", "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count",
                  "fi_decode_noalloc"):
         getattr(L, name).restype = c_int
@@ -99,19 +101,20 @@ def _dptr(t) -> c_void_p:
 
 
 def plan_compute(qo_indptr, kv_indptr, last_page_len, num_qo_heads, num_kv_heads, page_size, causal, num_sms,
-                 head_dim=128, alpha=1, beta=1, l_min=256) -> np.ndarray:
+                 head_dim=128, alpha=1, beta=1, l_min=256, window_left=-1) -> np.ndarray:
     """The host planner alone (no GPU): returns the flat int32 plan."""
     L = lib()
     qo, kv, last = _i32(qo_indptr), _i32(kv_indptr), _i32(last_page_len)
     batch = qo.shape[0] - 1
     n = c_int64(0)
     st = L.fi_plan_compute(_p32(qo), _p32(kv), _p32(last), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                           int(causal), num_sms, alpha, beta, l_min, None, 0, ctypes.byref(n))
+                           int(causal), num_sms, alpha, beta, l_min, window_left, None, 0, ctypes.byref(n))
     if st not in (FI_OK, 2):
         _check(st, "fi_plan_compute")
     out = np.zeros(max(int(n.value), 1), dtype=np.int32)
     st = L.fi_plan_compute(_p32(qo), _p32(kv), _p32(last), batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                           int(causal), num_sms, alpha, beta, l_min, _p32(out), out.shape[0], ctypes.byref(n))
+                           int(causal), num_sms, alpha, beta, l_min, window_left, _p32(out), out.shape[0],
+                           ctypes.byref(n))
     _check(st, "fi_plan_compute")
     return out[: n.value]
 
@@ -144,6 +147,12 @@ class Workspace:
 
     def set_cost_model(self, alpha=1, beta=1, l_min=256):
         _check(lib().fi_workspace_set_cost_model(self._h, alpha, beta, l_min), "fi_workspace_set_cost_model")
+
+    def set_variant(self, window_left=-1, logits_soft_cap=0.0, kv_layout="HND"):
+        """Sliding window / logit soft-cap / page layout ("HND" or "NHD") for the following plan()."""
+        layout = {"HND": 0, "NHD": 1}[kv_layout]
+        _check(lib().fi_workspace_set_variant(self._h, int(window_left), float(logits_soft_cap), layout),
+               "fi_workspace_set_variant")
 
     def plan(self, qo_indptr, kv_indptr, kv_indices, last_page_len, page_size, causal, stream=None):
         qo, kv, idx, last = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)

@@ -37,6 +37,8 @@
 // Scores are kept in the log2 domain.
 #pragma once
 
+#include <climits>
+
 #include "device_common.cuh"
 #include "plan.h"
 
@@ -59,8 +61,9 @@ struct DecodeParams {
   float* part_lse;  // [slots][slot_rows] fp32, log2 domain
   uint32_t* counters;
   int32_t* err;
-  long long page_stride;  // elements per page (H_kv * page_size * 128)
-  long long head_stride;  // elements per page-head (page_size * 128)
+  long long page_stride;   // elements per page (H_kv * page_size * 128)
+  long long head_stride;   // elements between KV heads of a page (HND: page_size * 128; NHD: 128)
+  int token_shift;         // log2 of the elements between tokens of a page-head (HND: 7; NHD: log2(H_kv * 128))
   int num_pages;
   int page_size;
   int page_shift;  // log2(page_size) when it is a power of two (LDGSTS loader), else -1
@@ -68,7 +71,11 @@ struct DecodeParams {
   int group;
   int slot_rows;
   float scale_log2;
+  int window_left;  // >= 0: a row at key position p sees keys p - window_left .. p
+  float cap_log2;   // > 0: logit soft-cap in the log2 domain, s -> cap_log2 * tanh(s / cap_log2)
+  float inv_cap_log2;
 };
+
 
 constexpr int kStageTokens = 32;
 constexpr int kIdxDepth = 4;  // page-index prefetch distance of the bulk producer (stages)
@@ -231,7 +238,7 @@ __device__ __forceinline__ void decode_index_warp(const DecodeParams& p, DecodeS
 // rows, 16 bytes per lane per instruction.
 // Copy c (0..1023) of a stage: K/V = c / 512, token = (c % 512) / 16, 16-byte chunk = c % 16,
 // so each warp instruction moves two consecutive 256-byte rows.
-template <int R, int NW, int S, int kCopiers, bool kSwizzle, bool kMs>
+template <int R, int NW, int S, int kCopiers, bool kSwizzle, bool kNhd, bool kMs>
 __device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
                                                    int end, int cw) {
   const int lane = threadIdx.x & 31;
@@ -266,7 +273,13 @@ __device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, Decode
       const int seg = min(max((pos >> sh) - first, 0), 31);
       const int page = __shfl_sync(0xffffffffu, pg, seg);
       if (tok < nt && page >= 0) {
-        const long long off = (long long)page * p.page_stride + (long long)(pos & row_mask) * kHeadDim + (lane & 15) * 8;
+        // One 64-bit expression, the row term a shift: this loop issues a 16-byte copy per lane per
+        // step, and measured on GB300 a run-time 64-bit multiply here cost a third of the copy rate,
+        // as did forming the row term in 32 bits.
+        const long long off = (long long)page * p.page_stride +
+                              (kNhd ? (long long)(pos & row_mask) << p.token_shift
+                                    : (long long)(pos & row_mask) * kHeadDim) +
+                              (lane & 15) * 8;
         const int chunk = kSwizzle ? ((lane & 15) ^ (tok & 7)) : (lane & 15);
         cp_async_16(&sm.kv[slot][0][tok][chunk * 8], kb + off);
         cp_async_16(&sm.kv[slot][1][tok][chunk * 8], vb + off);
@@ -412,7 +425,7 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, Decode
   named_bar_sync(1, NW * 32);
 }
 
-template <int R, int NW, int S, bool kMs>
+template <int R, int NW, int S, bool kVar, bool kMs>
 __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin, int end,
                                                 int w) {
   constexpr int NT = 16 / R;  // tokens per half per sub-batch
@@ -438,8 +451,9 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
 #pragma unroll
     for (int r = 0; r < R; ++r) acc[r][0] = acc[r][1] = make_float2(0.f, 0.f);
     float m_run = -INFINITY, l_run = 0.f;
-    // token limit of my score row: key j visible iff j <= diag + (row / g)
+    // token limits of my score row: key j visible iff row_low <= j <= diag + (row / g)
     const int row_limit = diag + my_row / p.group;
+    const int row_low = (kVar && p.window_left >= 0) ? row_limit - p.window_left : INT_MIN;
 
     for (int st = 0; st < nst; ++st) {
       const int n = stage_n + st;
@@ -491,8 +505,13 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
         for (int j = 4; j < 16; ++j) s4[j & 3] += red[tl * kRedHalf + j * kRedRow + dl];
         const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const int t = b * 2 * NT + tl * NT + dl / R;
-        const bool vis = (t < nt) && (t0 + t <= row_limit);
-        sc[b] = vis ? s : -INFINITY;
+        bool vis = (t < nt) && (t0 + t <= row_limit);
+        float sv = s;
+        if constexpr (kVar) {
+          vis = vis && (t0 + t >= row_low);
+          if (p.cap_log2 > 0.f) sv = p.cap_log2 * tanh_exp2(s * p.inv_cap_log2);
+        }
+        sc[b] = vis ? sv : -INFINITY;
       }
 
       // ---- online softmax over the stage --------------------------------------
@@ -603,7 +622,7 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
 // chunk position c ^ (t & 7), so the eight row addresses of every ldmatrix hit distinct banks.
 // Lane l holds query rows 2(l%4), 2(l%4)+1; a row's running max is reduced over the 8 lanes
 // that share it; its running sum stays per lane until the end of the item.
-template <int R, int NW, int S, bool kMs>
+template <int R, int NW, int S, bool kVar, bool kMs>
 __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
                                                     int end, int w) {
   const int lane = threadIdx.x & 31;
@@ -648,6 +667,8 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     const int lim0 = diag + (2 * qd) / p.group, lim1 = diag + (2 * qd + 1) / p.group;
+    const int low0 = (kVar && p.window_left >= 0) ? lim0 - p.window_left : INT_MIN;
+    const int low1 = (kVar && p.window_left >= 0) ? lim1 - p.window_left : INT_MIN;
 
     for (int st = 0; st < nst; ++st) {
       const int n = stage_n + st;
@@ -692,8 +713,13 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
           const bool in = t < nt;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const bool vis = in && (t0 + t <= (e ? lim1 : lim0));
-            const float v = vis ? s[mt][2 * h + e] * p.scale_log2 : -INFINITY;
+            bool vis = in && (t0 + t <= (e ? lim1 : lim0));
+            float sv = s[mt][2 * h + e] * p.scale_log2;
+            if constexpr (kVar) {
+              vis = vis && (t0 + t >= (e ? low1 : low0));
+              if (p.cap_log2 > 0.f) sv = p.cap_log2 * tanh_exp2(sv * p.inv_cap_log2);
+            }
+            const float v = vis ? sv : -INFINITY;
             s[mt][2 * h + e] = v;
             mx[e] = fmaxf(mx[e], v);
           }
@@ -780,10 +806,15 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
 }
 
 // kMma selects the tensor-core consumer (LDGSTS loader only, whose copies it swizzles).
-template <int R, int NW, int S, int kCopiers = 0, bool kMma = false>
+// kFlags: kDecodeNhd (NHD pages, 16-byte-copy loader only), kDecodeVariant (sliding window / soft-cap).
+constexpr int kDecodeNhd = 1;
+constexpr int kDecodeVariant = 2;
+template <int R, int NW, int S, int kCopiers = 0, bool kMma = false, int kFlags = 0>
 __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   static_assert(!kMma || kCopiers > 0, "the tensor-core consumer reads swizzled LDGSTS stages");
+  static_assert(!(kFlags & kDecodeNhd) || kCopiers > 0, "NHD pages are read by the 16-byte-copy loader");
+  constexpr bool kVar = (kFlags & kDecodeVariant) != 0;
   constexpr bool kLdgsts = kCopiers > 0;
   constexpr int kLoaders = kLdgsts ? 1 + kCopiers : 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -817,15 +848,15 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp >= kLoaders) {
     if constexpr (kMma)
-      decode_consumer_mma<R, NW, S>(p, sm, begin, end, warp - kLoaders);
+      decode_consumer_mma<R, NW, S, kVar>(p, sm, begin, end, warp - kLoaders);
     else
-      decode_consumer<R, NW, S>(p, sm, begin, end, warp - kLoaders);
+      decode_consumer<R, NW, S, kVar>(p, sm, begin, end, warp - kLoaders);
   } else if (!kLdgsts) {
     decode_producer<R, NW, S>(p, sm, begin, end);
   } else if (warp == 0) {
     decode_index_warp<R, NW, S>(p, sm, begin, end);
   } else {
-    decode_copier_warp<R, NW, S, kCopiers, kMma>(p, sm, begin, end, warp - 1);
+    decode_copier_warp<R, NW, S, kCopiers, kMma, (kFlags & kDecodeNhd) != 0>(p, sm, begin, end, warp - 1);
   }
 }
 

@@ -170,6 +170,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// tanh from the identity tanh(y) = sign(y) (1 - e) / (1 + e), e = 2^(-2 |y| log2(e)): absolute error
+// ~1e-7 (the exp2 and reciprocal are the approximate hardware ones), where a direct tanh
+// approximation would carry ~5e-4 relative error into soft-capped logits near the cap.
+__device__ __forceinline__ float tanh_exp2(float y) {
+  float e, r;
+  const float a = fabsf(y);
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-2.8853900817779268f * a));  // -2 log2(e) |y|
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return copysignf((1.f - e) * r, y);
+}
+
 __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

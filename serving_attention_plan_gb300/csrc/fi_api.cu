@@ -47,6 +47,8 @@ struct fi_workspace {
   int hqo = 0, hkv = 0, head_dim = 0, num_sms = 0, max_ctas = 0;
   int64_t max_items = 0, max_units = 0, max_slots = 0;
   fi::CostModel cost;
+  fi::Variant variant;       // as set for the next fi_plan
+  fi::Variant plan_variant;  // the one the current plan was made with (used by fi_run)
 
   // segment byte offsets; [0, plan_bytes) is mirrored in pinned host memory
   size_t off_header = 0, off_cta = 0, off_items = 0, off_units = 0, off_slot_unit = 0, off_kv = 0, plan_bytes = 0;
@@ -81,14 +83,14 @@ struct DecodeConfig {
   static constexpr int kStages = kMma ? 12 : (R >= 8 ? 11 : 9);
 };
 
-template <int R, int kCopiers>
+template <int R, int kCopiers, int kFlags>
 int launch_decode_as(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
   constexpr bool kMma = kCopiers > 0;
   constexpr int kDecodeWarps = DecodeConfig<R, kMma>::kWarps;
   constexpr int kDecodeStages = DecodeConfig<R, kMma>::kStages;
   using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages, kMma>;
   static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
-  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages, kCopiers, kMma>;
+  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages, kCopiers, kMma, kFlags>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -100,12 +102,24 @@ int launch_decode_as(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
   return FI_OK;
 }
 
-// Power-of-two page sizes take the 16-byte-copy loader, others the bulk-copy loader.
+// Power-of-two page sizes take the 16-byte-copy loader, others the bulk-copy loader (HND only).
+// The page layout and the attention variant are template flags, so the plain HND path compiles
+// without a trace of them.
 template <int R>
-int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
-  return p.page_shift >= 0 ? launch_decode_as<R, kDecodeCopiers>(grid, p, stream)
-                           : launch_decode_as<R, 0>(grid, p, stream);
+int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream, bool nhd, bool var) {
+  constexpr int kN = fi::kDecodeNhd, kV = fi::kDecodeVariant;
+  if (p.page_shift >= 0) {
+    if (nhd)
+      return var ? launch_decode_as<R, kDecodeCopiers, kN | kV>(grid, p, stream)
+                 : launch_decode_as<R, kDecodeCopiers, kN>(grid, p, stream);
+    return var ? launch_decode_as<R, kDecodeCopiers, kV>(grid, p, stream)
+               : launch_decode_as<R, kDecodeCopiers, 0>(grid, p, stream);
+  }
+  if (nhd) return FI_ERR_UNSUPPORTED;
+  return var ? launch_decode_as<R, 0, kV>(grid, p, stream) : launch_decode_as<R, 0, 0>(grid, p, stream);
 }
+
+bool var_on(const fi::Variant& v) { return v.window_left >= 0 || v.soft_cap > 0.f; }
 
 }  // namespace
 
@@ -214,6 +228,16 @@ int fi_workspace_set_cost_model(fi_workspace* ws, int64_t alpha, int64_t beta, i
   return FI_OK;
 }
 
+int fi_workspace_set_variant(fi_workspace* ws, int32_t window_left, float logits_soft_cap, int32_t kv_layout) {
+  if (ws == nullptr || window_left < -1 || !(logits_soft_cap >= 0.f) || logits_soft_cap > 1e30f ||
+      (kv_layout != FI_KV_LAYOUT_HND && kv_layout != FI_KV_LAYOUT_NHD))
+    return FI_ERR_INVALID_ARG;
+  ws->variant.window_left = window_left;
+  ws->variant.soft_cap = logits_soft_cap;
+  ws->variant.kv_layout = kv_layout;
+  return FI_OK;
+}
+
 int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
             const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
             int causal, void* stream) {
@@ -221,7 +245,7 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   if (num_qo_heads != ws->hqo || num_kv_heads != ws->hkv || head_dim != ws->head_dim) return FI_ERR_INVALID_ARG;
   if (batch > ws->max_batch) return FI_ERR_CAPACITY;
   fi::PlanInput in{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                   causal, ws->num_sms};
+                   causal, ws->num_sms, ws->variant.window_left};
   int st = fi::validate_input(in);
   if (st != FI_OK) return st;
   const int64_t nnz = kv_indptr[batch];
@@ -235,6 +259,11 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   fi::Plan plan;
   st = fi::build_plan(in, ws->cost, &plan);
   if (st != FI_OK) return st;
+  // NHD decode reads page rows with the 16-byte-copy loader (power-of-two pages), which steps over
+  // tokens by a shift (power-of-two KV-head count)
+  if (ws->variant.kv_layout == FI_KV_LAYOUT_NHD && plan.header[fi::H_PATH] == fi::kPathDecode &&
+      ((page_size & (page_size - 1)) != 0 || (num_kv_heads & (num_kv_heads - 1)) != 0))
+    return FI_ERR_UNSUPPORTED;
   const int64_t n_items = plan.header[fi::H_NUM_ITEMS], n_units = plan.header[fi::H_NUM_UNITS],
                 n_slots = plan.header[fi::H_NUM_SLOTS];
   if (n_items > ws->max_items || n_units > ws->max_units || n_slots > ws->max_slots) return FI_ERR_CAPACITY;
@@ -272,6 +301,7 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   ws->plan_nnz = nnz;
   ws->plan_total_q = qo_indptr[batch];
   ws->has_plan = true;
+  ws->plan_variant = ws->variant;
   return FI_OK;
 }
 
@@ -314,8 +344,14 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     p.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
     p.counters = reinterpret_cast<uint32_t*>(d + ws->off_counters);
     p.err = reinterpret_cast<int32_t*>(d + ws->off_err);
+    const fi::Variant& var = ws->plan_variant;
+    const bool nhd = var.kv_layout == FI_KV_LAYOUT_NHD;
     p.page_stride = (long long)ws->hkv * ps * fi::kHeadDim;
-    p.head_stride = (long long)ps * fi::kHeadDim;
+    p.head_stride = nhd ? fi::kHeadDim : (long long)ps * fi::kHeadDim;
+    p.token_shift = nhd ? 7 + __builtin_ctz(unsigned(ws->hkv)) : 7;  // NHD plans have a power-of-two H_kv
+    p.window_left = var.window_left;
+    p.cap_log2 = var.soft_cap > 0.f ? var.soft_cap * fi::kLog2e : 0.f;
+    p.inv_cap_log2 = var.soft_cap > 0.f ? 1.f / p.cap_log2 : 0.f;
     p.num_pages = num_pages;
     p.page_size = ps;
     p.page_shift = (ps & (ps - 1)) == 0 ? __builtin_ctz(unsigned(ps)) : -1;
@@ -323,11 +359,12 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     p.group = h[fi::H_GROUP];
     p.slot_rows = fi::kTcRows;
     p.scale_log2 = scale_log2;
+    const bool variant = var_on(var);
     switch (h[fi::H_ROWS_TILE]) {
-      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s);
-      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s);
-      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s);
-      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s);
+      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
+      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
+      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
+      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
       default: return FI_ERR_UNSUPPORTED;
     }
   }
@@ -358,6 +395,9 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
   a.total_q = ws->plan_total_q;
   a.num_ctas = h[fi::H_NUM_CTAS];
   a.scale_log2 = scale_log2;
+  a.window_left = ws->plan_variant.window_left;
+  a.cap_log2 = ws->plan_variant.soft_cap > 0.f ? ws->plan_variant.soft_cap * fi::kLog2e : 0.f;
+  a.nhd = ws->plan_variant.kv_layout == FI_KV_LAYOUT_NHD ? 1 : 0;
   return fi::launch_prefill(a, s);
 }
 

@@ -53,6 +53,7 @@ int validate_input(const PlanInput& in) {
   if (in.num_qo_heads <= 0 || in.num_kv_heads <= 0 || in.page_size <= 0 || in.num_sms <= 0)
     return FI_ERR_INVALID_ARG;
   if (in.causal != 0 && in.causal != 1) return FI_ERR_INVALID_ARG;
+  if (in.window_left >= 0 && !in.causal) return FI_ERR_UNSUPPORTED;  // the window is read with causal masks
   if (in.head_dim != kHeadDim) return FI_ERR_UNSUPPORTED;
   if (in.num_qo_heads % in.num_kv_heads != 0) return FI_ERR_UNSUPPORTED;
   if (in.qo_indptr[0] != 0 || in.kv_indptr[0] != 0) return FI_ERR_INVALID_ARG;
@@ -103,9 +104,34 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
   }
   const int num_ctas = (path == kPathTensor ? kTcCtasPerSm : kDecodeCtasPerSm) * in.num_sms;
 
-  // a3: KV chunk bound
+  // keys [lo, e) that tile rows q0 .. q0+qn-1 of request i can see
+  auto extent = [&](int i, int64_t q0, int64_t qn, int64_t* lo, int64_t* e) {
+    if (!in.causal) {
+      *lo = 0;
+      *e = lkv[i];
+      return;
+    }
+    *e = std::min(std::max<int64_t>(lkv[i] - lq[i] + q0 + qn, 0), lkv[i]);
+    *lo = 0;
+    if (in.window_left >= 0) {
+      *lo = std::max<int64_t>(0, lkv[i] - lq[i] + q0 - in.window_left) / ps * ps;
+      *lo = std::min(*lo, *e);
+    }
+  };
+
+  // a3: KV chunk bound (with a window: the keys each tile reads, which is all a window touches)
   int64_t total = 0;
-  for (int i = 0; i < B; ++i) total += int64_t(in.num_kv_heads) * ceil_div(lq[i], tile_tokens) * lkv[i];
+  for (int i = 0; i < B; ++i) {
+    if (in.window_left < 0) {
+      total += int64_t(in.num_kv_heads) * ceil_div(lq[i], tile_tokens) * lkv[i];
+    } else {
+      for (int64_t j = 0; j < ceil_div(lq[i], tile_tokens); ++j) {
+        int64_t lo, e;
+        extent(i, j * tile_tokens, std::min<int64_t>(tile_tokens, lq[i] - j * tile_tokens), &lo, &e);
+        total += int64_t(in.num_kv_heads) * (e - lo);
+      }
+    }
+  }
   int64_t l_chunk = std::max<int64_t>(ceil_div(total, num_ctas), cm.l_min);
   l_chunk = ceil_div(l_chunk, ps) * ps;
   if (l_chunk > (int64_t(1) << 30)) return FI_ERR_UNSUPPORTED;
@@ -123,22 +149,17 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
       for (int64_t j = 0; j < n_tiles; ++j) {
         const int64_t q0 = j * tile_tokens;
         const int64_t qn = std::min<int64_t>(tile_tokens, lq[i] - q0);
-        int64_t e, diag;
-        if (in.causal) {
-          e = std::min(std::max<int64_t>(lkv[i] - lq[i] + q0 + qn, 0), lkv[i]);
-          diag = lkv[i] - lq[i] + q0;
-        } else {
-          e = lkv[i];
-          diag = kNotCausalDiag;
-        }
+        int64_t lo_e, e;
+        extent(i, q0, qn, &lo_e, &e);
+        const int64_t diag = in.causal ? lkv[i] - lq[i] + q0 : kNotCausalDiag;
         int64_t n, cs;
-        if (e == 0) {
+        if (e - lo_e == 0) {
           n = 1;
           cs = 0;
         } else {
-          n = ceil_div(e, l_chunk);
-          cs = ceil_div(ceil_div(e, n), ps) * ps;
-          n = ceil_div(e, cs);
+          n = ceil_div(e - lo_e, l_chunk);
+          cs = ceil_div(ceil_div(e - lo_e, n), ps) * ps;
+          n = ceil_div(e - lo_e, cs);
         }
         int32_t first_slot = -1;
         if (n > 1) {
@@ -150,7 +171,7 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
           slot_unit.insert(slot_unit.end(), static_cast<size_t>(n), unit);
         }
         for (int64_t c = 0; c < n; ++c) {
-          const int64_t lo = c * cs, hi = std::min(e, (c + 1) * cs);
+          const int64_t lo = lo_e + c * cs, hi = std::min(e, lo_e + (c + 1) * cs);
           Work w;
           w.f[I_PAGE_BASE] = in.kv_indptr[i];
           w.f[I_Q_START] = in.qo_indptr[i] + static_cast<int32_t>(q0);
@@ -224,11 +245,11 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
 
 extern "C" int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* last_page_len,
                                int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal,
-                               int num_sms, int64_t alpha, int64_t beta, int32_t l_min, int32_t* out,
-                               int64_t capacity, int64_t* out_len) {
+                               int num_sms, int64_t alpha, int64_t beta, int32_t l_min, int32_t window_left,
+                               int32_t* out, int64_t capacity, int64_t* out_len) {
   if (out_len == nullptr) return FI_ERR_INVALID_ARG;
   fi::PlanInput in{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                   causal, num_sms};
+                   causal, num_sms, window_left};
   fi::CostModel cm;
   cm.alpha = alpha;
   cm.beta = beta;

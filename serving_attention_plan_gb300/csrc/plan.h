@@ -52,6 +52,15 @@ struct PlanInput {
   int page_size;
   int causal;
   int num_sms;  // SM budget; the plan's #CTA is k * num_sms with k fixed per path
+  int window_left = -1;  // >= 0: sliding window (causal plans): token at position p sees keys p - w .. p
+};
+
+// Attention variant of a plan (问题背景 挑战二; 核心机制 5, paper §3.2.3): a sliding window on
+// causal masks, a logit soft-cap, and the page layout.
+struct Variant {
+  int window_left = -1;  // < 0: none
+  float soft_cap = 0.f;  // <= 0: none
+  int kv_layout = 0;     // FI_KV_LAYOUT_HND or FI_KV_LAYOUT_NHD
 };
 
 struct Plan {

@@ -87,6 +87,8 @@ struct PrefillParams {
   int slot_rows;
   uint32_t q_tile_bytes;  // bytes of one Q tile as TMA writes it (2 halves x rows x 128 B)
   float scale_log2;
+  int window_left;   // >= 0: a row at key position p sees keys p - window_left .. p
+  float cap_log2;    // > 0: logit soft-cap in the log2 domain, s -> cap_log2 * tanh(s / cap_log2)
 };
 
 struct PrefillSmem {
@@ -118,6 +120,7 @@ struct Item {
 // ---------------------------------------------------------------------------------------------
 // warp 4: TMA producer
 // ---------------------------------------------------------------------------------------------
+template <bool kNhd>
 __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                          const CUtensorMap* tm_v, int begin, int end) {
   const int lane = threadIdx.x & 31;
@@ -140,33 +143,42 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
     }
     for (int t = 0; t < n_tiles; ++t) {
       const int base = it.kv_lo + t * kTile;
-      int z = oob_page;  // out-of-range page-head coordinate: the box reads as zeros
+      // out-of-range page(-head) coordinate: the box reads as zeros
+      int z = kNhd ? p.num_pages : oob_page;
       if (lane < ppt) {
         const int pp = base / ps + lane;
         if (pp * ps < it.kv_hi) {
           const int page = __ldg(p.kv_indices + it.page_base + pp);
           if (page >= 0 && page < p.num_pages) {
-            z = page * p.hkv + it.kv_head;
+            z = kNhd ? page : page * p.hkv + it.kv_head;
           } else {
             atomicOr(p.err, FI_DEVERR_PAGE_OOB);
           }
         }
       }
+      // one page of one KV head: HND box (64 dims, page_size tokens, 1 page-head), NHD box
+      // (64 dims, 1 head, page_size tokens, 1 page)
+      auto load_page = [&](uint8_t* dst, const CUtensorMap* tm, int x, uint64_t* bar) {
+        if constexpr (kNhd)
+          tc::tma_load_4d(dst, tm, x, it.kv_head, 0, z, bar);
+        else
+          tc::tma_load_3d(dst, tm, x, 0, z, bar);
+      };
       if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_empty, (tt - 1) & 1, p.err, &sm.abort));
       if (!ok) break;
       if (lane == 0) mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
       __syncwarp();
       if (lane < ppt) {
-        tc::tma_load_3d(sm.k + lane * ps * 128, tm_k, 0, 0, z, &sm.k_full);
-        tc::tma_load_3d(sm.k + kHalfBytes + lane * ps * 128, tm_k, 64, 0, z, &sm.k_full);
+        load_page(sm.k + lane * ps * 128, tm_k, 0, &sm.k_full);
+        load_page(sm.k + kHalfBytes + lane * ps * 128, tm_k, 64, &sm.k_full);
       }
       if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_empty, (tt - 1) & 1, p.err, &sm.abort));
       if (!ok) break;
       if (lane == 0) mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
       __syncwarp();
       if (lane < ppt) {
-        tc::tma_load_3d(sm.v + lane * ps * 128, tm_v, 0, 0, z, &sm.v_full);
-        tc::tma_load_3d(sm.v + kHalfBytes + lane * ps * 128, tm_v, 64, 0, z, &sm.v_full);
+        load_page(sm.v + lane * ps * 128, tm_v, 0, &sm.v_full);
+        load_page(sm.v + kHalfBytes + lane * ps * 128, tm_v, 64, &sm.v_full);
       }
       ++tt;
     }
@@ -255,10 +267,12 @@ __device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst_ptr, const floa
 
 __device__ __forceinline__ float lse_out(float lse2) { return (lse2 == -INFINITY) ? -INFINITY : lse2 * kLn2; }
 
-// One KV tile: scores -> mask -> online-softmax update -> P into the S columns of TMEM.
-template <bool kMasked>
-__device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lim, float scale, float& m, float& l,
-                                             bool first, PrefillSmem& sm, int tt, const PrefillParams& p,
+
+// One KV tile: scores -> (soft-cap) -> mask keys outside [lo, lim) -> online-softmax update -> P
+// into the S columns of TMEM.
+template <bool kMasked, bool kCap>
+__device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lo, int lim, float scale, float& m,
+                                             float& l, bool first, PrefillSmem& sm, int tt, const PrefillParams& p,
                                              bool& alive) {
   uint32_t s[kTile];
   tc::tmem_ld32(t_lane + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
@@ -266,13 +280,20 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lim, flo
   tc::tmem_ld32(t_lane + kColS + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
   tc::tmem_ld32(t_lane + kColS + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
   tc::tmem_wait_ld();
-  // row maximum of the raw scores with 8 independent partial maxima
+  if (kCap) {
+    // capped logits in the log2 domain; the scale is then already applied
+    const float in_scale = scale / p.cap_log2;
+#pragma unroll
+    for (int j = 0; j < kTile; ++j) s[j] = __float_as_uint(p.cap_log2 * tanh_exp2(__uint_as_float(s[j]) * in_scale));
+    scale = 1.f;
+  }
+  // row maximum of the (scaled) scores with 8 independent partial maxima
   float mx8[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
 #pragma unroll
   for (int j = 0; j < kTile; ++j) {
-    if (kMasked) s[j] = (j < lim) ? s[j] : __float_as_uint(-INFINITY);
+    if (kMasked) s[j] = (j < lim && j >= lo) ? s[j] : __float_as_uint(-INFINITY);
     mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(s[j]));
   }
   const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
@@ -326,6 +347,8 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lim, flo
   }
 }
 
+// kVar: the plan has a sliding window or a logit soft-cap (compiled out of the plain kernel).
+template <bool kVar>
 __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
   const int row = threadIdx.x;  // 0..127 == TMEM lane
   const int warp = row >> 5;
@@ -345,13 +368,22 @@ __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32
     for (int t = 0; t < n_tiles; ++t) {
       const int base = it.kv_lo + t * kTile;
       const int lim = max(0, min(kTile, min(it.kv_hi - base, it.diag + u + 1 - base)));
+      // sliding window: keys below diag + u - window_left are masked
+      const int lo = (kVar && p.window_left >= 0) ? min(kTile, max(0, it.diag + u - p.window_left - base)) : 0;
       alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.s_full, tt & 1, p.err, &sm.abort));
       if (alive) {
         tc::fence_after_sync();
-        if (__all_sync(0xffffffffu, lim >= kTile)) {
-          softmax_tile<false>(t_lane, lim, scale, m, l, t == 0, sm, tt, p, alive);
+        const bool full = __all_sync(0xffffffffu, lim >= kTile && lo <= 0);
+        if (kVar && p.cap_log2 > 0.f) {
+          if (full)
+            softmax_tile<false, true>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
+          else
+            softmax_tile<true, true>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
         } else {
-          softmax_tile<true>(t_lane, lim, scale, m, l, t == 0, sm, tt, p, alive);
+          if (full)
+            softmax_tile<false, false>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
+          else
+            softmax_tile<true, false>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
         }
         tc::fence_before_sync();
       }
@@ -437,6 +469,7 @@ __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32
   }
 }
 
+template <bool kVar, bool kNhd>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -480,11 +513,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) atomicOr(p.err, FI_DEVERR_TMEM);
   } else if (warp < 4) {
     tc::regs_increase<kSoftmaxRegs>();
-    softmax_epilogue(p, sm, tmem, begin, end);
+    softmax_epilogue<kVar>(p, sm, tmem, begin, end);
   } else {
     tc::regs_decrease<kControlRegs>();
     if (warp == 4) {
-      producer(p, sm, &tm_q, &tm_k, &tm_v, begin, end);
+      producer<kNhd>(p, sm, &tm_q, &tm_k, &tm_v, begin, end);
     } else if (warp == 5 && (threadIdx.x & 31) == 0) {
       mma_issuer(p, sm, tmem, begin, end);
     }
@@ -606,6 +639,19 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// NHD pages [pages, page_size, H_kv, 128]: dims (dim, head, token in page, page); a box is 64 dims
+// of one head and one page, i.e. page_size rows of 128 B, as the HND box lands.
+bool make_map_nhd(CUtensorMap* m, const void* base, uint64_t hkv, uint64_t page_size, uint64_t pages) {
+  const uint64_t row = uint64_t(kHeadDim) * 2;
+  const cuuint64_t dims[4] = {uint64_t(kHeadDim), hkv, page_size, pages};
+  const cuuint64_t strides[3] = {row, row * hkv, row * hkv * page_size};
+  const cuuint32_t box[4] = {64u, 1u, uint32_t(page_size), 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
@@ -624,11 +670,16 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     return FI_ERR_INVALID_ARG;
   // k, v: (dim, token in page, page * H_kv + head); a box is one page-head half
   const uint64_t page_heads = uint64_t(a.num_pages) * a.hkv;
-  if (!make_map(&tk, a.k, uint64_t(a.page_size), page_heads, row_bytes, row_bytes * a.page_size,
-                uint32_t(a.page_size), 1u) ||
-      !make_map(&tv, a.v, uint64_t(a.page_size), page_heads, row_bytes, row_bytes * a.page_size,
-                uint32_t(a.page_size), 1u))
+  if (a.nhd) {
+    if (!make_map_nhd(&tk, a.k, uint64_t(a.hkv), uint64_t(a.page_size), uint64_t(a.num_pages)) ||
+        !make_map_nhd(&tv, a.v, uint64_t(a.hkv), uint64_t(a.page_size), uint64_t(a.num_pages)))
+      return FI_ERR_INVALID_ARG;
+  } else if (!make_map(&tk, a.k, uint64_t(a.page_size), page_heads, row_bytes, row_bytes * a.page_size,
+                       uint32_t(a.page_size), 1u) ||
+             !make_map(&tv, a.v, uint64_t(a.page_size), page_heads, row_bytes, row_bytes * a.page_size,
+                       uint32_t(a.page_size), 1u)) {
     return FI_ERR_INVALID_ARG;
+  }
 
   PrefillParams p{};
   p.cta_indptr = a.cta_indptr;
@@ -651,15 +702,24 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.slot_rows = kTcRows;
   p.q_tile_bytes = uint32_t(2 * 128 * a.group * a.tile_tokens);
   p.scale_log2 = a.scale_log2;
+  p.window_left = a.window_left;
+  p.cap_log2 = a.cap_log2;
 
   const size_t smem = sizeof(PrefillSmem) + 1024;
+  // the attention variant and the page layout are template flags: the plain HND kernel carries neither
+  const bool var = a.window_left >= 0 || a.cap_log2 > 0.f;
+  using Kernel = void (*)(PrefillParams, CUtensorMap, CUtensorMap, CUtensorMap);
+  const Kernel kernels[2][2] = {{prefill_kernel<false, false>, prefill_kernel<false, true>},
+                                {prefill_kernel<true, false>, prefill_kernel<true, true>}};
+  const Kernel kernel = kernels[var ? 1 : 0][a.nhd ? 1 : 0];
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    for (int i = 0; i < 4 && attr == cudaSuccess; ++i)
+      attr = cudaFuncSetAttribute(kernels[i / 2][i % 2], cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   });
   if (attr != cudaSuccess) return record_cuda_error(attr, "cudaFuncSetAttribute(prefill_kernel)");
-  prefill_kernel<<<a.num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
+  kernel<<<a.num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) {
     // the contraction of split rows; launched for every plan of this path (it reads the number
@@ -693,7 +753,7 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   }
   cudaFuncAttributes fa;
   char what[256] = "prefill_kernel launch";
-  if (cudaFuncGetAttributes(&fa, prefill_kernel) == cudaSuccess)
+  if (cudaFuncGetAttributes(&fa, kernel) == cudaSuccess)
     snprintf(what, sizeof(what), "prefill_kernel launch (regs %d, max threads %d, static smem %zu, dyn smem %zu/%d, local %zu)",
              fa.numRegs, fa.maxThreadsPerBlock, fa.sharedSizeBytes, smem, fa.maxDynamicSharedSizeBytes,
              fa.localSizeBytes);

@@ -33,6 +33,9 @@ struct PrefillArgs {
   int total_q;   // rows of q / o (capacity of the workspace)
   int num_ctas;
   float scale_log2;
+  int window_left;  // < 0: none
+  float cap_log2;   // <= 0: no soft-cap; else cap * log2(e)
+  int nhd;          // page layout NHD instead of HND
 };
 
 // Returns an fi_status.

@@ -176,3 +176,21 @@ def test_tensor_core_path_page_size_rule(lib):
     with pytest.raises(B.FiError) as ei:
         B.plan_compute(qo, kv, last, 8, 2, 1, True, 4)   # 400 rows, page size 1: not tiled by TMA boxes
     assert ei.value.status == 3
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_cpp_planner_matches_oracle_with_window(lib, seed):
+    """Sliding-window plans (causal): C++ == restatement, bit for bit; non-causal windows rejected."""
+    rng = np.random.default_rng(800 + seed)
+    qo, kv, last, hq, hk, ps, causal = _case(rng, ps_choices=(1, 8, 16))
+    n_cta = int(rng.choice([1, 7, 152]))
+    w = int(rng.choice([0, 3, 64, 999, 10 ** 6]))
+    g = hq // hk
+    if int(np.diff(qo).max(initial=0)) * g > 8 and ps % 8:
+        return
+    if not causal:
+        with pytest.raises(B.FiError) as ei:
+            B.plan_compute(qo, kv, last, hq, hk, ps, False, n_cta, window_left=w)
+        assert ei.value.status == 3
+        return
+    _compare(qo, kv, last, hq, hk, ps, True, n_cta, window_left=w)

@@ -161,3 +161,52 @@ def test_skewed_long_request_is_split():
     assert len(long_items) > 8 and all(it["slot"] >= 0 for it in long_items)
     assert all(it["slot"] == -1 for it in p.items if it["request"] != 0)
     assert len(p.units) == 8
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_sliding_window_coverage(seed):
+    """With a window (causal), a tile's chunks cover exactly [first key any of its tokens can see,
+    last key), the start rounded down to a page; brute force over the tokens' windows."""
+    rng = np.random.default_rng(900 + seed)
+    c = _random_case(rng)
+    if not c["causal"]:
+        with pytest.raises(ValueError):
+            P.plan(c["qo_indptr"], c["kv_indptr"], c["last"], c["hq"], c["hk"], c["ps"], False, c["n_cta"],
+                   window_left=5)
+        return
+    w = int(rng.choice([0, 1, 17, 300, 5000]))
+    p = P.plan(c["qo_indptr"], c["kv_indptr"], c["last"], c["hq"], c["hk"], c["ps"], True, c["n_cta"],
+               window_left=w)
+    lq, lk = c["lq"], c["lk"]
+    by_unit = {}
+    for it in p.items:
+        by_unit.setdefault((it["request"], it["kv_head"], it["tile"]), []).append(it)
+    for (i, h, j), chunks in by_unit.items():
+        chunks = sorted(chunks, key=lambda x: x["chunk"])
+        toks = range(j * p.tile_tokens, min((j + 1) * p.tile_tokens, int(lq[i])))
+        vis = [k for t in toks for k in range(int(lk[i])) if lk[i] - lq[i] + t - w <= k <= lk[i] - lq[i] + t]
+        lo, hi = chunks[0]["kv_lo"], chunks[-1]["kv_hi"]
+        if vis:
+            assert lo <= min(vis) and min(vis) - lo < c["ps"] and lo % c["ps"] == 0
+            assert hi == max(vis) + 1
+        else:
+            assert lo == hi
+        for a, b in zip(chunks, chunks[1:]):
+            assert a["kv_hi"] == b["kv_lo"] and b["kv_lo"] % c["ps"] == 0
+        assert all(ch["kv_hi"] - ch["kv_lo"] <= p.l_kv_chunk for ch in chunks)
+    costs = [it["cost"] for it in p.items]
+    if costs:
+        assert max(p.loads) <= sum(costs) / p.num_ctas + (1 - 1 / p.num_ctas) * max(costs) + 1e-9
+
+
+def test_wide_window_plan_equals_no_window_chunks():
+    """A window longer than every KV reads the same keys as no window (only L_kv's sum differs)."""
+    lk = np.array([700, 1500, 90])
+    lq = np.array([3, 1, 90])
+    kv = np.concatenate([[0], np.cumsum((lk + 15) // 16)])
+    last = lk - ((lk + 15) // 16 - 1) * 16
+    qo = np.concatenate([[0], np.cumsum(lq)])
+    a = P.plan(qo, kv, last, 8, 2, 16, True, 4, window_left=10 ** 6)
+    b = P.plan(qo, kv, last, 8, 2, 16, True, 4)
+    cover = lambda pl: sorted((it["request"], it["kv_head"], it["tile"], it["kv_lo"]) for it in pl.items if it["chunk"] == 0)
+    assert cover(a) == cover(b)
