@@ -66,8 +66,14 @@ def algorithmic_bytes(b):
     return kv_bytes(b) + rows * b.head_dim * 2 * 2 + rows * 4 + int(b.kv_indptr[-1]) * 4
 
 
-def visible_pairs(b):
+def visible_pairs(b, window_left=-1):
     l_q, l_kv = lengths(b)
+    if window_left >= 0:  # causal with a sliding window: token t sees keys p - w .. p, p = l_kv - l_q + t
+        tot = 0
+        for lq, lk in zip(l_q.tolist(), l_kv.tolist()):
+            p = lk - lq + np.arange(lq)
+            tot += int(np.clip(np.minimum(p + 1, window_left + 1), 0, None).sum())
+        return tot
     tot = 0
     for lq, lk in zip(l_q.tolist(), l_kv.tolist()):
         if b.causal:
@@ -78,8 +84,8 @@ def visible_pairs(b):
     return tot
 
 
-def flops(b):
-    return 4 * b.head_dim * visible_pairs(b) * b.num_qo_heads
+def flops(b, window_left=-1):
+    return 4 * b.head_dim * visible_pairs(b, window_left) * b.num_qo_heads
 
 
 # ----------------------------------------------------------------------------------------------
@@ -93,8 +99,9 @@ def to_dev(a, torch, dev):
 class Case:
     """One batch resident on the device with its workspace and plan."""
 
-    def __init__(self, b, torch, dev, num_ctas=0):
+    def __init__(self, b, torch, dev, num_ctas=0, variant=None):
         from serving_attention_plan_gb300 import binding as B
+        self.variant = variant
         self.b = b
         self.torch = torch
         self.q, self.k, self.v = to_dev(b.q, torch, dev), to_dev(b.k_pages, torch, dev), to_dev(b.v_pages, torch, dev)
@@ -102,6 +109,8 @@ class Case:
         self.lse = torch.empty((b.total_q, b.num_qo_heads), dtype=torch.float32, device=dev)
         self.ws = B.Workspace(b.batch_size, b.total_q, int(b.kv_indptr[-1]), b.num_qo_heads, b.num_kv_heads,
                               b.head_dim, num_ctas)
+        if variant:
+            self.ws.set_variant(**variant)
         self.plan()
 
     def plan(self):
@@ -387,7 +396,7 @@ def main():
     extra = {}
     if not args.no_extra:
         for name in ("tiny_decode", "skewed_long_decode", "ragged_causal_prefill", "shared_prefix_decode") + \
-                W.KERNEL_DIST_WORKLOADS:
+                W.KERNEL_DIST_WORKLOADS + tuple(VARIANT_WORKLOADS):
             try:
                 extra[name] = bench_other(name, torch, dev, hbm_peak, bf16_peak)
             except Exception as e:  # report, never hide
@@ -425,9 +434,41 @@ def main():
         torch.distributed.destroy_process_group()
 
 
+# Attention variants (sliding window, logit soft-cap, NHD pages) on two of the workloads
+VARIANT_WORKLOADS = {
+    "variant_llama3_8b_decode_nhd_softcap50": ("llama3_8b_decode", dict(logits_soft_cap=50.0, kv_layout="NHD")),
+    "variant_ragged_causal_prefill_window1024_softcap50": ("ragged_causal_prefill",
+                                                            dict(window_left=1024, logits_soft_cap=50.0)),
+}
+
+
+def bench_variant(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
+    import dataclasses
+    from serving_attention_plan_gb300 import workloads as W
+    base, var = VARIANT_WORKLOADS[name]
+    w = W.by_name(base)
+    if var.get("kv_layout") == "NHD":
+        w = dataclasses.replace(w, k_pages=np.ascontiguousarray(w.k_pages.transpose(0, 2, 1, 3)),
+                                v_pages=np.ascontiguousarray(w.v_pages.transpose(0, 2, 1, 3)))
+    c = Case(w, torch, dev, variant=var)
+    ms = time_launches(torch, c.run, steps, warmup)
+    hdr = c.ws.info()
+    out = {"us_per_batch": ms * 1e3, "path": path_name(w, hdr), "variant": var,
+           "config": dict(workload_config(base, w), l2="inputs larger than L2"), "device_errors": c.ws.get_error()}
+    if hdr[1] == 1:
+        tf = flops(w, var.get("window_left", -1)) / (ms * 1e-3) / 1e12
+        out.update({"tflops_visible_pairs": tf, "frac_of_bf16_peak": tf / bf16_peak})
+    else:
+        gbs = kv_bytes(w) / (ms * 1e-3) / 1e9
+        out.update({"kv_gbs": gbs, "frac_of_hbm_peak": gbs / hbm_peak})
+    return out
+
+
 def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
     from serving_attention_plan_gb300 import binding as B
     from serving_attention_plan_gb300 import workloads as W
+    if name in VARIANT_WORKLOADS:
+        return bench_variant(name, torch, dev, hbm_peak, bf16_peak, steps, warmup)
     w = W.by_name(name)
     if name == "shared_prefix_decode":
         pre, suf = Case(w.prefix, torch, dev), None

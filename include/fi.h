@@ -113,7 +113,8 @@ int fi_workspace_set_cost_model(fi_workspace* ws, int64_t alpha, int64_t beta, i
  *
  * The variant is fixed into the plan at fi_plan; fi_run uses the plan's.  A
  * window on a non-causal batch makes fi_plan return UNSUPPORTED; so does NHD
- * decode with a page size or a KV-head count that is not a power of two.  A captured fi_run keeps
+ * decode unless the page size is a power of two and num_kv_heads is 1, 2, 4,
+ * 8 or 16.  A captured fi_run keeps
  * the variant it was captured with.  Default: none, none, HND.
  * Errors: INVALID_ARG.
  */

@@ -63,7 +63,6 @@ struct DecodeParams {
   int32_t* err;
   long long page_stride;   // elements per page (H_kv * page_size * 128)
   long long head_stride;   // elements between KV heads of a page (HND: page_size * 128; NHD: 128)
-  int token_shift;         // log2 of the elements between tokens of a page-head (HND: 7; NHD: log2(H_kv * 128))
   int num_pages;
   int page_size;
   int page_shift;  // log2(page_size) when it is a power of two (LDGSTS loader), else -1
@@ -238,7 +237,8 @@ __device__ __forceinline__ void decode_index_warp(const DecodeParams& p, DecodeS
 // rows, 16 bytes per lane per instruction.
 // Copy c (0..1023) of a stage: K/V = c / 512, token = (c % 512) / 16, 16-byte chunk = c % 16,
 // so each warp instruction moves two consecutive 256-byte rows.
-template <int R, int NW, int S, int kCopiers, bool kSwizzle, bool kNhd, bool kMs>
+// kNhdStride: 0 for HND pages, else the elements between tokens of an NHD page-head (H_kv * 128).
+template <int R, int NW, int S, int kCopiers, bool kSwizzle, int kNhdStride, bool kMs>
 __device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
                                                    int end, int cw) {
   const int lane = threadIdx.x & 31;
@@ -273,13 +273,11 @@ __device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, Decode
       const int seg = min(max((pos >> sh) - first, 0), 31);
       const int page = __shfl_sync(0xffffffffu, pg, seg);
       if (tok < nt && page >= 0) {
-        // One 64-bit expression, the row term a shift: this loop issues a 16-byte copy per lane per
-        // step, and measured on GB300 a run-time 64-bit multiply here cost a third of the copy rate,
-        // as did forming the row term in 32 bits.
+        // One 64-bit expression with a compile-time row stride: this loop issues a 16-byte copy per
+        // lane per step, and measured on GB300 a run-time stride (multiply or shift) here cost a
+        // third of the copy rate, as did forming the row term in 32 bits.
         const long long off = (long long)page * p.page_stride +
-                              (kNhd ? (long long)(pos & row_mask) << p.token_shift
-                                    : (long long)(pos & row_mask) * kHeadDim) +
-                              (lane & 15) * 8;
+                              (long long)(pos & row_mask) * (kNhdStride ? kNhdStride : kHeadDim) + (lane & 15) * 8;
         const int chunk = kSwizzle ? ((lane & 15) ^ (tok & 7)) : (lane & 15);
         cp_async_16(&sm.kv[slot][0][tok][chunk * 8], kb + off);
         cp_async_16(&sm.kv[slot][1][tok][chunk * 8], vb + off);
@@ -806,9 +804,11 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
 }
 
 // kMma selects the tensor-core consumer (LDGSTS loader only, whose copies it swizzles).
-// kFlags: kDecodeNhd (NHD pages, 16-byte-copy loader only), kDecodeVariant (sliding window / soft-cap).
+// kFlags: kDecodeNhd (NHD pages, 16-byte-copy loader only; bits 4-6 hold log2(H_kv)),
+// kDecodeVariant (sliding window / soft-cap).
 constexpr int kDecodeNhd = 1;
 constexpr int kDecodeVariant = 2;
+constexpr int kDecodeNhdHeadsShift = 4;
 template <int R, int NW, int S, int kCopiers = 0, bool kMma = false, int kFlags = 0>
 __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
     decode_kernel(const __grid_constant__ DecodeParams p) {
@@ -856,7 +856,8 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
   } else if (warp == 0) {
     decode_index_warp<R, NW, S>(p, sm, begin, end);
   } else {
-    decode_copier_warp<R, NW, S, kCopiers, kMma, (kFlags & kDecodeNhd) != 0>(p, sm, begin, end, warp - 1);
+    constexpr int kNhdStride = (kFlags & kDecodeNhd) ? kHeadDim << ((kFlags >> kDecodeNhdHeadsShift) & 7) : 0;
+    decode_copier_warp<R, NW, S, kCopiers, kMma, kNhdStride>(p, sm, begin, end, warp - 1);
   }
 }
 

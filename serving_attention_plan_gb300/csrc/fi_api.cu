@@ -15,7 +15,7 @@
 #include <string>
 
 #include "../../include/fi.h"
-#include "decode_kernel.cuh"
+#include "decode_launch.cuh"
 #include "merge_kernel.cuh"
 #include "plan.h"
 #include "prefill_launch.h"
@@ -67,56 +67,17 @@ struct fi_workspace {
 
 namespace {
 
-// Consumer warps and ring depth (32-token stages) of the decode CTA, per tile height R and
-// consumer kind, from sweeps on GB300.  The 16-byte-copy loader (power-of-two page sizes) feeds
-// tensor-core consumers, which spend little issue per stage and keep no transpose scratch,
-// leaving the shared memory to a 12-stage ring; four of them hide the stage latency (two fall
-// behind).  Against the CUDA-core consumers they raised the Llama-3-8B-shaped batch (R = 4) from
-// 0.75 to 0.99 of the measured copy bandwidth, the skewed batch (R = 8) from 0.35 to 0.85, and
-// g = 1 / g = 2 batches of the same lengths from 0.96 / 0.90 to 1.00 / 0.99.  The bulk loader
-// (other page sizes) feeds CUDA-core consumers: eight warps hide the latency of the R <= 4 math;
-// R = 8 needs more registers per thread, so four.
-constexpr int kDecodeCopiers = 3;  // copier warps of the 16-byte-copy loader: ~0.9 of HBM in flight
-template <int R, bool kMma>
-struct DecodeConfig {
-  static constexpr int kWarps = kMma ? 4 : (R >= 8 ? 4 : 8);
-  static constexpr int kStages = kMma ? 12 : (R >= 8 ? 11 : 9);
-};
-
-template <int R, int kCopiers, int kFlags>
-int launch_decode_as(int grid, const fi::DecodeParams& p, cudaStream_t stream) {
-  constexpr bool kMma = kCopiers > 0;
-  constexpr int kDecodeWarps = DecodeConfig<R, kMma>::kWarps;
-  constexpr int kDecodeStages = DecodeConfig<R, kMma>::kStages;
-  using Smem = fi::DecodeSmem<R, kDecodeWarps, kDecodeStages, kMma>;
-  static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
-  auto kernel = fi::decode_kernel<R, kDecodeWarps, kDecodeStages, kCopiers, kMma, kFlags>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
-  });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(decode)");
-  kernel<<<grid, (kDecodeWarps + (kCopiers ? 1 + kCopiers : 1)) * 32, sizeof(Smem), stream>>>(p);
-  FI_CUDA(cudaGetLastError());
-  return FI_OK;
-}
-
 // Power-of-two page sizes take the 16-byte-copy loader, others the bulk-copy loader (HND only).
 // The page layout and the attention variant are template flags, so the plain HND path compiles
 // without a trace of them.
 template <int R>
-int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream, bool nhd, bool var) {
-  constexpr int kN = fi::kDecodeNhd, kV = fi::kDecodeVariant;
-  if (p.page_shift >= 0) {
-    if (nhd)
-      return var ? launch_decode_as<R, kDecodeCopiers, kN | kV>(grid, p, stream)
-                 : launch_decode_as<R, kDecodeCopiers, kN>(grid, p, stream);
-    return var ? launch_decode_as<R, kDecodeCopiers, kV>(grid, p, stream)
-               : launch_decode_as<R, kDecodeCopiers, 0>(grid, p, stream);
-  }
-  if (nhd) return FI_ERR_UNSUPPORTED;
-  return var ? launch_decode_as<R, 0, kV>(grid, p, stream) : launch_decode_as<R, 0, 0>(grid, p, stream);
+int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream, bool var) {
+  using fi::kDecodeCopiers;
+  constexpr int kV = fi::kDecodeVariant;
+  if (p.page_shift >= 0)
+    return var ? fi::launch_decode_as<R, kDecodeCopiers, kV>(grid, p, stream)
+               : fi::launch_decode_as<R, kDecodeCopiers, 0>(grid, p, stream);
+  return var ? fi::launch_decode_as<R, 0, kV>(grid, p, stream) : fi::launch_decode_as<R, 0, 0>(grid, p, stream);
 }
 
 bool var_on(const fi::Variant& v) { return v.window_left >= 0 || v.soft_cap > 0.f; }
@@ -259,10 +220,10 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   fi::Plan plan;
   st = fi::build_plan(in, ws->cost, &plan);
   if (st != FI_OK) return st;
-  // NHD decode reads page rows with the 16-byte-copy loader (power-of-two pages), which steps over
-  // tokens by a shift (power-of-two KV-head count)
+  // NHD decode reads page rows with the 16-byte-copy loader (power-of-two pages); its kernels are
+  // instantiated for 1, 2, 4, 8 and 16 KV heads
   if (ws->variant.kv_layout == FI_KV_LAYOUT_NHD && plan.header[fi::H_PATH] == fi::kPathDecode &&
-      ((page_size & (page_size - 1)) != 0 || (num_kv_heads & (num_kv_heads - 1)) != 0))
+      ((page_size & (page_size - 1)) != 0 || (num_kv_heads & (num_kv_heads - 1)) != 0 || num_kv_heads > 16))
     return FI_ERR_UNSUPPORTED;
   const int64_t n_items = plan.header[fi::H_NUM_ITEMS], n_units = plan.header[fi::H_NUM_UNITS],
                 n_slots = plan.header[fi::H_NUM_SLOTS];
@@ -348,7 +309,6 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     const bool nhd = var.kv_layout == FI_KV_LAYOUT_NHD;
     p.page_stride = (long long)ws->hkv * ps * fi::kHeadDim;
     p.head_stride = nhd ? fi::kHeadDim : (long long)ps * fi::kHeadDim;
-    p.token_shift = nhd ? 7 + __builtin_ctz(unsigned(ws->hkv)) : 7;  // NHD plans have a power-of-two H_kv
     p.window_left = var.window_left;
     p.cap_log2 = var.soft_cap > 0.f ? var.soft_cap * fi::kLog2e : 0.f;
     p.inv_cap_log2 = var.soft_cap > 0.f ? 1.f / p.cap_log2 : 0.f;
@@ -360,11 +320,13 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     p.slot_rows = fi::kTcRows;
     p.scale_log2 = scale_log2;
     const bool variant = var_on(var);
+    if (nhd)
+      return fi::launch_decode_nhd(h[fi::H_ROWS_TILE], __builtin_ctz(unsigned(ws->hkv)), h[fi::H_NUM_CTAS], p, s);
     switch (h[fi::H_ROWS_TILE]) {
-      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
-      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
-      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
-      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s, nhd, variant);
+      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s, variant);
+      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s, variant);
+      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s, variant);
+      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s, variant);
       default: return FI_ERR_UNSUPPORTED;
     }
   }

@@ -335,7 +335,6 @@ extern "C" int fi_decode_noalloc(const int32_t* qo_indptr, const int32_t* kv_ind
   p.err = reinterpret_cast<int32_t*>(d + L.err);
   p.page_stride = (long long)num_kv_heads * page_size * fi::kHeadDim;
   p.head_stride = (long long)page_size * fi::kHeadDim;
-  p.token_shift = 7;  // HND: tokens of a page-head are 128 elements apart
   p.window_left = -1;  // no window, no soft-cap (cap_log2 = 0)
   p.num_pages = num_pages;
   p.page_size = page_size;

@@ -268,6 +268,14 @@ __device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst_ptr, const floa
 __device__ __forceinline__ float lse_out(float lse2) { return (lse2 == -INFINITY) ? -INFINITY : lse2 * kLn2; }
 
 
+// Hardware tanh (relative error about 2^-11, so a capped logit is within about 7e-4 * cap): one
+// instruction per score, where the exp2-based tanh would double the softmax's per-score work.
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One KV tile: scores -> (soft-cap) -> mask keys outside [lo, lim) -> online-softmax update -> P
 // into the S columns of TMEM.
 template <bool kMasked, bool kCap>
@@ -284,7 +292,7 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lo, int 
     // capped logits in the log2 domain; the scale is then already applied
     const float in_scale = scale / p.cap_log2;
 #pragma unroll
-    for (int j = 0; j < kTile; ++j) s[j] = __float_as_uint(p.cap_log2 * tanh_exp2(__uint_as_float(s[j]) * in_scale));
+    for (int j = 0; j < kTile; ++j) s[j] = __float_as_uint(p.cap_log2 * tanh_fast(__uint_as_float(s[j]) * in_scale));
     scale = 1.f;
   }
   // row maximum of the (scaled) scores with 8 independent partial maxima
@@ -347,8 +355,8 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lo, int 
   }
 }
 
-// kVar: the plan has a sliding window or a logit soft-cap (compiled out of the plain kernel).
-template <bool kVar>
+// kWin / kCap: the plan has a sliding window / a logit soft-cap (compiled out of the plain kernel).
+template <bool kWin, bool kCap>
 __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
   const int row = threadIdx.x;  // 0..127 == TMEM lane
   const int warp = row >> 5;
@@ -369,22 +377,14 @@ __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32
       const int base = it.kv_lo + t * kTile;
       const int lim = max(0, min(kTile, min(it.kv_hi - base, it.diag + u + 1 - base)));
       // sliding window: keys below diag + u - window_left are masked
-      const int lo = (kVar && p.window_left >= 0) ? min(kTile, max(0, it.diag + u - p.window_left - base)) : 0;
+      const int lo = kWin ? min(kTile, max(0, it.diag + u - p.window_left - base)) : 0;
       alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.s_full, tt & 1, p.err, &sm.abort));
       if (alive) {
         tc::fence_after_sync();
-        const bool full = __all_sync(0xffffffffu, lim >= kTile && lo <= 0);
-        if (kVar && p.cap_log2 > 0.f) {
-          if (full)
-            softmax_tile<false, true>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
-          else
-            softmax_tile<true, true>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
-        } else {
-          if (full)
-            softmax_tile<false, false>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
-          else
-            softmax_tile<true, false>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
-        }
+        if (__all_sync(0xffffffffu, lim >= kTile && lo <= 0))
+          softmax_tile<false, kCap>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
+        else
+          softmax_tile<true, kCap>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
         tc::fence_before_sync();
       }
       __syncwarp();
@@ -469,7 +469,7 @@ __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32
   }
 }
 
-template <bool kVar, bool kNhd>
+template <bool kWin, bool kCap, bool kNhd>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) atomicOr(p.err, FI_DEVERR_TMEM);
   } else if (warp < 4) {
     tc::regs_increase<kSoftmaxRegs>();
-    softmax_epilogue<kVar>(p, sm, tmem, begin, end);
+    softmax_epilogue<kWin, kCap>(p, sm, tmem, begin, end);
   } else {
     tc::regs_decrease<kControlRegs>();
     if (warp == 4) {
@@ -706,17 +706,18 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.cap_log2 = a.cap_log2;
 
   const size_t smem = sizeof(PrefillSmem) + 1024;
-  // the attention variant and the page layout are template flags: the plain HND kernel carries neither
-  const bool var = a.window_left >= 0 || a.cap_log2 > 0.f;
+  // window, soft-cap and page layout are template flags: the plain HND kernel carries none of them
   using Kernel = void (*)(PrefillParams, CUtensorMap, CUtensorMap, CUtensorMap);
-  const Kernel kernels[2][2] = {{prefill_kernel<false, false>, prefill_kernel<false, true>},
-                                {prefill_kernel<true, false>, prefill_kernel<true, true>}};
-  const Kernel kernel = kernels[var ? 1 : 0][a.nhd ? 1 : 0];
+  const Kernel kernels[8] = {prefill_kernel<false, false, false>, prefill_kernel<false, false, true>,
+                             prefill_kernel<false, true, false>,  prefill_kernel<false, true, true>,
+                             prefill_kernel<true, false, false>,  prefill_kernel<true, false, true>,
+                             prefill_kernel<true, true, false>,   prefill_kernel<true, true, true>};
+  const Kernel kernel = kernels[(a.window_left >= 0 ? 4 : 0) + (a.cap_log2 > 0.f ? 2 : 0) + (a.nhd ? 1 : 0)];
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
-    for (int i = 0; i < 4 && attr == cudaSuccess; ++i)
-      attr = cudaFuncSetAttribute(kernels[i / 2][i % 2], cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    for (int i = 0; i < 8 && attr == cudaSuccess; ++i)
+      attr = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   });
   if (attr != cudaSuccess) return record_cuda_error(attr, "cudaFuncSetAttribute(prefill_kernel)");
   kernel<<<a.num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
