@@ -35,6 +35,13 @@ soft-cap among the variants a serving library must carry; 核心机制 5, paper
     p = l_kv - l_q + t, sees keys p - window_left .. p (window_left + 1 keys).
   * Logit soft-cap: the scaled logit x = scale * q.k becomes cap * tanh(x / cap)
     before the softmax, so every logit lies in (-cap, cap).
+
+FP8 KV (核心机制 8 / paper App. F lists FP8 KV-cache support; reading): pages may
+hold e4m3 codes with one scale per tensor, K = k_scale * e4m3(K code) and
+likewise V.  e4m3 is the 8-bit float with 1 sign bit, 4 exponent bits (bias 7)
+and 3 mantissa bits: exponent field 0 encodes subnormals m/8 * 2^-6, field 15
+with mantissa 7 encodes NaN, there are no infinities, and the largest finite
+value is 1.75 * 2^8 = 448.
 """
 from __future__ import annotations
 
@@ -47,6 +54,17 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     """bfloat16 bit patterns (uint16) -> exact float64 values (bf16 is the top half of an f32)."""
     b = np.asarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """e4m3 codes (uint8) -> float64: sign * (1 + m/8) * 2^(e - 7), or sign * (m/8) * 2^-6 when e = 0."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
 
 
 def request_lengths(qo_indptr, kv_indptr, last_page_len, page_size):
@@ -80,7 +98,11 @@ def gather_kv(pages: np.ndarray, kv_indptr, kv_indices, l_kv: int, page_size: in
         rows = pages[page, r, kv_head]
     else:
         raise ValueError(layout)
-    return bf16_to_f64(rows) if pages.dtype == np.uint16 else np.asarray(rows, dtype=np.float64)
+    if pages.dtype == np.uint16:
+        return bf16_to_f64(rows)
+    if pages.dtype == np.uint8:
+        return e4m3_to_f64(rows)
+    return np.asarray(rows, dtype=np.float64)
 
 
 def visible_counts(l_q: int, l_kv: int, causal: bool) -> np.ndarray:
@@ -132,7 +154,7 @@ def attention_state(q_rows: np.ndarray, k: np.ndarray, v: np.ndarray, n_visible,
 
 
 def batch_attention(b, layout: str = "HND", requests=None, scale: float | None = None, window_left: int = -1,
-                    soft_cap: float = 0.0):
+                    soft_cap: float = 0.0, k_scale: float = 1.0, v_scale: float = 1.0):
     """O [total_q, H_qo, D] and LSE [total_q, H_qo] (float64) for a paged batch.
 
     `b` carries the library's input arrays (see serving_attention_plan_gb300.workloads.PagedBatch).
@@ -156,8 +178,8 @@ def batch_attention(b, layout: str = "HND", requests=None, scale: float | None =
         vis = visible_counts(nq, nk, b.causal)
         lo = window_starts(nq, nk, window_left)
         for hk in range(b.num_kv_heads):
-            k = gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, hk, layout)
-            v = gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, hk, layout)
+            k = k_scale * gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, hk, layout)
+            v = v_scale * gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, hk, layout)
             for h in range(hk * g, (hk + 1) * g):
                 qr = bf16_to_f64(b.q[q0:q0 + nq, h])
                 oo, ll = attention_state(qr, k, v, vis, scale, lo, soft_cap)
@@ -167,7 +189,7 @@ def batch_attention(b, layout: str = "HND", requests=None, scale: float | None =
 
 
 def attention_rows(b, i: int, h: int, tokens, layout: str = "HND", scale: float | None = None,
-                   window_left: int = -1, soft_cap: float = 0.0):
+                   window_left: int = -1, soft_cap: float = 0.0, k_scale: float = 1.0, v_scale: float = 1.0):
     """State of selected query tokens (0-based within request i) of query head h."""
     if window_left >= 0 and not b.causal:
         raise ValueError("the sliding window is read with causal masks")
@@ -179,8 +201,8 @@ def attention_rows(b, i: int, h: int, tokens, layout: str = "HND", scale: float 
     tokens = np.asarray(tokens, dtype=np.int64)
     vis = visible_counts(nq, nk, b.causal)[tokens]
     lo = window_starts(nq, nk, window_left)[tokens]
-    k = gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, h // g, layout)
-    v = gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, h // g, layout)
+    k = k_scale * gather_kv(b.k_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, h // g, layout)
+    v = v_scale * gather_kv(b.v_pages, b.kv_indptr, b.kv_indices, nk, b.page_size, i, h // g, layout)
     qr = bf16_to_f64(b.q[int(b.qo_indptr[i]) + tokens, h])
     return attention_state(qr, k, v, vis, scale, lo, soft_cap)
 

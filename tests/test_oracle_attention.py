@@ -403,3 +403,42 @@ def test_window_needs_causal():
                              kv_len_range=(1, 10), head_dim=8)
     with pytest.raises(ValueError):
         A.batch_attention(b, window_left=3)
+
+
+# ---- FP8 (e4m3) KV (核心机制 8 / paper App. F; the format's own definition) -----------------------
+
+def test_e4m3_decoder_pins():
+    """Values fixed by the format: 1.0, the extremes, subnormal spacing, sign symmetry, NaN, ordering."""
+    d = A.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    assert d[0x38] == 1.0 and d[0x40] == 2.0 and d[0x30] == 0.5
+    assert d[0x7E] == 448.0                       # largest finite value
+    assert d[0x08] == 2.0 ** -6                   # smallest normal
+    assert d[0x01] == 2.0 ** -9                   # smallest subnormal
+    assert d[0x00] == 0.0 and d[0x80] == 0.0
+    assert np.isnan(d[0x7F]) and np.isnan(d[0xFF]) and np.isnan(d).sum() == 2
+    np.testing.assert_array_equal(d[0x80:0xFF], -d[0x00:0x7F])
+    pos = d[0x00:0x7F]
+    assert np.all(np.diff(pos) > 0)               # codes ascend with value
+    # every normal binade holds 8 evenly spaced values; the next binade doubles them
+    for c in range(0x08, 0x77):
+        assert d[c + 8] == 2.0 * d[c]
+    # subnormals are the multiples of 2^-9 below the smallest normal
+    np.testing.assert_array_equal(d[0x00:0x08], np.arange(8) * 2.0 ** -9)
+
+
+def test_fp8_attention_equals_dequantized_bf16_free_attention():
+    """Attention over e4m3 pages with scales == attention over the same values given as float64 pages."""
+    rng = np.random.default_rng(730)
+    b = W.random_small_batch(730, batch=3, num_qo_heads=4, num_kv_heads=2, page_size=4, causal=False,
+                             kv_len_range=(1, 20), head_dim=8)
+    codes_k = rng.integers(0, 0x7E, size=b.k_pages.shape, dtype=np.uint8) | (rng.integers(0, 2, size=b.k_pages.shape, dtype=np.uint8) << 7)
+    codes_v = rng.integers(0, 0x7E, size=b.v_pages.shape, dtype=np.uint8)
+    b8 = W.PagedBatch(b.name, b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.causal, b.qo_indptr,
+                      b.kv_indptr, b.kv_indices, b.last_page_len, b.q, codes_k, codes_v)
+    o, l = A.batch_attention(b8, k_scale=0.25, v_scale=3.0)
+    bf = W.PagedBatch(b.name, b.num_qo_heads, b.num_kv_heads, b.head_dim, b.page_size, b.causal, b.qo_indptr,
+                      b.kv_indptr, b.kv_indices, b.last_page_len, b.q, 0.25 * A.e4m3_to_f64(codes_k),
+                      3.0 * A.e4m3_to_f64(codes_v))
+    o2, l2 = A.batch_attention(bf)
+    np.testing.assert_allclose(o, o2, atol=TOL)
+    np.testing.assert_allclose(l, l2, atol=TOL)
