@@ -57,7 +57,8 @@ def lengths(b):
 
 def kv_bytes(b):
     _, l_kv = lengths(b)
-    return int(l_kv.sum()) * b.num_kv_heads * b.head_dim * 2 * 2
+    elem = b.k_pages.dtype.itemsize  # 2 for bf16 bits, 1 for e4m3 codes
+    return int(l_kv.sum()) * b.num_kv_heads * b.head_dim * elem * 2
 
 
 def algorithmic_bytes(b):
@@ -93,6 +94,8 @@ def flops(b, window_left=-1):
 # ----------------------------------------------------------------------------------------------
 
 def to_dev(a, torch, dev):
+    if a.dtype == np.uint8:  # e4m3 codes
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
 
@@ -110,7 +113,12 @@ class Case:
         self.ws = B.Workspace(b.batch_size, b.total_q, int(b.kv_indptr[-1]), b.num_qo_heads, b.num_kv_heads,
                               b.head_dim, num_ctas)
         if variant:
-            self.ws.set_variant(**variant)
+            variant = dict(variant)
+            kv_dtype = variant.pop("kv_dtype", None)
+            if kv_dtype:
+                self.ws.set_kv_dtype(*kv_dtype)
+            if variant:
+                self.ws.set_variant(**variant)
         self.plan()
 
     def plan(self):
@@ -439,6 +447,7 @@ VARIANT_WORKLOADS = {
     "variant_llama3_8b_decode_nhd_softcap50": ("llama3_8b_decode", dict(logits_soft_cap=50.0, kv_layout="NHD")),
     "variant_ragged_causal_prefill_window1024_softcap50": ("ragged_causal_prefill",
                                                             dict(window_left=1024, logits_soft_cap=50.0)),
+    "variant_llama3_8b_decode_fp8_e4m3": ("llama3_8b_decode", dict(kv_dtype=("e4m3", 0.5, 0.5))),
 }
 
 
@@ -447,6 +456,8 @@ def bench_variant(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
     from serving_attention_plan_gb300 import workloads as W
     base, var = VARIANT_WORKLOADS[name]
     w = W.by_name(base)
+    if var.get("kv_dtype"):
+        w = W.as_e4m3(w, var["kv_dtype"][1], var["kv_dtype"][2])
     if var.get("kv_layout") == "NHD":
         w = dataclasses.replace(w, k_pages=np.ascontiguousarray(w.k_pages.transpose(0, 2, 1, 3)),
                                 v_pages=np.ascontiguousarray(w.v_pages.transpose(0, 2, 1, 3)))

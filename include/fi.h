@@ -49,6 +49,10 @@ typedef enum fi_status {
 #define FI_KV_LAYOUT_HND 0 /* [num_pages, num_kv_heads, page_size, head_dim] */
 #define FI_KV_LAYOUT_NHD 1 /* [num_pages, page_size, num_kv_heads, head_dim] */
 
+/* Element types of k_pages / v_pages (fi_workspace_set_kv_dtype). */
+#define FI_KV_DTYPE_BF16 0 /* bfloat16 */
+#define FI_KV_DTYPE_E4M3 1 /* fp8 e4m3 codes (1 byte), one scale per tensor */
+
 /* Device-side error bits reported by fi_get_error. */
 #define FI_DEVERR_PAGE_OOB 0x1     /* a page index >= num_pages was skipped */
 #define FI_DEVERR_WAIT_TIMEOUT 0x2 /* a pipeline wait gave up after its iteration limit */
@@ -119,6 +123,24 @@ int fi_workspace_set_cost_model(fi_workspace* ws, int64_t alpha, int64_t beta, i
  * Errors: INVALID_ARG.
  */
 int fi_workspace_set_variant(fi_workspace* ws, int32_t window_left, float logits_soft_cap, int32_t kv_layout);
+
+/*
+ * fi_workspace_set_kv_dtype -- element type of the KV pages for the following fi_plan.
+ *
+ * Source: 核心机制 8 (paper App. F): a mixed-precision kernel keeps queries and
+ * outputs in 16-bit floats and stores the KV-cache in fp8.  Reading: e4m3
+ * codes with one scale per tensor, K = k_scale * code and V = v_scale * code.
+ *
+ *   kv_dtype          FI_KV_DTYPE_BF16 (default) or FI_KV_DTYPE_E4M3
+ *   k_scale, v_scale  > 0; used with e4m3 pages
+ *
+ * With e4m3, k_pages / v_pages hold one byte per element in the HND shape, q and
+ * o stay bf16, and the decode kernel computes in f16 MMAs with fp32
+ * accumulation.  e4m3 plans need decode tiles, the HND layout and a
+ * power-of-two page size: fi_plan returns UNSUPPORTED otherwise.  NaN codes in
+ * the pages give undefined rows.  Errors: INVALID_ARG.
+ */
+int fi_workspace_set_kv_dtype(fi_workspace* ws, int32_t kv_dtype, float k_scale, float v_scale);
 
 /*
  * fi_plan -- inspector step: compute the work plan for one batch on the CPU.

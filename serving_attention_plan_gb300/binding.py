@@ -47,6 +47,7 @@ def lib() -> ctypes.CDLL:
     L.fi_workspace_destroy.argtypes = [c_void_p]
     L.fi_workspace_set_cost_model.argtypes = [c_void_p, c_int64, c_int64, c_int32]
     L.fi_workspace_set_variant.argtypes = [c_void_p, c_int32, ctypes.c_float, c_int32]
+    L.fi_workspace_set_kv_dtype.argtypes = [c_void_p, c_int32, ctypes.c_float, ctypes.c_float]
     L.fi_plan.argtypes = [c_void_p, P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]
     L.fi_run.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     L.fi_run_merge.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -65,7 +66,7 @@ def lib() -> ctypes.CDLL:
     L.fi_last_error_message.argtypes = []
     L.fi_last_error_message.restype = ctypes.c_char_p
     for name in ("fi_workspace_create", "fi_workspace_destroy", "fi_workspace_set_cost_model",
-                 "fi_workspace_set_variant", "fi_plan", "fi_run",
+                 "fi_workspace_set_variant", "fi_workspace_set_kv_dtype", "fi_plan", "fi_run",
                  "fi_run_merge", "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count",
                  "fi_decode_noalloc"):
         getattr(L, name).restype = c_int
@@ -153,6 +154,11 @@ class Workspace:
         layout = {"HND": 0, "NHD": 1}[kv_layout]
         _check(lib().fi_workspace_set_variant(self._h, int(window_left), float(logits_soft_cap), layout),
                "fi_workspace_set_variant")
+
+    def set_kv_dtype(self, kv_dtype="bf16", k_scale=1.0, v_scale=1.0):
+        """KV page element type ("bf16" or "e4m3", with per-tensor scales) for the following plan()."""
+        _check(lib().fi_workspace_set_kv_dtype(self._h, {"bf16": 0, "e4m3": 1}[kv_dtype], float(k_scale),
+                                               float(v_scale)), "fi_workspace_set_kv_dtype")
 
     def plan(self, qo_indptr, kv_indptr, kv_indices, last_page_len, page_size, causal, stream=None):
         qo, kv, idx, last = _i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)

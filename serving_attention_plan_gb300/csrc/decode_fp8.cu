@@ -1,0 +1,43 @@
+// Launch of the FP8-KV decode kernel (核心机制 8, paper App. F), one instantiation per rows-per-tile.
+#include "decode_fp8.cuh"
+#include "decode_launch.cuh"
+
+namespace fi {
+
+namespace {
+
+// Four consumer warps (each converts its own stages), a 16-stage ring of 8 KB stages (128 KB in
+// flight, as much as the bf16 ring's bytes per token allow in its 192 KB), three copier warps.
+constexpr int kFp8Warps = 4;
+constexpr int kFp8Stages = 16;
+
+template <int R>
+int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream) {
+  using Smem = DecodeSmemFp8<R, kFp8Warps, kFp8Stages>;
+  static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages, kDecodeCopiers>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
+  });
+  if (attr_err != cudaSuccess) return record_cuda_error(attr_err, "cudaFuncSetAttribute(decode fp8)");
+  kernel<<<grid, (kFp8Warps + 1 + kDecodeCopiers) * 32, sizeof(Smem), stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel_fp8 launch");
+}
+
+}  // namespace
+
+int launch_decode_fp8(int rows_tile, int grid, const DecodeParams& p, cudaStream_t stream) {
+  if (p.page_shift < 0) return FI_ERR_UNSUPPORTED;
+  switch (rows_tile) {
+    case 1: return launch_fp8_rows<1>(grid, p, stream);
+    case 2: return launch_fp8_rows<2>(grid, p, stream);
+    case 4: return launch_fp8_rows<4>(grid, p, stream);
+    case 8: return launch_fp8_rows<8>(grid, p, stream);
+    default: return FI_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace fi

@@ -1,0 +1,342 @@
+// Decode tiles over FP8 (e4m3) KV pages.
+//
+// Page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎", 核心机制 8 (paper App. F):
+// a mixed-precision kernel keeps queries and outputs in 16-bit floats and the KV-cache in fp8,
+// dequantising with a fast numeric converter.  Here: one scale per tensor (K = k_scale * code,
+// V = v_scale * code); the 16-byte-copy loader moves 128-byte K/V rows (half the bytes of bf16)
+// into a ring of 8 KB stages; the consumer warp that owns a stage converts it to f16 in its own
+// 128B-swizzled buffer (cvt e4m3x2 -> f16x2 is exact), releases the ring slot, and runs the same
+// warp-level MMAs as the bf16 consumer in f16 (Q converted from bf16, P rounded to f16).  The K
+// scale is folded into the logit scale and the V scale into the output.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "decode_kernel.cuh"
+
+namespace fi {
+
+template <int R, int NW, int S>
+struct DecodeSmemFp8 {
+  uint8_t kv8[S][2][kStageTokens][kHeadDim];  // [stage][K|V][token][dim] e4m3 codes, 8 KB per stage
+  __half f16[NW][2][kStageTokens][kHeadDim];   // per consumer warp: its stage in f16, chunks swizzled
+  float macc[NW][R][kHeadDim];
+  float mm[NW][8];
+  float ml[NW][8];
+  int32_t idx[kIdxSlots][32];
+  uint64_t full[S];
+  uint64_t empty[S];
+  uint64_t idx_full[kIdxSlots];
+  uint64_t idx_empty[kIdxSlots];
+  int slot_consumed[S];  // as in DecodeSmem: keeps every parity wait unambiguous
+  int slot_filled[S];
+  int flag;
+  int abort;
+};
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_codes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+
+// d (16x8 fp32) += a (16x16 f16, row-major) * b (16x8 f16, column-major)
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t f2_to_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Copier warp `cw` of kCopiers: stages cw, cw + kCopiers, ...; a warp instruction moves four
+// 128-byte rows (lane = token (lane / 8) of the four, 16-byte chunk lane % 8).
+template <int R, int NW, int S, int kCopiers>
+__device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm, int begin,
+                                                  int end, int cw) {
+  const int lane = threadIdx.x & 31;
+  const int sh = p.page_shift;
+  const int row_mask = p.page_size - 1;
+  StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
+  bool ok = c.load(p.items);
+  for (int k = 0; k < cw && ok; ++k) ok = c.next(p.items);
+  for (int n = cw; ok; n += kCopiers) {
+    const int islot = n % kIdxSlots;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.idx_full[islot], (n / kIdxSlots) & 1, p.err, &sm.abort))) break;
+    const int t0 = c.tok0();
+    const int nt = c.ntok();
+    const int first = t0 >> sh;
+    const int nseg = ((t0 + nt - 1) >> sh) - first + 1;
+    int pg = (lane < nseg) ? sm.idx[islot][lane] : 0;
+    if (lane < nseg && (pg < 0 || pg >= p.num_pages)) {
+      atomicOr(p.err, FI_DEVERR_PAGE_OOB);
+      pg = -1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.idx_empty[islot]);
+    const int slot = n % S, fill = n / S;
+    if (!__all_sync(0xffffffffu, spin_until_eq(&sm.slot_filled[slot], n - S, p.err, &sm.abort))) break;
+    if (fill > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.empty[slot], (fill - 1) & 1, p.err, &sm.abort))) break;
+    const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.k) + (long long)c.kv_head * p.head_stride;
+    const uint8_t* vb = reinterpret_cast<const uint8_t*>(p.v) + (long long)c.kv_head * p.head_stride;
+#pragma unroll
+    for (int j = 0; j < kStageTokens / 4; ++j) {
+      const int tok = 4 * j + (lane >> 3);
+      const int pos = t0 + tok;
+      const int seg = min(max((pos >> sh) - first, 0), 31);
+      const int page = __shfl_sync(0xffffffffu, pg, seg);
+      if (tok < nt && page >= 0) {
+        const long long off = (long long)page * p.page_stride + (long long)(pos & row_mask) * kHeadDim + (lane & 7) * 16;
+        cp_async_16(&sm.kv8[slot][0][tok][(lane & 7) * 16], kb + off);
+        cp_async_16(&sm.kv8[slot][1][tok][(lane & 7) * 16], vb + off);
+      }
+    }
+    cp_async_arrive_noinc(&sm.full[slot]);
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<volatile int*>(&sm.slot_filled[slot]) = n;
+    for (int k = 0; k < kCopiers && ok; ++k) ok = c.next(p.items);
+  }
+  cp_async_wait_all();
+}
+
+// Consumer warp w: stages w, w + NW, ... of the CTA's queue.  Same MMA body and fragment layout as
+// decode_consumer_mma (see there), in f16, plus the conversion of each stage.
+template <int R, int NW, int S>
+__device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm, int begin,
+                                                    int end, int w) {
+  const int lane = threadIdx.x & 31;
+  const int qd = lane & 3;
+  const int gq = lane >> 2;
+  const int ctid = w * 32 + lane;
+  const int lk_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lk_chunk = lane >> 4;
+  const int lv_tok = (lane & 7) + (lane >> 4) * 8, lv_chunk = (lane >> 3) & 1;
+  const __half* Ks = &sm.f16[w][0][0][0];
+  const __half* Vs = &sm.f16[w][1][0][0];
+
+  int stage_n = 0;
+  bool alive = true;
+  for (int pos = begin; pos < end; ++pos) {
+    const int4 ia = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields));
+    const int4 ib = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields + 4));
+    const int q_start = ia.y, q_len = ia.z, kv_head = ia.w;
+    const int kv_lo = ib.x, kv_hi = ib.y, diag = ib.z, slot_out = ib.w;
+    const int nst = (kv_hi - kv_lo + kStageTokens - 1) / kStageTokens;
+    const int rows_valid = q_len * p.group;
+
+    // B fragments of Q^T in f16: row gq, dims 16ks + 2qd (+1) and 16ks + 8 + 2qd (+1)
+    uint32_t qb[8][2];
+    if (gq < R && gq < rows_valid) {
+      const int tok = q_start + gq / p.group;
+      const int head = kv_head * p.group + gq % p.group;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((size_t)tok * p.hqo + head) * kHeadDim);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const float2 a = bf16x2_to_f2(__ldg(qrow + 8 * ks + qd)), b = bf16x2_to_f2(__ldg(qrow + 8 * ks + 4 + qd));
+        qb[ks][0] = f2_to_f16x2(a.x, a.y);
+        qb[ks][1] = f2_to_f16x2(b.x, b.y);
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+    }
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+    const int lim0 = diag + (2 * qd) / p.group, lim1 = diag + (2 * qd + 1) / p.group;
+    const int low0 = p.window_left >= 0 ? lim0 - p.window_left : INT_MIN;
+    const int low1 = p.window_left >= 0 ? lim1 - p.window_left : INT_MIN;
+
+    for (int st = 0; st < nst; ++st) {
+      const int n = stage_n + st;
+      if (n % NW != w) continue;
+      const int slot = n % S;
+      if (!alive) continue;
+      const bool got = spin_until_eq(&sm.slot_consumed[slot], n - S, p.err, &sm.abort) &&
+                       mbar_wait(&sm.full[slot], (n / S) & 1, p.err, &sm.abort);
+      if (!__all_sync(0xffffffffu, got)) {
+        alive = false;
+        continue;
+      }
+      // ---- e4m3 -> f16 into this warp's buffer (16-byte chunk c of token t at c ^ (t & 7)) ---
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+#pragma unroll
+        for (int i = 0; i < kStageTokens / 4; ++i) {
+          const int tok = 4 * i + (lane >> 3), q = lane & 7;
+          const uint4 raw = *reinterpret_cast<const uint4*>(&sm.kv8[slot][kv][tok][q * 16]);
+          uint4 h0, h1;
+          h0.x = e4m3x2_to_f16x2(raw.x);
+          h0.y = e4m3x2_to_f16x2(raw.x >> 16);
+          h0.z = e4m3x2_to_f16x2(raw.y);
+          h0.w = e4m3x2_to_f16x2(raw.y >> 16);
+          h1.x = e4m3x2_to_f16x2(raw.z);
+          h1.y = e4m3x2_to_f16x2(raw.z >> 16);
+          h1.z = e4m3x2_to_f16x2(raw.w);
+          h1.w = e4m3x2_to_f16x2(raw.w >> 16);
+          __half* row = &sm.f16[w][kv][tok][0];
+          *reinterpret_cast<uint4*>(row + ((2 * q) ^ (tok & 7)) * 8) = h0;
+          *reinterpret_cast<uint4*>(row + ((2 * q + 1) ^ (tok & 7)) * 8) = h1;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {  // the stage now lives in this warp's f16 buffer: its ring slot is free
+        *reinterpret_cast<volatile int*>(&sm.slot_consumed[slot]) = n;
+        mbar_arrive(&sm.empty[slot]);
+      }
+      const int t0 = kv_lo + st * kStageTokens;
+      const int nt = min(kStageTokens, kv_hi - t0);
+      const int n_mt = nt > 16 ? 2 : 1;
+
+      float s[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+        if (mt < n_mt) {
+          const int tok = 16 * mt + lk_tok;
+          const __half* row = Ks + tok * kHeadDim;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, row + (((2 * ks + lk_chunk) ^ (tok & 7)) * 8));
+            mma_16816_f16(s[mt], a, qb[ks][0], qb[ks][1]);
+          }
+        }
+      }
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = 16 * mt + 8 * h + gq;
+          const bool in = t < nt;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool vis = in && (t0 + t <= (e ? lim1 : lim0)) && (t0 + t >= (e ? low1 : low0));
+            float sv = s[mt][2 * h + e] * p.scale_log2;
+            if (p.cap_log2 > 0.f) sv = p.cap_log2 * tanh_exp2(sv * p.inv_cap_log2);
+            const float v = vis ? sv : -INFINITY;
+            s[mt][2 * h + e] = v;
+            mx[e] = fmaxf(mx[e], v);
+          }
+        }
+      }
+      float alpha[2], m_use[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
+        mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
+        const float m_new = fmaxf(m_run[e], mx[e]);
+        m_use[e] = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[e] = fast_exp2(m_run[e] - m_use[e]);
+        m_run[e] = m_new;
+        l_run[e] *= alpha[e];
+      }
+      uint32_t pb[2][2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float p0 = fast_exp2(s[mt][2 * h] - m_use[0]);
+          const float p1 = fast_exp2(s[mt][2 * h + 1] - m_use[1]);
+          l_run[0] += p0;
+          l_run[1] += p1;
+          pb[mt][h] = movmatrix_trans(f2_to_f16x2(p0, p1));
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0];
+        o[mt][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int kt = 0; kt < 2; ++kt) {
+        if (kt < n_mt) {
+          const int tok = 16 * kt + lv_tok;
+          const __half* row = Vs + tok * kHeadDim;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a[4];
+            ldsm_x4_trans(a, row + (((2 * mt + lv_chunk) ^ (tok & 7)) * 8));
+            mma_16816_f16(o[mt], a, pb[kt][0], pb[kt][1]);
+          }
+        }
+      }
+      __syncwarp();  // this warp's f16 buffer is read before the next stage's conversion overwrites it
+    }
+    stage_n += nst;
+
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 4);
+      l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 8);
+      l_run[e] += __shfl_xor_sync(0xffffffffu, l_run[e], 16);
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 2 * qd + e;
+      if (r < R) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {  // the V scale enters with the unnormalised output
+          sm.macc[w][r][16 * mt + gq] = o[mt][e] * p.v_scale;
+          sm.macc[w][r][16 * mt + 8 + gq] = o[mt][2 + e] * p.v_scale;
+        }
+        if (gq == 0) {
+          sm.mm[w][r] = m_run[e];
+          sm.ml[w][r] = l_run[e];
+        }
+      }
+    }
+    named_bar_sync(1, NW * 32);
+    decode_finish_item<R, NW, S>(p, sm, ctid, q_start, kv_head, rows_valid, slot_out);
+  }
+}
+
+template <int R, int NW, int S, int kCopiers>
+__global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
+    decode_kernel_fp8(const __grid_constant__ DecodeParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  auto& sm = *reinterpret_cast<DecodeSmemFp8<R, NW, S>*>(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      sm.slot_consumed[s] = s - S;
+      sm.slot_filled[s] = s - S;
+      mbar_init(&sm.full[s], 32);  // one arrival per lane of the stage's copier
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < kIdxSlots; ++s) {
+      mbar_init(&sm.idx_full[s], 32);
+      mbar_init(&sm.idx_empty[s], 1);
+    }
+    sm.abort = 0;
+    sm.flag = 0;
+    fence_mbar_init();
+  }
+  // Rows past the end of a short stage are converted and read by the P.V MMA with weight 0: they
+  // must hold finite values, so the V ring starts as zero codes (later: earlier stages' codes).
+  for (int i = threadIdx.x; i < S * kStageTokens * kHeadDim / 16; i += blockDim.x) {
+    const int st = i / (kStageTokens * kHeadDim / 16), rem = i % (kStageTokens * kHeadDim / 16);
+    reinterpret_cast<uint4*>(&sm.kv8[st][1][0][0])[rem] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  const int begin = __ldg(p.cta_indptr + blockIdx.x);
+  const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
+  if (warp > kCopiers) {
+    decode_consumer_fp8<R, NW, S>(p, sm, begin, end, warp - 1 - kCopiers);
+  } else if (warp == 0) {
+    decode_index_warp<R, NW, S>(p, sm, begin, end);
+  } else {
+    decode_copier_fp8<R, NW, S, kCopiers>(p, sm, begin, end, warp - 1);
+  }
+}
+
+}  // namespace fi

@@ -73,6 +73,7 @@ struct DecodeParams {
   int window_left;  // >= 0: a row at key position p sees keys p - window_left .. p
   float cap_log2;   // > 0: logit soft-cap in the log2 domain, s -> cap_log2 * tanh(s / cap_log2)
   float inv_cap_log2;
+  float v_scale;  // FP8 pages: V = v_scale * e4m3 code (the K scale is folded into scale_log2)
 };
 
 
@@ -214,9 +215,8 @@ __device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSme
 }
 
 // LDGSTS loader, warp 0: page ids of each stage into a ring of kIdxSlots x 32 entries.
-template <int R, int NW, int S, bool kMs>
-__device__ __forceinline__ void decode_index_warp(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
-                                                  int end) {
+template <int R, int NW, int S, class SM>
+__device__ __forceinline__ void decode_index_warp(const DecodeParams& p, SM& sm, int begin, int end) {
   const int lane = threadIdx.x & 31;
   StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
   bool ok = c.load(p.items);
@@ -317,9 +317,9 @@ __device__ __forceinline__ void load_q_rows(const DecodeParams& p, int q_start, 
 // End of a work item, all NW consumer warps: merge their (O, m, l) states from shared memory in
 // warp order, then write the row (single chunk) or its partial state, and if this chunk is the
 // last of a split row to finish, contract all of the row's slots in plan order.
-template <int R, int NW, int S, bool kMs>
-__device__ __forceinline__ void decode_finish_item(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int ctid,
-                                                   int q_start, int kv_head, int rows_valid, int slot_out) {
+template <int R, int NW, int S, class SM>
+__device__ __forceinline__ void decode_finish_item(const DecodeParams& p, SM& sm, int ctid, int q_start, int kv_head,
+                                                   int rows_valid, int slot_out) {
   for (int u = ctid; u < R * 32; u += NW * 32) {
     const int r = u >> 5, dq = u & 31;
     float M = -INFINITY;

@@ -51,4 +51,7 @@ int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream) {
 // instantiated per rows-per-tile and per log2(H_kv) in 0..4.  Returns an fi_status.
 int launch_decode_nhd(int rows_tile, int log2_heads, int grid, const DecodeParams& p, cudaStream_t stream);
 
+// FP8 (e4m3) KV pages, HND layout, 16-byte-copy loader (power-of-two pages).  Returns an fi_status.
+int launch_decode_fp8(int rows_tile, int grid, const DecodeParams& p, cudaStream_t stream);
+
 }  // namespace fi

@@ -199,6 +199,16 @@ int fi_workspace_set_variant(fi_workspace* ws, int32_t window_left, float logits
   return FI_OK;
 }
 
+int fi_workspace_set_kv_dtype(fi_workspace* ws, int32_t kv_dtype, float k_scale, float v_scale) {
+  if (ws == nullptr || (kv_dtype != FI_KV_DTYPE_BF16 && kv_dtype != FI_KV_DTYPE_E4M3) || !(k_scale > 0.f) ||
+      !(v_scale > 0.f) || k_scale > 1e30f || v_scale > 1e30f)
+    return FI_ERR_INVALID_ARG;
+  ws->variant.kv_dtype = kv_dtype;
+  ws->variant.k_scale = k_scale;
+  ws->variant.v_scale = v_scale;
+  return FI_OK;
+}
+
 int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
             const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim, int page_size,
             int causal, void* stream) {
@@ -222,6 +232,11 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   if (st != FI_OK) return st;
   // NHD decode reads page rows with the 16-byte-copy loader (power-of-two pages); its kernels are
   // instantiated for 1, 2, 4, 8 and 16 KV heads
+  // e4m3 pages: decode tiles, HND layout, power-of-two pages (the FP8 kernel's loader)
+  if (ws->variant.kv_dtype == FI_KV_DTYPE_E4M3 &&
+      (plan.header[fi::H_PATH] != fi::kPathDecode || ws->variant.kv_layout != FI_KV_LAYOUT_HND ||
+       (page_size & (page_size - 1)) != 0))
+    return FI_ERR_UNSUPPORTED;
   if (ws->variant.kv_layout == FI_KV_LAYOUT_NHD && plan.header[fi::H_PATH] == fi::kPathDecode &&
       ((page_size & (page_size - 1)) != 0 || (num_kv_heads & (num_kv_heads - 1)) != 0 || num_kv_heads > 16))
     return FI_ERR_UNSUPPORTED;
@@ -312,6 +327,7 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     p.window_left = var.window_left;
     p.cap_log2 = var.soft_cap > 0.f ? var.soft_cap * fi::kLog2e : 0.f;
     p.inv_cap_log2 = var.soft_cap > 0.f ? 1.f / p.cap_log2 : 0.f;
+    p.v_scale = 1.f;
     p.num_pages = num_pages;
     p.page_size = ps;
     p.page_shift = (ps & (ps - 1)) == 0 ? __builtin_ctz(unsigned(ps)) : -1;
@@ -319,6 +335,11 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     p.group = h[fi::H_GROUP];
     p.slot_rows = fi::kTcRows;
     p.scale_log2 = scale_log2;
+    if (var.kv_dtype == FI_KV_DTYPE_E4M3) {  // every field above is set before this launch
+      p.scale_log2 *= var.k_scale;           // logits of the stored codes, scaled back to K
+      p.v_scale = var.v_scale;
+      return fi::launch_decode_fp8(h[fi::H_ROWS_TILE], h[fi::H_NUM_CTAS], p, s);
+    }
     const bool variant = var_on(var);
     if (nhd)
       return fi::launch_decode_nhd(h[fi::H_ROWS_TILE], __builtin_ctz(unsigned(ws->hkv)), h[fi::H_NUM_CTAS], p, s);

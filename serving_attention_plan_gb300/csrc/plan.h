@@ -61,6 +61,9 @@ struct Variant {
   int window_left = -1;  // < 0: none
   float soft_cap = 0.f;  // <= 0: none
   int kv_layout = 0;     // FI_KV_LAYOUT_HND or FI_KV_LAYOUT_NHD
+  int kv_dtype = 0;      // FI_KV_DTYPE_BF16 or FI_KV_DTYPE_E4M3
+  float k_scale = 1.f;   // e4m3 pages: K = k_scale * code, V = v_scale * code
+  float v_scale = 1.f;
 };
 
 struct Plan {

@@ -246,6 +246,41 @@ def shared_prefix_decode(n_req: int = 64, prefix_len: int = 8192, lo: int = 256,
 
 
 # ---------------------------------------------------------------------------
+# FP8 (e4m3) pages
+# ---------------------------------------------------------------------------
+
+def _e4m3_table() -> np.ndarray:
+    """Values of the 127 non-negative finite e4m3 codes (1 sign, 4 exponent bits with bias 7,
+    3 mantissa bits; exponent 0 holds subnormals; code 0x7F is NaN)."""
+    vals = []
+    for code in range(0x7F):
+        e, m = code >> 3, code & 7
+        vals.append(m / 8.0 * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.array(vals)
+
+
+def to_e4m3(x: np.ndarray) -> np.ndarray:
+    """float -> e4m3 codes, round to nearest (ties to the even code), saturating at +-448."""
+    table = _e4m3_table()
+    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), table[-1])
+    hi = np.clip(np.searchsorted(table, a), 1, len(table) - 1)
+    lo = hi - 1
+    d_lo, d_hi = a - table[lo], table[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(a == 0, 0, code).astype(np.uint8)
+    return (code | np.where(np.signbit(np.asarray(x, dtype=np.float64)) & (code != 0), 0x80, 0)).astype(np.uint8)
+
+
+def as_e4m3(b: PagedBatch, k_scale: float, v_scale: float) -> PagedBatch:
+    """The batch with its K/V pages quantised to e4m3 codes of K / k_scale and V / v_scale."""
+    import dataclasses
+    bf = lambda bits: (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return dataclasses.replace(b, k_pages=to_e4m3(bf(b.k_pages) / k_scale), v_pages=to_e4m3(bf(b.v_pages) / v_scale),
+                               meta=dict(b.meta, k_scale=k_scale, v_scale=v_scale))
+
+
+# ---------------------------------------------------------------------------
 # Kernel-level length distributions (batch 16; constant / uniform / Zipf)
 # ---------------------------------------------------------------------------
 
