@@ -331,6 +331,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--batch", type=int, default=0, help="smaller batch of the decode workload (profiling captures)")
+    ap.add_argument("--only", default="", help="time only this other workload or variant line (profiling captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
@@ -352,6 +353,10 @@ def main():
     from serving_attention_plan_gb300 import workloads as W
 
     hbm_peak, bf16_peak, bf16_sus, peak_src = measured_peaks()
+    if args.only:
+        print(json.dumps({"only": args.only, **bench_other(args.only, torch, dev, hbm_peak, bf16_peak, args.steps,
+                                                          args.warmup)}))
+        return
     if args.batch and args.config == PRIMARY:
         b = W.llama3_8b_decode(batch=args.batch)
     elif args.batch and args.config == "ragged_causal_prefill":

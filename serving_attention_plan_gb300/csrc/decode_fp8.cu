@@ -6,16 +6,19 @@ namespace fi {
 
 namespace {
 
-// Four consumer warps (each converts its own stages), a 16-stage ring of 8 KB stages (128 KB in
-// flight, as much as the bf16 ring's bytes per token allow in its 192 KB), three copier warps.
-constexpr int kFp8Warps = 4;
-constexpr int kFp8Stages = 16;
+// Consumer warps, ring stages of 16 KB (12, or 11 when R = 8 rows need a larger merge buffer),
+// and the code widening (cvt instruction or integer ops; the cvt form measured faster).
+constexpr int kFp8Warps = 8;
+template <int R>
+constexpr int kFp8Stages = R >= 8 ? 11 : 12;
+constexpr bool kFp8Div256 = false;
+constexpr int kFp8Halves = 1;  // consumer warps per stage (two, each on 32 tokens, measured slower)
 
 template <int R>
 int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream) {
-  using Smem = DecodeSmemFp8<R, kFp8Warps, kFp8Stages>;
+  using Smem = DecodeSmemFp8<R, kFp8Warps, kFp8Stages<R>>;
   static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
-  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages, kDecodeCopiers>;
+  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers, kFp8Halves, kFp8Div256>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {

@@ -4,10 +4,13 @@
 // a mixed-precision kernel keeps queries and outputs in 16-bit floats and the KV-cache in fp8,
 // dequantising with a fast numeric converter.  Here: one scale per tensor (K = k_scale * code,
 // V = v_scale * code); the 16-byte-copy loader moves 128-byte K/V rows (half the bytes of bf16)
-// into a ring of 8 KB stages; the consumer warp that owns a stage converts it to f16 in its own
-// 128B-swizzled buffer (cvt e4m3x2 -> f16x2 is exact), releases the ring slot, and runs the same
-// warp-level MMAs as the bf16 consumer in f16 (Q converted from bf16, P rounded to f16).  The K
-// scale is folded into the logit scale and the V scale into the output.
+// into a ring of 64-token stages (8 KB of K + 8 KB of V: the bytes of a bf16 stage, so the
+// loader's fixed cost per stage is spread over as many bytes), 16-byte chunk c of token t at
+// chunk position c ^ (t & 7).
+// Consumer warps read MMA fragments straight from the e4m3 stage with ldmatrix (b16 view: each
+// lane receives four codes) and widen them in registers to f16 (exact), then run f16 warp MMAs
+// (Q converted from bf16 once per item, P rounded to f16).  The K scale is folded into the
+// logit scale and the V scale into the output.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -16,29 +19,41 @@
 
 namespace fi {
 
+constexpr int kFp8StageTokens = 64;
+
 template <int R, int NW, int S>
 struct DecodeSmemFp8 {
-  uint8_t kv8[S][2][kStageTokens][kHeadDim];  // [stage][K|V][token][dim] e4m3 codes, 8 KB per stage
-  __half f16[NW][2][kStageTokens][kHeadDim];   // per consumer warp: its stage in f16, chunks swizzled
+  uint8_t kv8[S][2][kFp8StageTokens][kHeadDim];  // [stage][K|V][token][dim chunks swizzled] e4m3 codes
   float macc[NW][R][kHeadDim];
   float mm[NW][8];
   float ml[NW][8];
-  int32_t idx[kIdxSlots][32];
+  int32_t idx[kIdxSlots][kFp8StageTokens];
   uint64_t full[S];
   uint64_t empty[S];
   uint64_t idx_full[kIdxSlots];
   uint64_t idx_empty[kIdxSlots];
-  int slot_consumed[S];  // as in DecodeSmem: keeps every parity wait unambiguous
+  int slot_consumed[S][2];  // per half-stage consumer: keeps every parity wait unambiguous
   int slot_filled[S];
   int flag;
   int abort;
 };
 
+// Two e4m3 codes -> f16x2 (code of bits 0-7 in the low half), exact.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t r;
   const uint16_t v = static_cast<uint16_t>(two_codes);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
+}
+
+// Bytes sel_lo and sel_hi of x (two e4m3 codes) -> f16x2 holding code / 256, by moving the bit
+// fields: e4m3 (s, 4-bit exponent biased 7, 3-bit mantissa) placed at f16 bit 7 reads as the same
+// significand with the exponent biased 15, i.e. 2^-8 times the value, subnormals included.  The
+// two NaN codes come out as +-480 / 256 instead of NaN.
+template <int kSel>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t x) {
+  const uint32_t a = __byte_perm(x, 0u, kSel);  // [0, code_lo, 0, code_hi]
+  return (a & 0x80008000u) | ((a >> 1) & 0x3f803f80u);
 }
 
 // d (16x8 fp32) += a (16x16 f16, row-major) * b (16x8 f16, column-major)
@@ -55,14 +70,16 @@ __device__ __forceinline__ uint32_t f2_to_f16x2(float lo, float hi) {
 }
 
 // Copier warp `cw` of kCopiers: stages cw, cw + kCopiers, ...; a warp instruction moves four
-// 128-byte rows (lane = token (lane / 8) of the four, 16-byte chunk lane % 8).
+// 128-byte rows (lane = token (lane / 8) of the four, 16-byte chunk lane % 8).  Page ids of the
+// stage's segments: lane l holds those of segments l and l + 32 (64 segments only with 1-token
+// pages; stages start on a page boundary, so segment = token >> page_shift).
 template <int R, int NW, int S, int kCopiers>
 __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm, int begin,
                                                   int end, int cw) {
   const int lane = threadIdx.x & 31;
   const int sh = p.page_shift;
   const int row_mask = p.page_size - 1;
-  StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
+  StageCursorT<kFp8StageTokens> c{begin, end, 0, 0, 0, 0, 0, 0};
   bool ok = c.load(p.items);
   for (int k = 0; k < cw && ok; ++k) ok = c.next(p.items);
   for (int n = cw; ok; n += kCopiers) {
@@ -73,9 +90,14 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
     const int first = t0 >> sh;
     const int nseg = ((t0 + nt - 1) >> sh) - first + 1;
     int pg = (lane < nseg) ? sm.idx[islot][lane] : 0;
+    int pg_hi = (lane + 32 < nseg) ? sm.idx[islot][lane + 32] : 0;
     if (lane < nseg && (pg < 0 || pg >= p.num_pages)) {
       atomicOr(p.err, FI_DEVERR_PAGE_OOB);
       pg = -1;
+    }
+    if (lane + 32 < nseg && (pg_hi < 0 || pg_hi >= p.num_pages)) {
+      atomicOr(p.err, FI_DEVERR_PAGE_OOB);
+      pg_hi = -1;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.idx_empty[islot]);
@@ -85,15 +107,20 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
     const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.k) + (long long)c.kv_head * p.head_stride;
     const uint8_t* vb = reinterpret_cast<const uint8_t*>(p.v) + (long long)c.kv_head * p.head_stride;
 #pragma unroll
-    for (int j = 0; j < kStageTokens / 4; ++j) {
+    for (int j = 0; j < kFp8StageTokens / 4; ++j) {
       const int tok = 4 * j + (lane >> 3);
       const int pos = t0 + tok;
-      const int seg = min(max((pos >> sh) - first, 0), 31);
-      const int page = __shfl_sync(0xffffffffu, pg, seg);
+      const int seg = min(max((pos >> sh) - first, 0), kFp8StageTokens - 1);
+      int page = __shfl_sync(0xffffffffu, pg, seg & 31);
+      if (j >= 8) {  // tokens 32..63: segment >= 32 only for 1-token pages
+        const int hi = __shfl_sync(0xffffffffu, pg_hi, seg & 31);
+        page = seg >= 32 ? hi : page;
+      }
       if (tok < nt && page >= 0) {
         const long long off = (long long)page * p.page_stride + (long long)(pos & row_mask) * kHeadDim + (lane & 7) * 16;
-        cp_async_16(&sm.kv8[slot][0][tok][(lane & 7) * 16], kb + off);
-        cp_async_16(&sm.kv8[slot][1][tok][(lane & 7) * 16], vb + off);
+        const int sw = ((lane & 7) ^ (tok & 7)) * 16;
+        cp_async_16(&sm.kv8[slot][0][tok][sw], kb + off);
+        cp_async_16(&sm.kv8[slot][1][tok][sw], vb + off);
       }
     }
     cp_async_arrive_noinc(&sm.full[slot]);
@@ -104,19 +131,31 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
   cp_async_wait_all();
 }
 
-// Consumer warp w: stages w, w + NW, ... of the CTA's queue.  Same MMA body and fragment layout as
-// decode_consumer_mma (see there), in f16, plus the conversion of each stage.
-template <int R, int NW, int S>
+// Consumer units of kFp8StageTokens / kHalves tokens: unit u of the CTA's queue (stage u / kHalves,
+// part u % kHalves) goes to warp u % NW, so the halves of a stage are computed side by side and the
+// slot, freed after kHalves arrivals, is held for half as long.  Fragment layouts as in
+// decode_consumer_mma, with the reduction dimension permuted where that lets ldmatrix hand each
+// lane whole code groups (a permutation of the summed index changes nothing):
+//   S^T = K Q^T: an x4 ldmatrix of tokens 16mt..+15 x dim chunks 2kb, 2kb+1 gives lane (gq, qd)
+//     codes of dims 16c + 4qd .. +3 of tokens gq and gq + 8; MMA k-slot 2qd, 2qd+1 takes dims
+//     16c + 4qd, +1 and k-slot 8 + 2qd, +1 takes dims 16c + 4qd + 2, +3, so the Q^T fragment of
+//     query row gq is dims 16c + 4qd .. +3 (one 8-byte load per chunk c).
+//   O^T += V^T P^T: an x4 transposing ldmatrix of tokens 16kt..+15 x chunks 2db, 2db+1 gives lane
+//     (gq, qd) codes of tokens 2qd, 2qd+1 (and 8 + those) at dims 2gq, 2gq+1 of each chunk; a byte
+//     permute splits them into the even-dim and the odd-dim fragment, so output tile mt = 2db + e
+//     holds dims 32db + 2gq + e (rows gq) and 32db + 16 + 2gq + e (rows gq + 8).
+// kDiv256: widen codes with e4m3x2_to_f16x2_div256 (integer ops) and fold the 2^8 into the scales.
+template <int R, int NW, int S, int kHalves, bool kDiv256>
 __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm, int begin,
                                                     int end, int w) {
   const int lane = threadIdx.x & 31;
   const int qd = lane & 3;
   const int gq = lane >> 2;
   const int ctid = w * 32 + lane;
-  const int lk_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lk_chunk = lane >> 4;
-  const int lv_tok = (lane & 7) + (lane >> 4) * 8, lv_chunk = (lane >> 3) & 1;
-  const __half* Ks = &sm.f16[w][0][0][0];
-  const __half* Vs = &sm.f16[w][1][0][0];
+  const int lk_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lk_chunk = lane >> 4;  // K x4: tokens, then chunk
+  const int lv_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lv_chunk = lane >> 4;  // V x4: same matrices
+  const float scale_log2 = kDiv256 ? p.scale_log2 * 256.f : p.scale_log2;
+  const float v_scale = kDiv256 ? p.v_scale * 256.f : p.v_scale;
 
   int stage_n = 0;
   bool alive = true;
@@ -125,24 +164,25 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
     const int4 ib = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields + 4));
     const int q_start = ia.y, q_len = ia.z, kv_head = ia.w;
     const int kv_lo = ib.x, kv_hi = ib.y, diag = ib.z, slot_out = ib.w;
-    const int nst = (kv_hi - kv_lo + kStageTokens - 1) / kStageTokens;
+    const int nst = (kv_hi - kv_lo + kFp8StageTokens - 1) / kFp8StageTokens;
     const int rows_valid = q_len * p.group;
 
-    // B fragments of Q^T in f16: row gq, dims 16ks + 2qd (+1) and 16ks + 8 + 2qd (+1)
+    // Q^T fragments in f16: query row gq, dims 16c + 4qd .. +3 for chunk c
     uint32_t qb[8][2];
     if (gq < R && gq < rows_valid) {
       const int tok = q_start + gq / p.group;
       const int head = kv_head * p.group + gq % p.group;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((size_t)tok * p.hqo + head) * kHeadDim);
+      const uint2* qrow = reinterpret_cast<const uint2*>(p.q + ((size_t)tok * p.hqo + head) * kHeadDim);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const float2 a = bf16x2_to_f2(__ldg(qrow + 8 * ks + qd)), b = bf16x2_to_f2(__ldg(qrow + 8 * ks + 4 + qd));
-        qb[ks][0] = f2_to_f16x2(a.x, a.y);
-        qb[ks][1] = f2_to_f16x2(b.x, b.y);
+      for (int c = 0; c < 8; ++c) {
+        const uint2 u = __ldg(qrow + 4 * c + qd);
+        const float2 a = bf16x2_to_f2(u.x), b = bf16x2_to_f2(u.y);
+        qb[c][0] = f2_to_f16x2(a.x, a.y);
+        qb[c][1] = f2_to_f16x2(b.x, b.y);
       }
     } else {
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+      for (int c = 0; c < 8; ++c) qb[c][0] = qb[c][1] = 0u;
     }
     float o[8][4];
 #pragma unroll
@@ -152,65 +192,59 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
     const int low0 = p.window_left >= 0 ? lim0 - p.window_left : INT_MIN;
     const int low1 = p.window_left >= 0 ? lim1 - p.window_left : INT_MIN;
 
-    for (int st = 0; st < nst; ++st) {
-      const int n = stage_n + st;
-      if (n % NW != w) continue;
+    constexpr int kSub = kFp8StageTokens / kHalves;  // tokens of one consumer unit
+    for (int u = 0; u < nst * kHalves; ++u) {
+      const int n = stage_n + u / kHalves, h = u % kHalves;
+      if ((stage_n * kHalves + u) % NW != w) continue;
       const int slot = n % S;
       if (!alive) continue;
-      const bool got = spin_until_eq(&sm.slot_consumed[slot], n - S, p.err, &sm.abort) &&
+      const bool got = spin_until_eq(&sm.slot_consumed[slot][h], n - S, p.err, &sm.abort) &&
                        mbar_wait(&sm.full[slot], (n / S) & 1, p.err, &sm.abort);
       if (!__all_sync(0xffffffffu, got)) {
         alive = false;
         continue;
       }
-      // ---- e4m3 -> f16 into this warp's buffer (16-byte chunk c of token t at c ^ (t & 7)) ---
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-#pragma unroll
-        for (int i = 0; i < kStageTokens / 4; ++i) {
-          const int tok = 4 * i + (lane >> 3), q = lane & 7;
-          const uint4 raw = *reinterpret_cast<const uint4*>(&sm.kv8[slot][kv][tok][q * 16]);
-          uint4 h0, h1;
-          h0.x = e4m3x2_to_f16x2(raw.x);
-          h0.y = e4m3x2_to_f16x2(raw.x >> 16);
-          h0.z = e4m3x2_to_f16x2(raw.y);
-          h0.w = e4m3x2_to_f16x2(raw.y >> 16);
-          h1.x = e4m3x2_to_f16x2(raw.z);
-          h1.y = e4m3x2_to_f16x2(raw.z >> 16);
-          h1.z = e4m3x2_to_f16x2(raw.w);
-          h1.w = e4m3x2_to_f16x2(raw.w >> 16);
-          __half* row = &sm.f16[w][kv][tok][0];
-          *reinterpret_cast<uint4*>(row + ((2 * q) ^ (tok & 7)) * 8) = h0;
-          *reinterpret_cast<uint4*>(row + ((2 * q + 1) ^ (tok & 7)) * 8) = h1;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {  // the stage now lives in this warp's f16 buffer: its ring slot is free
-        *reinterpret_cast<volatile int*>(&sm.slot_consumed[slot]) = n;
-        mbar_arrive(&sm.empty[slot]);
-      }
-      const int t0 = kv_lo + st * kStageTokens;
-      const int nt = min(kStageTokens, kv_hi - t0);
-      const int n_mt = nt > 16 ? 2 : 1;
+      const int t0 = kv_lo + (u / kHalves) * kFp8StageTokens + h * kSub;
+      const int nt = min(kSub, kv_hi - t0);
+      if (nt > 0) {
+      const int n_mt = (nt + 15) >> 4;
+      const uint8_t* Ks = &sm.kv8[slot][0][h * kSub][0];
+      const uint8_t* Vs = &sm.kv8[slot][1][h * kSub][0];
 
-      float s[2][4];
+      constexpr int kMt = kSub / 16;
+      float s[kMt][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < kMt; ++mt) {
         s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
         if (mt < n_mt) {
           const int tok = 16 * mt + lk_tok;
-          const __half* row = Ks + tok * kHeadDim;
+          const uint8_t* row = Ks + tok * kHeadDim;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a[4];
-            ldsm_x4(a, row + (((2 * ks + lk_chunk) ^ (tok & 7)) * 8));
-            mma_16816_f16(s[mt], a, qb[ks][0], qb[ks][1]);
+          for (int kb = 0; kb < 4; ++kb) {
+            uint32_t r[4];
+            ldsm_x4(r, row + (((2 * kb + lk_chunk) ^ (tok & 7)) * 16));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // chunk 2kb + h: registers r[2h] (token gq), r[2h+1] (gq + 8)
+              uint32_t a[4];
+              if constexpr (kDiv256) {
+                a[0] = e4m3x2_to_f16x2_div256<0x1404>(r[2 * h]);
+                a[1] = e4m3x2_to_f16x2_div256<0x1404>(r[2 * h + 1]);
+                a[2] = e4m3x2_to_f16x2_div256<0x3424>(r[2 * h]);
+                a[3] = e4m3x2_to_f16x2_div256<0x3424>(r[2 * h + 1]);
+              } else {
+                a[0] = e4m3x2_to_f16x2(r[2 * h]);
+                a[1] = e4m3x2_to_f16x2(r[2 * h + 1]);
+                a[2] = e4m3x2_to_f16x2(r[2 * h] >> 16);
+                a[3] = e4m3x2_to_f16x2(r[2 * h + 1] >> 16);
+              }
+              mma_16816_f16(s[mt], a, qb[2 * kb + h][0], qb[2 * kb + h][1]);
+            }
           }
         }
       }
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < kMt; ++mt) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int t = 16 * mt + 8 * h + gq;
@@ -218,7 +252,7 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const bool vis = in && (t0 + t <= (e ? lim1 : lim0)) && (t0 + t >= (e ? low1 : low0));
-            float sv = s[mt][2 * h + e] * p.scale_log2;
+            float sv = s[mt][2 * h + e] * scale_log2;
             if (p.cap_log2 > 0.f) sv = p.cap_log2 * tanh_exp2(sv * p.inv_cap_log2);
             const float v = vis ? sv : -INFINITY;
             s[mt][2 * h + e] = v;
@@ -238,9 +272,9 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
         m_run[e] = m_new;
         l_run[e] *= alpha[e];
       }
-      uint32_t pb[2][2];
+      uint32_t pb[kMt][2];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < kMt; ++mt) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float p0 = fast_exp2(s[mt][2 * h] - m_use[0]);
@@ -258,19 +292,41 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
         o[mt][3] *= alpha[1];
       }
 #pragma unroll
-      for (int kt = 0; kt < 2; ++kt) {
+      for (int kt = 0; kt < kMt; ++kt) {
         if (kt < n_mt) {
           const int tok = 16 * kt + lv_tok;
-          const __half* row = Vs + tok * kHeadDim;
+          const uint8_t* row = Vs + tok * kHeadDim;
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            uint32_t a[4];
-            ldsm_x4_trans(a, row + (((2 * mt + lv_chunk) ^ (tok & 7)) * 8));
-            mma_16816_f16(o[mt], a, pb[kt][0], pb[kt][1]);
+          for (int db = 0; db < 4; ++db) {
+            // r[0]: tokens 2qd, 2qd+1 x dims 2gq, 2gq+1 of chunk 2db; r[1]: tokens + 8;
+            // r[2], r[3]: the same for chunk 2db + 1.  Bytes of each: [t0 d0, t0 d1, t1 d0, t1 d1].
+            uint32_t r[4];
+            ldsm_x4_trans(r, row + (((2 * db + lv_chunk) ^ (tok & 7)) * 16));
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              uint32_t a[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                // fragment order: (chunk 2db, tokens lo), (chunk 2db+1, lo), (2db, hi), (2db+1, hi)
+                const uint32_t x = r[(i & 1) * 2 + (i >> 1)];
+                if constexpr (kDiv256) {
+                  a[i] = e ? e4m3x2_to_f16x2_div256<0x3414>(x) : e4m3x2_to_f16x2_div256<0x2404>(x);
+                } else {
+                  const uint32_t y = __byte_perm(x, 0u, 0x3120);  // [t0 d0, t1 d0, t0 d1, t1 d1]
+                  a[i] = e4m3x2_to_f16x2(e ? (y >> 16) : y);
+                }
+              }
+              mma_16816_f16(o[2 * db + e], a, pb[kt][0], pb[kt][1]);
+            }
           }
         }
       }
-      __syncwarp();  // this warp's f16 buffer is read before the next stage's conversion overwrites it
+      }  // nt > 0
+      __syncwarp();
+      if (lane == 0) {
+        *reinterpret_cast<volatile int*>(&sm.slot_consumed[slot][h]) = n;
+        mbar_arrive(&sm.empty[slot]);
+      }
     }
     stage_n += nst;
 
@@ -285,9 +341,12 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
       const int r = 2 * qd + e;
       if (r < R) {
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {  // the V scale enters with the unnormalised output
-          sm.macc[w][r][16 * mt + gq] = o[mt][e] * p.v_scale;
-          sm.macc[w][r][16 * mt + 8 + gq] = o[mt][2 + e] * p.v_scale;
+        for (int db = 0; db < 4; ++db) {  // the V scale enters with the unnormalised output
+#pragma unroll
+          for (int ee = 0; ee < 2; ++ee) {
+            sm.macc[w][r][32 * db + 2 * gq + ee] = o[2 * db + ee][e] * v_scale;
+            sm.macc[w][r][32 * db + 16 + 2 * gq + ee] = o[2 * db + ee][2 + e] * v_scale;
+          }
         }
         if (gq == 0) {
           sm.mm[w][r] = m_run[e];
@@ -300,7 +359,7 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
   }
 }
 
-template <int R, int NW, int S, int kCopiers>
+template <int R, int NW, int S, int kCopiers, int kHalves, bool kDiv256>
 __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
     decode_kernel_fp8(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -308,10 +367,10 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      sm.slot_consumed[s] = s - S;
+      sm.slot_consumed[s][0] = sm.slot_consumed[s][1] = s - S;
       sm.slot_filled[s] = s - S;
       mbar_init(&sm.full[s], 32);  // one arrival per lane of the stage's copier
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], kHalves);  // one arrival per half-stage consumer
     }
     for (int s = 0; s < kIdxSlots; ++s) {
       mbar_init(&sm.idx_full[s], 32);
@@ -321,19 +380,19 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
     sm.flag = 0;
     fence_mbar_init();
   }
-  // Rows past the end of a short stage are converted and read by the P.V MMA with weight 0: they
-  // must hold finite values, so the V ring starts as zero codes (later: earlier stages' codes).
-  for (int i = threadIdx.x; i < S * kStageTokens * kHeadDim / 16; i += blockDim.x) {
-    const int st = i / (kStageTokens * kHeadDim / 16), rem = i % (kStageTokens * kHeadDim / 16);
+  // Rows past the end of a short stage are read by the P.V MMA with weight 0: they must hold
+  // finite values, so the V ring starts as zero codes (later: earlier stages' codes).
+  for (int i = threadIdx.x; i < S * kFp8StageTokens * kHeadDim / 16; i += blockDim.x) {
+    const int st = i / (kFp8StageTokens * kHeadDim / 16), rem = i % (kFp8StageTokens * kHeadDim / 16);
     reinterpret_cast<uint4*>(&sm.kv8[st][1][0][0])[rem] = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp > kCopiers) {
-    decode_consumer_fp8<R, NW, S>(p, sm, begin, end, warp - 1 - kCopiers);
+    decode_consumer_fp8<R, NW, S, kHalves, kDiv256>(p, sm, begin, end, warp - 1 - kCopiers);
   } else if (warp == 0) {
-    decode_index_warp<R, NW, S>(p, sm, begin, end);
+    decode_index_warp<R, NW, S, DecodeSmemFp8<R, NW, S>, kFp8StageTokens>(p, sm, begin, end);
   } else {
     decode_copier_fp8<R, NW, S, kCopiers>(p, sm, begin, end, warp - 1);
   }

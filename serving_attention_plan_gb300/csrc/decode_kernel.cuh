@@ -109,7 +109,8 @@ struct DecodeSmem {
 };
 
 // Walks the stages of one CTA's queue in order: (item, stage within item).
-struct StageCursor {
+template <int kT>
+struct StageCursorT {
   int pos, end;
   int st, nst;
   int page_base, kv_head, kv_lo, kv_hi;
@@ -122,7 +123,7 @@ struct StageCursor {
       kv_head = a.w;
       kv_lo = b.x;
       kv_hi = b.y;
-      nst = (kv_hi - kv_lo + kStageTokens - 1) / kStageTokens;
+      nst = (kv_hi - kv_lo + kT - 1) / kT;
       st = 0;
       if (nst > 0) return true;
       ++pos;
@@ -134,9 +135,10 @@ struct StageCursor {
     ++pos;
     return load(items);
   }
-  __device__ __forceinline__ int tok0() const { return kv_lo + st * kStageTokens; }
-  __device__ __forceinline__ int ntok() const { return min(kStageTokens, kv_hi - tok0()); }
+  __device__ __forceinline__ int tok0() const { return kv_lo + st * kT; }
+  __device__ __forceinline__ int ntok() const { return min(kT, kv_hi - tok0()); }
 };
+using StageCursor = StageCursorT<kStageTokens>;
 
 template <int R, int NW, int S, bool kMs>
 __device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin, int end) {
@@ -214,11 +216,12 @@ __device__ __forceinline__ void decode_producer(const DecodeParams& p, DecodeSme
   for (int n = max(0, issued - S); n < issued; ++n) mbar_wait_bounded(&sm.full[n % S], (n / S) & 1);
 }
 
-// LDGSTS loader, warp 0: page ids of each stage into a ring of kIdxSlots x 32 entries.
-template <int R, int NW, int S, class SM>
+// LDGSTS loader, warp 0: page ids of each stage into a ring of kIdxSlots x kT entries (kT tokens
+// per stage: up to kT pages).
+template <int R, int NW, int S, class SM, int kT = kStageTokens>
 __device__ __forceinline__ void decode_index_warp(const DecodeParams& p, SM& sm, int begin, int end) {
   const int lane = threadIdx.x & 31;
-  StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
+  StageCursorT<kT> c{begin, end, 0, 0, 0, 0, 0, 0};
   bool ok = c.load(p.items);
   for (int n = 0; ok; ++n) {
     const int slot = n % kIdxSlots, fill = n / kIdxSlots;
@@ -227,6 +230,9 @@ __device__ __forceinline__ void decode_index_warp(const DecodeParams& p, SM& sm,
     const int first = t0 >> p.page_shift;
     const int nseg = ((t0 + c.ntok() - 1) >> p.page_shift) - first + 1;
     if (lane < nseg) cp_async_4(&sm.idx[slot][lane], p.kv_indices + c.page_base + first + lane);
+    if constexpr (kT > 32) {
+      if (lane + 32 < nseg) cp_async_4(&sm.idx[slot][lane + 32], p.kv_indices + c.page_base + first + lane + 32);
+    }
     cp_async_arrive_noinc(&sm.idx_full[slot]);
     ok = c.next(p.items);
   }
