@@ -12,7 +12,10 @@ kernel launch (page gather, attention, in-kernel merge of split rows).
             across layers).
   e2e    -- same metric through the C ABI from host buffers: every step plans
             from host index arrays (pinned copy inside), copies q host->device
-            from pinned memory, runs, and reads o and lse back.
+            from pinned memory, runs, and reads o and lse back.  Steps alternate
+            between two workspaces on two streams, so one step's host planning
+            and copies overlap the other's kernel (the serial time is reported
+            beside it).
   configs -- the other workloads (tiny, skewed long-context, causal prefill,
             shared prefix) timed the same way, each with its own unit.
 
@@ -151,17 +154,22 @@ def time_launches(torch, fn, steps, warmup, barrier=None):
 
 
 def time_launches_cold(torch, fn, steps, warmup):
-    """Device time of one call with a cold L2: before each call a buffer twice the L2 size is written
-    (outside the timed events); the CUDA events bracket the call alone.  Mean over `steps`."""
+    """Device time of one call with a cold L2: before each call a buffer twice the L2 size is written,
+    then another one of that size is read (outside the timed events), so L2 holds none of the call's
+    data and no dirty lines whose write-back the call would pay for; the CUDA events bracket the call
+    alone.  Mean over `steps`."""
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
+    clean = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device="cuda")
     for _ in range(warmup):
         flush.fill_(1)
+        clean.sum()
         fn()
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
     ev = []
     for i in range(steps):
         flush.fill_(i)
+        clean.sum()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         fn()
@@ -401,7 +409,53 @@ def main():
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
+    serial_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+
+    # The same steps pipelined: two workspaces, each with its own q/o/lse buffers and stream.
+    # Step i runs on context i % 2; before reusing a context the host waits for its previous
+    # step's completion event, i.e. for that step's o and lse to be in host memory.
+    from serving_attention_plan_gb300 import binding as B
+
+    class _Ctx:
+        pass
+
+    ctxs = []
+    for _ in range(2):
+        c = _Ctx()
+        c.ws = B.Workspace(b.batch_size, b.total_q, int(b.kv_indptr[-1]), b.num_qo_heads, b.num_kv_heads,
+                           b.head_dim)
+        c.q, c.o, c.lse = torch.empty_like(case.q), torch.empty_like(case.o), torch.empty_like(case.lse)
+        c.o_host, c.lse_host = torch.empty_like(o_host).pin_memory(), torch.empty_like(lse_host).pin_memory()
+        c.stream, c.done, c.busy = torch.cuda.Stream(), torch.cuda.Event(), False
+        ctxs.append(c)
+
+    def e2e_step_pipelined(i):
+        c = ctxs[i % 2]
+        if c.busy:
+            c.done.synchronize()
+        c.ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.page_size, b.causal, stream=c.stream)
+        with torch.cuda.stream(c.stream):
+            c.q.view(torch.int16).copy_(q_host, non_blocking=True)
+        c.ws.run(c.q, case.k, case.v, c.o, c.lse, stream=c.stream)
+        with torch.cuda.stream(c.stream):
+            c.o_host.copy_(c.o.view(torch.int16), non_blocking=True)
+            c.lse_host.copy_(c.lse, non_blocking=True)
+        c.done.record(c.stream)
+        c.busy = True
+
+    for i in range(4):
+        e2e_step_pipelined(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step_pipelined(i)
+    for c in ctxs:
+        c.done.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    e2e_same = all(torch.equal(c.o_host, o_host) and torch.equal(c.lse_host, lse_host) for c in ctxs)
+    e2e_errors = [c.ws.get_error() for c in ctxs]
+    if any(e2e_errors):
+        print(f"bench: device error bits {e2e_errors} during the end-to-end steps", file=sys.stderr)
     plan_bytes = 4 * (16 + int(hdr[5]) + 1 + 8 * int(hdr[6]) + 8 * int(hdr[7]) + int(hdr[8]) + int(b.kv_indptr[-1]))
     h2d = int(b.q.nbytes) + plan_bytes
     d2h = int(o_host.numel() * 2 + lse_host.numel() * 4)
@@ -432,7 +486,10 @@ def main():
                      "traffic": ncu_traffic(f"{kernel_name}/{args.config}"), "kernel": kernel_name,
                      "algorithmic_bytes_per_launch": abytes},
         "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "pipelining": "2 workspaces / 2 streams", "outputs_equal_serial": e2e_same,
+                "serial_ms_per_step": serial_ms,
+                "serial_value": world * nbytes / (serial_ms * 1e-3) / 1e9},
         "gpu_launches": args.steps,
         "device_errors": device_errors,
         "clocks": clocks,
@@ -519,7 +576,7 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
     hdr = c.ws.info()
     errs = c.ws.get_error()
     out = {"us_per_batch": ms * 1e3, "path": path_name(w, hdr),
-           "config": dict(workload_config(name, w), l2="flushed before every launch" if cold else
+           "config": dict(workload_config(name, w), l2="flushed before every launch (2x L2 written, then 2x L2 of other data read)" if cold else
                           "inputs larger than L2"),
            "device_errors": errs}
     if hdr[1] == 1:
