@@ -6,19 +6,19 @@ namespace fi {
 
 namespace {
 
-// Consumer warps, ring stages of 16 KB (12, or 11 when R = 8 rows need a larger merge buffer),
-// and the code widening (cvt instruction or integer ops; the cvt form measured faster).
+// Eight consumer warps and a ring of 16 KB stages: 12, or 11 when R = 8 rows need a larger merge
+// buffer.  Measured on GB300 (Llama-3-8B-shaped batch): 4 / 6 / 10 consumer warps were slower, and
+// so were two warps per stage (32 tokens each) and widening the codes with integer ops instead of
+// the cvt instruction.
 constexpr int kFp8Warps = 8;
 template <int R>
 constexpr int kFp8Stages = R >= 8 ? 11 : 12;
-constexpr bool kFp8Div256 = false;
-constexpr int kFp8Halves = 1;  // consumer warps per stage (two, each on 32 tokens, measured slower)
 
 template <int R>
 int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream) {
   using Smem = DecodeSmemFp8<R, kFp8Warps, kFp8Stages<R>>;
   static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
-  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers, kFp8Halves, kFp8Div256>;
+  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {

@@ -32,7 +32,7 @@ struct DecodeSmemFp8 {
   uint64_t empty[S];
   uint64_t idx_full[kIdxSlots];
   uint64_t idx_empty[kIdxSlots];
-  int slot_consumed[S][2];  // per half-stage consumer: keeps every parity wait unambiguous
+  int slot_consumed[S];  // as in DecodeSmem: keeps every parity wait unambiguous
   int slot_filled[S];
   int flag;
   int abort;
@@ -44,16 +44,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   const uint16_t v = static_cast<uint16_t>(two_codes);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
-}
-
-// Bytes sel_lo and sel_hi of x (two e4m3 codes) -> f16x2 holding code / 256, by moving the bit
-// fields: e4m3 (s, 4-bit exponent biased 7, 3-bit mantissa) placed at f16 bit 7 reads as the same
-// significand with the exponent biased 15, i.e. 2^-8 times the value, subnormals included.  The
-// two NaN codes come out as +-480 / 256 instead of NaN.
-template <int kSel>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t x) {
-  const uint32_t a = __byte_perm(x, 0u, kSel);  // [0, code_lo, 0, code_hi]
-  return (a & 0x80008000u) | ((a >> 1) & 0x3f803f80u);
 }
 
 // d (16x8 fp32) += a (16x16 f16, row-major) * b (16x8 f16, column-major)
@@ -131,9 +121,7 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
   cp_async_wait_all();
 }
 
-// Consumer units of kFp8StageTokens / kHalves tokens: unit u of the CTA's queue (stage u / kHalves,
-// part u % kHalves) goes to warp u % NW, so the halves of a stage are computed side by side and the
-// slot, freed after kHalves arrivals, is held for half as long.  Fragment layouts as in
+// Consumer warp w: stages w, w + NW, ... of the CTA's queue.  Fragment layouts as in
 // decode_consumer_mma, with the reduction dimension permuted where that lets ldmatrix hand each
 // lane whole code groups (a permutation of the summed index changes nothing):
 //   S^T = K Q^T: an x4 ldmatrix of tokens 16mt..+15 x dim chunks 2kb, 2kb+1 gives lane (gq, qd)
@@ -144,8 +132,7 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
 //     (gq, qd) codes of tokens 2qd, 2qd+1 (and 8 + those) at dims 2gq, 2gq+1 of each chunk; a byte
 //     permute splits them into the even-dim and the odd-dim fragment, so output tile mt = 2db + e
 //     holds dims 32db + 2gq + e (rows gq) and 32db + 16 + 2gq + e (rows gq + 8).
-// kDiv256: widen codes with e4m3x2_to_f16x2_div256 (integer ops) and fold the 2^8 into the scales.
-template <int R, int NW, int S, int kHalves, bool kDiv256>
+template <int R, int NW, int S>
 __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm, int begin,
                                                     int end, int w) {
   const int lane = threadIdx.x & 31;
@@ -154,8 +141,6 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
   const int ctid = w * 32 + lane;
   const int lk_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lk_chunk = lane >> 4;  // K x4: tokens, then chunk
   const int lv_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lv_chunk = lane >> 4;  // V x4: same matrices
-  const float scale_log2 = kDiv256 ? p.scale_log2 * 256.f : p.scale_log2;
-  const float v_scale = kDiv256 ? p.v_scale * 256.f : p.v_scale;
 
   int stage_n = 0;
   bool alive = true;
@@ -192,26 +177,24 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
     const int low0 = p.window_left >= 0 ? lim0 - p.window_left : INT_MIN;
     const int low1 = p.window_left >= 0 ? lim1 - p.window_left : INT_MIN;
 
-    constexpr int kSub = kFp8StageTokens / kHalves;  // tokens of one consumer unit
-    for (int u = 0; u < nst * kHalves; ++u) {
-      const int n = stage_n + u / kHalves, h = u % kHalves;
-      if ((stage_n * kHalves + u) % NW != w) continue;
+    for (int st = 0; st < nst; ++st) {
+      const int n = stage_n + st;
+      if (n % NW != w) continue;
       const int slot = n % S;
       if (!alive) continue;
-      const bool got = spin_until_eq(&sm.slot_consumed[slot][h], n - S, p.err, &sm.abort) &&
+      const bool got = spin_until_eq(&sm.slot_consumed[slot], n - S, p.err, &sm.abort) &&
                        mbar_wait(&sm.full[slot], (n / S) & 1, p.err, &sm.abort);
       if (!__all_sync(0xffffffffu, got)) {
         alive = false;
         continue;
       }
-      const int t0 = kv_lo + (u / kHalves) * kFp8StageTokens + h * kSub;
-      const int nt = min(kSub, kv_hi - t0);
-      if (nt > 0) {
+      const int t0 = kv_lo + st * kFp8StageTokens;
+      const int nt = min(kFp8StageTokens, kv_hi - t0);
       const int n_mt = (nt + 15) >> 4;
-      const uint8_t* Ks = &sm.kv8[slot][0][h * kSub][0];
-      const uint8_t* Vs = &sm.kv8[slot][1][h * kSub][0];
+      const uint8_t* Ks = &sm.kv8[slot][0][0][0];
+      const uint8_t* Vs = &sm.kv8[slot][1][0][0];
 
-      constexpr int kMt = kSub / 16;
+      constexpr int kMt = kFp8StageTokens / 16;
       float s[kMt][4];
 #pragma unroll
       for (int mt = 0; mt < kMt; ++mt) {
@@ -226,17 +209,10 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // chunk 2kb + h: registers r[2h] (token gq), r[2h+1] (gq + 8)
               uint32_t a[4];
-              if constexpr (kDiv256) {
-                a[0] = e4m3x2_to_f16x2_div256<0x1404>(r[2 * h]);
-                a[1] = e4m3x2_to_f16x2_div256<0x1404>(r[2 * h + 1]);
-                a[2] = e4m3x2_to_f16x2_div256<0x3424>(r[2 * h]);
-                a[3] = e4m3x2_to_f16x2_div256<0x3424>(r[2 * h + 1]);
-              } else {
-                a[0] = e4m3x2_to_f16x2(r[2 * h]);
-                a[1] = e4m3x2_to_f16x2(r[2 * h + 1]);
-                a[2] = e4m3x2_to_f16x2(r[2 * h] >> 16);
-                a[3] = e4m3x2_to_f16x2(r[2 * h + 1] >> 16);
-              }
+              a[0] = e4m3x2_to_f16x2(r[2 * h]);
+              a[1] = e4m3x2_to_f16x2(r[2 * h + 1]);
+              a[2] = e4m3x2_to_f16x2(r[2 * h] >> 16);
+              a[3] = e4m3x2_to_f16x2(r[2 * h + 1] >> 16);
               mma_16816_f16(s[mt], a, qb[2 * kb + h][0], qb[2 * kb + h][1]);
             }
           }
@@ -252,7 +228,7 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const bool vis = in && (t0 + t <= (e ? lim1 : lim0)) && (t0 + t >= (e ? low1 : low0));
-            float sv = s[mt][2 * h + e] * scale_log2;
+            float sv = s[mt][2 * h + e] * p.scale_log2;
             if (p.cap_log2 > 0.f) sv = p.cap_log2 * tanh_exp2(sv * p.inv_cap_log2);
             const float v = vis ? sv : -INFINITY;
             s[mt][2 * h + e] = v;
@@ -309,22 +285,17 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
               for (int i = 0; i < 4; ++i) {
                 // fragment order: (chunk 2db, tokens lo), (chunk 2db+1, lo), (2db, hi), (2db+1, hi)
                 const uint32_t x = r[(i & 1) * 2 + (i >> 1)];
-                if constexpr (kDiv256) {
-                  a[i] = e ? e4m3x2_to_f16x2_div256<0x3414>(x) : e4m3x2_to_f16x2_div256<0x2404>(x);
-                } else {
-                  const uint32_t y = __byte_perm(x, 0u, 0x3120);  // [t0 d0, t1 d0, t0 d1, t1 d1]
-                  a[i] = e4m3x2_to_f16x2(e ? (y >> 16) : y);
-                }
+                const uint32_t y = __byte_perm(x, 0u, 0x3120);  // [t0 d0, t1 d0, t0 d1, t1 d1]
+                a[i] = e4m3x2_to_f16x2(e ? (y >> 16) : y);
               }
               mma_16816_f16(o[2 * db + e], a, pb[kt][0], pb[kt][1]);
             }
           }
         }
       }
-      }  // nt > 0
       __syncwarp();
       if (lane == 0) {
-        *reinterpret_cast<volatile int*>(&sm.slot_consumed[slot][h]) = n;
+        *reinterpret_cast<volatile int*>(&sm.slot_consumed[slot]) = n;
         mbar_arrive(&sm.empty[slot]);
       }
     }
@@ -344,8 +315,8 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
         for (int db = 0; db < 4; ++db) {  // the V scale enters with the unnormalised output
 #pragma unroll
           for (int ee = 0; ee < 2; ++ee) {
-            sm.macc[w][r][32 * db + 2 * gq + ee] = o[2 * db + ee][e] * v_scale;
-            sm.macc[w][r][32 * db + 16 + 2 * gq + ee] = o[2 * db + ee][2 + e] * v_scale;
+            sm.macc[w][r][32 * db + 2 * gq + ee] = o[2 * db + ee][e] * p.v_scale;
+            sm.macc[w][r][32 * db + 16 + 2 * gq + ee] = o[2 * db + ee][2 + e] * p.v_scale;
           }
         }
         if (gq == 0) {
@@ -359,7 +330,7 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
   }
 }
 
-template <int R, int NW, int S, int kCopiers, int kHalves, bool kDiv256>
+template <int R, int NW, int S, int kCopiers>
 __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
     decode_kernel_fp8(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -367,10 +338,10 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      sm.slot_consumed[s][0] = sm.slot_consumed[s][1] = s - S;
+      sm.slot_consumed[s] = s - S;
       sm.slot_filled[s] = s - S;
       mbar_init(&sm.full[s], 32);  // one arrival per lane of the stage's copier
-      mbar_init(&sm.empty[s], kHalves);  // one arrival per half-stage consumer
+      mbar_init(&sm.empty[s], 1);
     }
     for (int s = 0; s < kIdxSlots; ++s) {
       mbar_init(&sm.idx_full[s], 32);
@@ -390,7 +361,7 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp > kCopiers) {
-    decode_consumer_fp8<R, NW, S, kHalves, kDiv256>(p, sm, begin, end, warp - 1 - kCopiers);
+    decode_consumer_fp8<R, NW, S>(p, sm, begin, end, warp - 1 - kCopiers);
   } else if (warp == 0) {
     decode_index_warp<R, NW, S, DecodeSmemFp8<R, NW, S>, kFp8StageTokens>(p, sm, begin, end);
   } else {
