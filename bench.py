@@ -387,6 +387,20 @@ def main():
     value = replica_throughput(nbytes, ms * 1e-3, world) / 1e9
     achieved = abytes / (ms * 1e-3) / 1e9
 
+    # host time of fi_plan (planning + enqueueing the upload) with the device idle, and the launch
+    # replayed from a CUDA graph (fi_run is capturable; the plan stays in the workspace)
+    plan_us = []
+    for _ in range(30):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        case.plan()
+        plan_us.append((time.perf_counter() - t0) * 1e6)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        case.run()
+    graph_ms = time_launches(torch, graph.replay, min(args.steps, 500), 10)
+
     # end to end through the C ABI from host buffers
     q_host = torch.from_numpy(np.ascontiguousarray(b.q).view(np.int16)).pin_memory()
     o_host = torch.empty((b.total_q, b.num_qo_heads, b.head_dim), dtype=torch.int16).pin_memory()
@@ -490,6 +504,9 @@ def main():
                 "pipelining": "2 workspaces / 2 streams", "outputs_equal_serial": e2e_same,
                 "serial_ms_per_step": serial_ms,
                 "serial_value": world * nbytes / (serial_ms * 1e-3) / 1e9},
+        "breakdown": {"plan_host_us_median": float(np.median(plan_us)), "graph_replay_us": graph_ms * 1e3,
+                      "note": "fi_plan on the host with the device idle; one fi_run captured in a CUDA graph and "
+                              "replayed back to back"},
         "gpu_launches": args.steps,
         "device_errors": device_errors,
         "clocks": clocks,
@@ -579,6 +596,8 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
            "config": dict(workload_config(name, w), l2="flushed before every launch (2x L2 written, then 2x L2 of other data read)" if cold else
                           "inputs larger than L2"),
            "device_errors": errs}
+    if cold:
+        out["us_per_batch_hot_l2"] = time_launches(torch, c.run, steps, warmup) * 1e3
     if hdr[1] == 1:
         tf = flops(w) / (ms * 1e-3) / 1e12
         out.update({"tflops": tf, "frac_of_bf16_peak": tf / bf16_peak})
