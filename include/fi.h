@@ -134,11 +134,12 @@ int fi_workspace_set_variant(fi_workspace* ws, int32_t window_left, float logits
  *   kv_dtype          FI_KV_DTYPE_BF16 (default) or FI_KV_DTYPE_E4M3
  *   k_scale, v_scale  > 0; used with e4m3 pages
  *
- * With e4m3, k_pages / v_pages hold one byte per element in the HND shape, q and
- * o stay bf16, and the decode kernel computes in f16 MMAs with fp32
- * accumulation.  e4m3 plans need decode tiles, the HND layout and a
- * power-of-two page size: fi_plan returns UNSUPPORTED otherwise.  NaN codes in
- * the pages give undefined rows.  Errors: INVALID_ARG.
+ * With e4m3, k_pages / v_pages hold one byte per element in the workspace's
+ * layout (HND or NHD), q and o stay bf16, and the decode kernel computes in f16
+ * MMAs with fp32 accumulation.  e4m3 plans need decode tiles and a power-of-two
+ * page size (NHD pages, as for bf16, also a power-of-two H_kv of at most 16):
+ * fi_plan returns UNSUPPORTED otherwise.  NaN codes in the pages give undefined
+ * rows.  Errors: INVALID_ARG.
  */
 int fi_workspace_set_kv_dtype(fi_workspace* ws, int32_t kv_dtype, float k_scale, float v_scale);
 

@@ -14,11 +14,11 @@ constexpr int kFp8Warps = 8;
 template <int R>
 constexpr int kFp8Stages = R >= 8 ? 11 : 12;
 
-template <int R>
+template <int R, bool kNhd>
 int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream) {
   using Smem = DecodeSmemFp8<R, kFp8Warps, kFp8Stages<R>>;
   static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
-  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers>;
+  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers, kNhd>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -32,13 +32,17 @@ int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int launch_decode_fp8(int rows_tile, int grid, const DecodeParams& p, cudaStream_t stream) {
+int launch_decode_fp8(int rows_tile, bool nhd, int grid, const DecodeParams& p, cudaStream_t stream) {
   if (p.page_shift < 0) return FI_ERR_UNSUPPORTED;
-  switch (rows_tile) {
-    case 1: return launch_fp8_rows<1>(grid, p, stream);
-    case 2: return launch_fp8_rows<2>(grid, p, stream);
-    case 4: return launch_fp8_rows<4>(grid, p, stream);
-    case 8: return launch_fp8_rows<8>(grid, p, stream);
+  switch (rows_tile * 2 + (nhd ? 1 : 0)) {
+    case 2: return launch_fp8_rows<1, false>(grid, p, stream);
+    case 3: return launch_fp8_rows<1, true>(grid, p, stream);
+    case 4: return launch_fp8_rows<2, false>(grid, p, stream);
+    case 5: return launch_fp8_rows<2, true>(grid, p, stream);
+    case 8: return launch_fp8_rows<4, false>(grid, p, stream);
+    case 9: return launch_fp8_rows<4, true>(grid, p, stream);
+    case 16: return launch_fp8_rows<8, false>(grid, p, stream);
+    case 17: return launch_fp8_rows<8, true>(grid, p, stream);
     default: return FI_ERR_UNSUPPORTED;
   }
 }

@@ -60,15 +60,18 @@ __device__ __forceinline__ uint32_t f2_to_f16x2(float lo, float hi) {
 }
 
 // Copier warp `cw` of kCopiers: stages cw, cw + kCopiers, ...; a warp instruction moves four
-// 128-byte rows (lane = token (lane / 8) of the four, 16-byte chunk lane % 8).  Page ids of the
+// 128-byte rows (lane = token (lane / 8) of the four, 16-byte chunk lane % 8).  HND pages hold a
+// head's rows 128 bytes apart; NHD pages (kNhd) H_kv * 128 bytes apart, i.e. the page stride over
+// the page size, a power of two (H_kv is one for NHD decode).  Page ids of the
 // stage's segments: lane l holds those of segments l and l + 32 (64 segments only with 1-token
 // pages; stages start on a page boundary, so segment = token >> page_shift).
-template <int R, int NW, int S, int kCopiers>
+template <int R, int NW, int S, int kCopiers, bool kNhd>
 __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm, int begin,
                                                   int end, int cw) {
   const int lane = threadIdx.x & 31;
   const int sh = p.page_shift;
   const int row_mask = p.page_size - 1;
+  const int nhd_row_shift = kNhd ? __ffsll(p.page_stride >> sh) - 1 : 0;  // log2(H_kv * 128)
   StageCursorT<kFp8StageTokens> c{begin, end, 0, 0, 0, 0, 0, 0};
   bool ok = c.load(p.items);
   for (int k = 0; k < cw && ok; ++k) ok = c.next(p.items);
@@ -107,7 +110,12 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
         page = seg >= 32 ? hi : page;
       }
       if (tok < nt && page >= 0) {
-        const long long off = (long long)page * p.page_stride + (long long)(pos & row_mask) * kHeadDim + (lane & 7) * 16;
+        long long off;
+        if constexpr (kNhd) {
+          off = (long long)page * p.page_stride + ((long long)(pos & row_mask) << nhd_row_shift) + (lane & 7) * 16;
+        } else {
+          off = (long long)page * p.page_stride + (long long)(pos & row_mask) * kHeadDim + (lane & 7) * 16;
+        }
         const int sw = ((lane & 7) ^ (tok & 7)) * 16;
         cp_async_16(&sm.kv8[slot][0][tok][sw], kb + off);
         cp_async_16(&sm.kv8[slot][1][tok][sw], vb + off);
@@ -330,7 +338,7 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
   }
 }
 
-template <int R, int NW, int S, int kCopiers>
+template <int R, int NW, int S, int kCopiers, bool kNhd>
 __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
     decode_kernel_fp8(const __grid_constant__ DecodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   } else if (warp == 0) {
     decode_index_warp<R, NW, S, DecodeSmemFp8<R, NW, S>, kFp8StageTokens>(p, sm, begin, end);
   } else {
-    decode_copier_fp8<R, NW, S, kCopiers>(p, sm, begin, end, warp - 1);
+    decode_copier_fp8<R, NW, S, kCopiers, kNhd>(p, sm, begin, end, warp - 1);
   }
 }
 

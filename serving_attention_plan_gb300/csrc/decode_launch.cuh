@@ -52,6 +52,6 @@ int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream) {
 int launch_decode_nhd(int rows_tile, int log2_heads, int grid, const DecodeParams& p, cudaStream_t stream);
 
 // FP8 (e4m3) KV pages, HND layout, 16-byte-copy loader (power-of-two pages).  Returns an fi_status.
-int launch_decode_fp8(int rows_tile, int grid, const DecodeParams& p, cudaStream_t stream);
+int launch_decode_fp8(int rows_tile, bool nhd, int grid, const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace fi

@@ -232,10 +232,9 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   if (st != FI_OK) return st;
   // NHD decode reads page rows with the 16-byte-copy loader (power-of-two pages); its kernels are
   // instantiated for 1, 2, 4, 8 and 16 KV heads
-  // e4m3 pages: decode tiles, HND layout, power-of-two pages (the FP8 kernel's loader)
+  // e4m3 pages: decode tiles, power-of-two pages (the FP8 kernel's loader)
   if (ws->variant.kv_dtype == FI_KV_DTYPE_E4M3 &&
-      (plan.header[fi::H_PATH] != fi::kPathDecode || ws->variant.kv_layout != FI_KV_LAYOUT_HND ||
-       (page_size & (page_size - 1)) != 0))
+      (plan.header[fi::H_PATH] != fi::kPathDecode || (page_size & (page_size - 1)) != 0))
     return FI_ERR_UNSUPPORTED;
   if (ws->variant.kv_layout == FI_KV_LAYOUT_NHD && plan.header[fi::H_PATH] == fi::kPathDecode &&
       ((page_size & (page_size - 1)) != 0 || (num_kv_heads & (num_kv_heads - 1)) != 0 || num_kv_heads > 16))
@@ -338,7 +337,7 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     if (var.kv_dtype == FI_KV_DTYPE_E4M3) {  // every field above is set before this launch
       p.scale_log2 *= var.k_scale;           // logits of the stored codes, scaled back to K
       p.v_scale = var.v_scale;
-      return fi::launch_decode_fp8(h[fi::H_ROWS_TILE], h[fi::H_NUM_CTAS], p, s);
+      return fi::launch_decode_fp8(h[fi::H_ROWS_TILE], nhd, h[fi::H_NUM_CTAS], p, s);
     }
     const bool variant = var_on(var);
     if (nhd)
