@@ -442,3 +442,18 @@ def test_fp8_attention_equals_dequantized_bf16_free_attention():
     o2, l2 = A.batch_attention(bf)
     np.testing.assert_allclose(o, o2, atol=TOL)
     np.testing.assert_allclose(l, l2, atol=TOL)
+
+
+def test_fp8_pages_layout_invariant():
+    """e4m3 pages stored HND [pages, H_kv, page_size, D] or NHD [pages, page_size, H_kv, D] hold the
+    same codes at the same (page, head, row): attention over them is identical, bit for bit."""
+    b = W.random_small_batch(731, batch=4, num_qo_heads=6, num_kv_heads=3, page_size=4, causal=True,
+                             q_len_range=(1, 3), kv_len_range=(1, 23), head_dim=8)
+    b8 = W.as_e4m3(b, 0.5, 2.0)
+    nhd = W.PagedBatch(b8.name, b8.num_qo_heads, b8.num_kv_heads, b8.head_dim, b8.page_size, b8.causal,
+                       b8.qo_indptr, b8.kv_indptr, b8.kv_indices, b8.last_page_len, b8.q,
+                       np.ascontiguousarray(b8.k_pages.transpose(0, 2, 1, 3)),
+                       np.ascontiguousarray(b8.v_pages.transpose(0, 2, 1, 3)))
+    o1, l1 = A.batch_attention(b8, k_scale=0.5, v_scale=2.0)
+    o2, l2 = A.batch_attention(nhd, layout="NHD", k_scale=0.5, v_scale=2.0)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
