@@ -457,3 +457,52 @@ def test_fp8_pages_layout_invariant():
     o1, l1 = A.batch_attention(b8, k_scale=0.5, v_scale=2.0)
     o2, l2 = A.batch_attention(nhd, layout="NHD", k_scale=0.5, v_scale=2.0)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---- bfloat16 decoding and rounding (术语与记号 fixes bf16 inputs with fp32 accumulation) ----------
+
+def test_bf16_decoder_pins_all_bit_patterns():
+    """bf16_to_f64 against torch's own bfloat16 -> float64 cast on all 65536 bit patterns (NaNs by
+    class, everything else bit for bit), plus values the format fixes by definition: bf16 keeps the
+    sign, the 8 exponent bits (bias 127) and the top 7 mantissa bits of an IEEE float32."""
+    torch = pytest.importorskip("torch")
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):  # signalling NaN patterns widen to quiet NaNs
+        ours = A.bf16_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert nan.sum() == 2 * 127  # exponent all ones, mantissa non-zero, either sign
+    assert np.array_equal(ours[~nan].view(np.uint64), ref[~nan].view(np.uint64))  # bit for bit, -0 included
+    # values fixed by the format, independent of any library
+    assert ours[0x3F80] == 1.0 and ours[0xBF80] == -1.0 and ours[0x4000] == 2.0 and ours[0x3F00] == 0.5
+    assert ours[0x3FC0] == 1.5 and ours[0x3F81] == 1.0 + 2.0 ** -7           # last mantissa bit = 2^-7
+    assert ours[0x0080] == 2.0 ** -126 and ours[0x0001] == 2.0 ** -133      # smallest normal, subnormal
+    assert ours[0x7F7F] == (2.0 - 2.0 ** -7) * 2.0 ** 127                   # largest finite
+    assert ours[0x7F80] == np.inf and ours[0xFF80] == -np.inf
+    assert ours[0x0000] == 0.0 and np.signbit(ours[0x8000]) and ours[0x8000] == 0.0
+    # a byte-order or shift mistake would swap these two
+    assert ours[0x4049] == 3.140625 and ours[0x4940] != 3.140625
+
+
+def test_bf16_rounding_of_the_input_generator():
+    """The generator's float32 -> bf16 rounding (nearest, ties to even) equals torch's cast on a large
+    random sample, on exact ties, on subnormals and at the overflow edge."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(77)
+    x = np.concatenate([
+        rng.standard_normal(200_000, dtype=np.float32),
+        (rng.standard_normal(50_000, dtype=np.float32) * np.float32(1e-39)),    # float32 subnormals
+        rng.uniform(-3e38, 3e38, 50_000).astype(np.float32),                      # rounds to inf near the top
+    ])
+    hi = rng.integers(0, 1 << 16, 20_000, dtype=np.uint32)
+    hi = hi[((hi >> 7) & 0xFF) != 0xFF]                                           # finite upper halves only
+    ties = ((hi << 16) | np.uint32(0x8000)).view(np.float32)                      # exactly half way
+    near = ((hi << 16) | np.uint32(0x7FFF)).view(np.float32)                      # just below half way
+    x = np.concatenate([x, ties, near, np.float32([0.0, -0.0, 1.0, 3.4028235e38, -3.4028235e38])])
+    ours = W.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    # ties go to the even upper half: 1 + 2^-8 (half an ulp above 1) rounds down to 1, 1 + 3*2^-8 up
+    assert W.f32_to_bf16_bits(np.float32([1.0 + 2.0 ** -8]))[0] == 0x3F80
+    assert W.f32_to_bf16_bits(np.float32([1.0 + 3 * 2.0 ** -8]))[0] == 0x3F82
