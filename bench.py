@@ -515,10 +515,38 @@ def main():
         "configs": extra,
         "cpu_baseline": cpu,
     }
+    # last key, compact: every workload's headline number and its fraction of the measured roofline
+    line["targets"] = targets_summary(args.config, value / world, ms, hbm_peak, bf16_peak, peak_src, extra)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def targets_summary(name, gbs, ms, hbm_peak, bf16_peak, peak_src, extra):
+    """One short entry per workload (µs per batch, rate, fraction of the measured peak, the goal)."""
+    r3 = lambda x: None if x is None else round(float(x), 3)
+    out = {name: {"us": r3(ms * 1e3), "GB/s": r3(gbs), "frac_hbm": r3(gbs / hbm_peak), "goal": ">=0.75 hbm"}}
+    goals = {"skewed_long_decode": ">=0.75 hbm", "ragged_causal_prefill": ">=0.50 bf16",
+             "shared_prefix_decode": "reported", "variant_llama3_8b_decode_fp8_e4m3": "reported",
+             "tiny_decode": "latency"}
+    for k, goal in goals.items():
+        e = extra.get(k)
+        if not e or "error" in e:
+            out[k] = {"error": (e or {}).get("error", "not run")}
+            continue
+        t = {"us": r3(e["us_per_batch"])}
+        if "tflops" in e:
+            t.update({"TFLOP/s": r3(e["tflops"]), "frac_bf16": r3(e["frac_of_bf16_peak"])})
+        elif "kv_gbs_unique" in e:
+            t.update({"GB/s_unique_kv": r3(e["kv_gbs_unique"]), "frac_hbm": r3(e["frac_of_hbm_peak"]),
+                      "launches": e.get("launches_per_step")})
+        elif "kv_gbs" in e:
+            t.update({"GB/s": r3(e["kv_gbs"]), "frac_hbm": r3(e["frac_of_hbm_peak"])})
+        t["goal"] = goal
+        out[k] = t
+    out["peaks"] = {"hbm_gbs": hbm_peak, "bf16_tflops": bf16_peak, "source": peak_src}
+    return out
 
 
 # Attention variants (sliding window, logit soft-cap, NHD pages) on two of the workloads

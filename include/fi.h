@@ -301,20 +301,33 @@ int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const in
  *   q, k_pages, v_pages, o, lse   DEVICE, as for fi_run
  *   stream         the plan copy, the counter reset and the kernel run on it
  *
+ * The plan is the one fi_plan makes for the same lengths with the default cost
+ * model and every SM of the device (the same planner code, run over static
+ * storage), so it is bit-identical to fi_plan's and accepts the same inputs.
  * All calls share the array: calls that overlap on the GPU (different streams
  * without ordering) race; host calls are serialised.  The array keeps the last
- * call's contents, so each call clears its split counters and error word.
+ * call's contents, so each call clears its split counters.  Its first 256 bytes
+ * hold a device-side error word (FI_DEVERR_* bits) that calls only add to: read
+ * and clear it with fi_decode_noalloc_get_error.
  * The first call on a device looks up the array's device address and sets the
  * kernel attribute (with that device current); make it before any stream
  * capture.  Errors: INVALID_ARG, CAPACITY (plan + page indices + slots do not
  * fit in the array), UNSUPPORTED (the batch needs tensor-core tiles, i.e. some
- * request has more than 8 rows = query tokens x group size), CUDA.
+ * request has more than 8 rows = query tokens x group size, or a KV length
+ * above 2^30), CUDA.
  */
 #define FI_NOALLOC_SCRATCH_BYTES (4u << 20)
 int fi_decode_noalloc(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
                       const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
                       int page_size, int causal, const void* q, const void* k_pages, const void* v_pages,
                       int num_pages, void* o, float* lse, void* stream);
+
+/*
+ * fi_decode_noalloc_get_error -- read and clear the error word of fi_decode_noalloc's array on the
+ * current device (FI_DEVERR_* bits set by every call since the last read; 0 if none).
+ * Synchronises the device.  Allocates nothing.  Errors: INVALID_ARG, CUDA.
+ */
+int fi_decode_noalloc_get_error(int32_t* err_bits);
 
 /* Number of SMs of the current device (the default SM budget). Errors: CUDA. */
 int fi_device_sm_count(int* out);

@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
                                   c_int32, c_int32, P32, c_int64, POINTER(c_int64)]
     L.fi_decode_noalloc.argtypes = [P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                                     c_void_p, c_int, c_void_p, c_void_p, c_void_p]
+    L.fi_decode_noalloc_get_error.argtypes = [P32]
     L.fi_device_sm_count.argtypes = [POINTER(c_int)]
     L.fi_status_string.argtypes = [c_int]
     L.fi_status_string.restype = ctypes.c_char_p
@@ -68,7 +69,7 @@ def lib() -> ctypes.CDLL:
     for name in ("fi_workspace_create", "fi_workspace_destroy", "fi_workspace_set_cost_model",
                  "fi_workspace_set_variant", "fi_workspace_set_kv_dtype", "fi_plan", "fi_run",
                  "fi_run_merge", "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count",
-                 "fi_decode_noalloc"):
+                 "fi_decode_noalloc", "fi_decode_noalloc_get_error"):
         getattr(L, name).restype = c_int
     _LIB = L
     return L
@@ -202,6 +203,13 @@ def decode_noalloc(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads
                                    num_kv_heads, head_dim, page_size, int(causal), _dptr(q), _dptr(k_pages),
                                    _dptr(v_pages), int(k_pages.shape[0]), _dptr(o), _dptr(lse), _stream_ptr(stream)),
            "fi_decode_noalloc")
+
+
+def decode_noalloc_get_error() -> int:
+    """Read and clear the device-side error bits of the allocation-free entry point (synchronises)."""
+    e = np.zeros(1, np.int32)
+    _check(lib().fi_decode_noalloc_get_error(_p32(e)), "fi_decode_noalloc_get_error")
+    return int(e[0])
 
 
 def merge_states(o_a, lse_a, o_b, lse_b, o, lse, stream=None):

@@ -31,10 +31,9 @@
 #include "plan.h"
 
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <functional>
-#include <numeric>
-#include <queue>
 #include <utility>
 
 #include "../../include/fi.h"
@@ -44,6 +43,55 @@ namespace fi {
 namespace {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// a1: query and KV length of request i
+inline int64_t len_q(const PlanInput& in, int i) { return int64_t(in.qo_indptr[i + 1]) - in.qo_indptr[i]; }
+inline int64_t len_kv(const PlanInput& in, int i) {
+  const int64_t n_pages = int64_t(in.kv_indptr[i + 1]) - in.kv_indptr[i];
+  return n_pages > 0 ? (n_pages - 1) * in.page_size + in.last_page_len[i] : 0;
+}
+
+// keys [lo, e) that tile rows q0 .. q0+qn-1 of request i can see
+void extent(const PlanInput& in, int i, int64_t q0, int64_t qn, int64_t* lo, int64_t* e) {
+  const int64_t lq = len_q(in, i), lkv = len_kv(in, i);
+  *lo = 0;
+  if (!in.causal) {
+    *e = lkv;
+    return;
+  }
+  *e = std::min(std::max<int64_t>(lkv - lq + q0 + qn, 0), lkv);
+  if (in.window_left >= 0) {
+    *lo = std::max<int64_t>(0, lkv - lq + q0 - in.window_left) / in.page_size * in.page_size;
+    *lo = std::min(*lo, *e);
+  }
+}
+
+// a4: every unit (request, KV head, query tile) in enumeration order, cut into n chunks of cs keys
+// from lo_e (n = 1, cs = 0 when it sees no key); visit(i, h, q0, qn, lo_e, e, cs, n, diag).
+template <class Visit>
+void for_each_unit(const PlanInput& in, const PlanShape& s, Visit&& visit) {
+  const int ps = in.page_size;
+  for (int i = 0; i < in.batch; ++i) {
+    const int64_t lq = len_q(in, i), lkv = len_kv(in, i);
+    const int64_t n_tiles = ceil_div(lq, s.tile_tokens);
+    for (int h = 0; h < in.num_kv_heads; ++h) {
+      for (int64_t j = 0; j < n_tiles; ++j) {
+        const int64_t q0 = j * s.tile_tokens;
+        const int64_t qn = std::min<int64_t>(s.tile_tokens, lq - q0);
+        int64_t lo_e, e;
+        extent(in, i, q0, qn, &lo_e, &e);
+        const int64_t diag = in.causal ? lkv - lq + q0 : kNotCausalDiag;
+        int64_t n = 1, cs = 0;
+        if (e - lo_e > 0) {
+          n = ceil_div(e - lo_e, s.l_chunk);
+          cs = ceil_div(ceil_div(e - lo_e, n), ps) * ps;
+          n = ceil_div(e - lo_e, cs);
+        }
+        visit(i, h, q0, qn, lo_e, e, cs, n, diag);
+      }
+    }
+  }
+}
 
 }  // namespace
 
@@ -68,7 +116,7 @@ int validate_input(const PlanInput& in) {
   return FI_OK;
 }
 
-int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
+int plan_shape(const PlanInput& in, const CostModel& cm, PlanShape* s) {
   int st = validate_input(in);
   if (st != FI_OK) return st;
   if (cm.alpha < 0 || cm.beta < 1 || cm.l_min < 1) return FI_ERR_INVALID_ARG;
@@ -76,168 +124,173 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
   const int g = in.num_qo_heads / in.num_kv_heads;
   const int ps = in.page_size;
 
-  // a1: lengths
-  std::vector<int64_t> lq(B), lkv(B);
+  // a1: lengths (key positions must stay within int32 item fields)
   int64_t max_lq = 0;
   for (int i = 0; i < B; ++i) {
-    lq[i] = in.qo_indptr[i + 1] - in.qo_indptr[i];
-    const int64_t n_pages = in.kv_indptr[i + 1] - in.kv_indptr[i];
-    lkv[i] = n_pages > 0 ? (n_pages - 1) * ps + in.last_page_len[i] : 0;
-    if (lkv[i] > (int64_t(1) << 30)) return FI_ERR_UNSUPPORTED;
-    max_lq = std::max(max_lq, lq[i]);
+    if (len_kv(in, i) > (int64_t(1) << 30)) return FI_ERR_UNSUPPORTED;
+    max_lq = std::max(max_lq, len_q(in, i));
   }
 
   // a2: path and tile
-  int path, tile_tokens, rows_tile;
   if (max_lq * g <= kDecodeMaxRows) {
-    path = kPathDecode;
-    tile_tokens = static_cast<int>(std::max<int64_t>(1, max_lq));
-    rows_tile = 1;
-    while (rows_tile < tile_tokens * g) rows_tile *= 2;
+    s->path = kPathDecode;
+    s->tile_tokens = static_cast<int>(std::max<int64_t>(1, max_lq));
+    s->rows_tile = 1;
+    while (s->rows_tile < s->tile_tokens * g) s->rows_tile *= 2;
   } else {
     if (g > kTcRows) return FI_ERR_UNSUPPORTED;
     // tensor-core tiles read whole 128-key tiles page by page through TMA boxes
     if (ps % 8 != 0 || kTcRows % ps != 0) return FI_ERR_UNSUPPORTED;
-    path = kPathTensor;
-    tile_tokens = kTcRows / g;
-    rows_tile = kTcRows;
+    s->path = kPathTensor;
+    s->tile_tokens = kTcRows / g;
+    s->rows_tile = kTcRows;
   }
-  const int num_ctas = (path == kPathTensor ? kTcCtasPerSm : kDecodeCtasPerSm) * in.num_sms;
-
-  // keys [lo, e) that tile rows q0 .. q0+qn-1 of request i can see
-  auto extent = [&](int i, int64_t q0, int64_t qn, int64_t* lo, int64_t* e) {
-    if (!in.causal) {
-      *lo = 0;
-      *e = lkv[i];
-      return;
-    }
-    *e = std::min(std::max<int64_t>(lkv[i] - lq[i] + q0 + qn, 0), lkv[i]);
-    *lo = 0;
-    if (in.window_left >= 0) {
-      *lo = std::max<int64_t>(0, lkv[i] - lq[i] + q0 - in.window_left) / ps * ps;
-      *lo = std::min(*lo, *e);
-    }
-  };
+  s->group = g;
+  s->num_ctas = (s->path == kPathTensor ? kTcCtasPerSm : kDecodeCtasPerSm) * in.num_sms;
 
   // a3: KV chunk bound (with a window: the keys each tile reads, which is all a window touches)
   int64_t total = 0;
   for (int i = 0; i < B; ++i) {
+    const int64_t lq = len_q(in, i);
     if (in.window_left < 0) {
-      total += int64_t(in.num_kv_heads) * ceil_div(lq[i], tile_tokens) * lkv[i];
+      total += int64_t(in.num_kv_heads) * ceil_div(lq, s->tile_tokens) * len_kv(in, i);
     } else {
-      for (int64_t j = 0; j < ceil_div(lq[i], tile_tokens); ++j) {
+      for (int64_t j = 0; j < ceil_div(lq, s->tile_tokens); ++j) {
         int64_t lo, e;
-        extent(i, j * tile_tokens, std::min<int64_t>(tile_tokens, lq[i] - j * tile_tokens), &lo, &e);
+        extent(in, i, j * s->tile_tokens, std::min<int64_t>(s->tile_tokens, lq - j * s->tile_tokens), &lo, &e);
         total += int64_t(in.num_kv_heads) * (e - lo);
       }
     }
   }
-  int64_t l_chunk = std::max<int64_t>(ceil_div(total, num_ctas), cm.l_min);
+  int64_t l_chunk = std::max<int64_t>(ceil_div(total, s->num_ctas), cm.l_min);
   l_chunk = ceil_div(l_chunk, ps) * ps;
   if (l_chunk > (int64_t(1) << 30)) return FI_ERR_UNSUPPORTED;
+  s->l_chunk = l_chunk;
 
-  // a4: units -> chunks; a6: slots of split units (enumeration order)
-  struct Work {
-    int32_t f[kItemFields];
-    int64_t cost;
-  };
-  std::vector<Work> work;
-  std::vector<int32_t> units, slot_unit;
-  for (int i = 0; i < B; ++i) {
-    const int64_t n_tiles = ceil_div(lq[i], tile_tokens);
-    for (int h = 0; h < in.num_kv_heads; ++h) {
-      for (int64_t j = 0; j < n_tiles; ++j) {
-        const int64_t q0 = j * tile_tokens;
-        const int64_t qn = std::min<int64_t>(tile_tokens, lq[i] - q0);
-        int64_t lo_e, e;
-        extent(i, q0, qn, &lo_e, &e);
-        const int64_t diag = in.causal ? lkv[i] - lq[i] + q0 : kNotCausalDiag;
-        int64_t n, cs;
-        if (e - lo_e == 0) {
-          n = 1;
-          cs = 0;
-        } else {
-          n = ceil_div(e - lo_e, l_chunk);
-          cs = ceil_div(ceil_div(e - lo_e, n), ps) * ps;
-          n = ceil_div(e - lo_e, cs);
-        }
-        int32_t first_slot = -1;
-        if (n > 1) {
-          const int32_t unit = static_cast<int32_t>(units.size() / kUnitFields);
-          first_slot = static_cast<int32_t>(slot_unit.size());
-          const int32_t u[kUnitFields] = {first_slot, static_cast<int32_t>(n), in.qo_indptr[i] + static_cast<int32_t>(q0),
-                                          static_cast<int32_t>(qn), h, 0, 0, 0};
-          units.insert(units.end(), u, u + kUnitFields);
-          slot_unit.insert(slot_unit.end(), static_cast<size_t>(n), unit);
-        }
-        for (int64_t c = 0; c < n; ++c) {
-          const int64_t lo = lo_e + c * cs, hi = std::min(e, lo_e + (c + 1) * cs);
-          Work w;
-          w.f[I_PAGE_BASE] = in.kv_indptr[i];
-          w.f[I_Q_START] = in.qo_indptr[i] + static_cast<int32_t>(q0);
-          w.f[I_Q_LEN] = static_cast<int32_t>(qn);
-          w.f[I_KV_HEAD] = h;
-          w.f[I_KV_LO] = static_cast<int32_t>(lo);
-          w.f[I_KV_HI] = static_cast<int32_t>(hi);
-          w.f[I_DIAG] = static_cast<int32_t>(diag);
-          w.f[I_SLOT] = first_slot >= 0 ? first_slot + static_cast<int32_t>(c) : -1;
-          w.cost = cm.alpha * qn * g + cm.beta * (hi - lo);
-          work.push_back(w);
-        }
-      }
+  // exact sizes of the plan (a4, a6)
+  int64_t W = 0, U = 0, S = 0;
+  for_each_unit(in, *s, [&](int, int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t n, int64_t) {
+    W += n;
+    if (n > 1) {
+      U += 1;
+      S += n;
     }
+  });
+  if (W > INT32_MAX / kItemFields) return FI_ERR_UNSUPPORTED;
+  s->n_items = W;
+  s->n_units = U;
+  s->n_slots = S;
+  return FI_OK;
+}
+
+void plan_fill(const PlanInput& in, const CostModel& cm, const PlanShape& s, const PlanStorage& st,
+               int32_t* header) {
+  const int g = s.group;
+  // a4: units -> chunks; a6: slots of split units (enumeration order)
+  int64_t W = 0, U = 0, S = 0;
+  for_each_unit(in, s, [&](int i, int h, int64_t q0, int64_t qn, int64_t lo_e, int64_t e, int64_t cs, int64_t n,
+                           int64_t diag) {
+    int32_t first_slot = -1;
+    if (n > 1) {
+      first_slot = static_cast<int32_t>(S);
+      int32_t* u = st.units + U * kUnitFields;
+      u[U_FIRST_SLOT] = first_slot;
+      u[U_N_CHUNKS] = static_cast<int32_t>(n);
+      u[U_Q_START] = in.qo_indptr[i] + static_cast<int32_t>(q0);
+      u[U_Q_LEN] = static_cast<int32_t>(qn);
+      u[U_KV_HEAD] = h;
+      u[5] = u[6] = u[7] = 0;
+      for (int64_t c = 0; c < n; ++c) st.slot_unit[S + c] = static_cast<int32_t>(U);
+      U += 1;
+      S += n;
+    }
+    for (int64_t c = 0; c < n; ++c) {
+      const int64_t lo = lo_e + c * cs, hi = std::min(e, lo_e + (c + 1) * cs);
+      int32_t* w = st.work + W * kItemFields;
+      w[I_PAGE_BASE] = in.kv_indptr[i];
+      w[I_Q_START] = in.qo_indptr[i] + static_cast<int32_t>(q0);
+      w[I_Q_LEN] = static_cast<int32_t>(qn);
+      w[I_KV_HEAD] = h;
+      w[I_KV_LO] = static_cast<int32_t>(lo);
+      w[I_KV_HI] = static_cast<int32_t>(hi);
+      w[I_DIAG] = static_cast<int32_t>(diag);
+      w[I_SLOT] = first_slot >= 0 ? first_slot + static_cast<int32_t>(c) : -1;
+      st.cost[W] = cm.alpha * qn * g + cm.beta * (hi - lo);
+      st.order[W] = static_cast<int32_t>(W);
+      W += 1;
+    }
+  });
+
+  // a5: longest first (ties: enumeration order), then a min-queue of (load, CTA id)
+  const int64_t* cost = st.cost;
+  std::sort(st.order, st.order + W,
+            [cost](int32_t a, int32_t b) { return cost[a] > cost[b] || (cost[a] == cost[b] && a < b); });
+  const int C = s.num_ctas;
+  std::greater<std::pair<int64_t, int32_t>> later;
+  for (int c = 0; c < C; ++c) {
+    st.heap[c] = {0, c};
+    st.count[c] = 0;
+    if (st.loads) st.loads[c] = 0;
+  }
+  std::make_heap(st.heap, st.heap + C, later);
+  for (int64_t k = 0; k < W; ++k) {
+    const int32_t it = st.order[k];
+    std::pop_heap(st.heap, st.heap + C, later);
+    std::pair<int64_t, int32_t>& top = st.heap[C - 1];
+    st.cta_of[it] = top.second;
+    st.count[top.second] += 1;
+    top.first += cost[it];
+    if (st.loads) st.loads[top.second] = top.first;
+    std::push_heap(st.heap, st.heap + C, later);
   }
 
-  // a5: longest first (ties: enumeration order), then a min-queue of (load, cta id)
-  const size_t W = work.size();
-  std::vector<int32_t> order(W);
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return work[a].cost > work[b].cost; });
-  using Entry = std::pair<int64_t, int32_t>;
-  std::priority_queue<Entry, std::vector<Entry>, std::greater<Entry>> queue;
-  for (int32_t c = 0; c < num_ctas; ++c) queue.push({0, c});
-  std::vector<int32_t> cta_of(W);
-  std::vector<int32_t> count(num_ctas, 0);
-  std::vector<int64_t> loads(num_ctas, 0);
-  for (int32_t k : order) {
-    Entry top = queue.top();
-    queue.pop();
-    cta_of[k] = top.second;
-    count[top.second] += 1;
-    top.first += work[k].cost;
-    loads[top.second] = top.first;
-    queue.push(top);
+  // queues in CSR form: each CTA's items in the order they were assigned
+  st.cta_indptr[0] = 0;
+  for (int c = 0; c < C; ++c) st.cta_indptr[c + 1] = st.cta_indptr[c] + st.count[c];
+  for (int c = 0; c < C; ++c) st.count[c] = st.cta_indptr[c];  // fill cursors
+  for (int64_t k = 0; k < W; ++k) {
+    const int32_t it = st.order[k];
+    const int32_t pos = st.count[st.cta_of[it]]++;
+    std::memcpy(st.items + size_t(pos) * kItemFields, st.work + size_t(it) * kItemFields,
+                sizeof(int32_t) * kItemFields);
   }
 
-  out->cta_indptr.assign(num_ctas + 1, 0);
-  for (int c = 0; c < num_ctas; ++c) out->cta_indptr[c + 1] = out->cta_indptr[c] + count[c];
+  int32_t* hd = header;
+  hd[H_MAGIC] = kPlanMagic;
+  hd[H_PATH] = s.path;
+  hd[H_TILE_TOKENS] = s.tile_tokens;
+  hd[H_ROWS_TILE] = s.rows_tile;
+  hd[H_GROUP] = g;
+  hd[H_NUM_CTAS] = C;
+  hd[H_NUM_ITEMS] = static_cast<int32_t>(W);
+  hd[H_NUM_UNITS] = static_cast<int32_t>(U);
+  hd[H_NUM_SLOTS] = static_cast<int32_t>(S);
+  hd[H_LKV] = static_cast<int32_t>(s.l_chunk);
+  hd[H_PAGE_SIZE] = in.page_size;
+  hd[H_CAUSAL] = in.causal;
+  hd[H_HQO] = in.num_qo_heads;
+  hd[H_HKV] = in.num_kv_heads;
+  hd[H_HEAD_DIM] = in.head_dim;
+  hd[H_BATCH] = in.batch;
+}
+
+int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
+  PlanShape s;
+  const int st = plan_shape(in, cm, &s);
+  if (st != FI_OK) return st;
+  const size_t W = size_t(s.n_items), C = size_t(s.num_ctas);
+  out->cta_indptr.assign(C + 1, 0);
   out->items.assign(W * kItemFields, 0);
-  std::vector<int32_t> fill(out->cta_indptr.begin(), out->cta_indptr.end() - 1);
-  for (int32_t k : order) {
-    const int32_t pos = fill[cta_of[k]]++;
-    std::memcpy(&out->items[size_t(pos) * kItemFields], work[k].f, sizeof(work[k].f));
-  }
-  out->units = std::move(units);
-  out->slot_unit = std::move(slot_unit);
-  out->loads = std::move(loads);
-
-  int32_t* h = out->header;
-  h[H_MAGIC] = kPlanMagic;
-  h[H_PATH] = path;
-  h[H_TILE_TOKENS] = tile_tokens;
-  h[H_ROWS_TILE] = rows_tile;
-  h[H_GROUP] = g;
-  h[H_NUM_CTAS] = num_ctas;
-  h[H_NUM_ITEMS] = static_cast<int32_t>(W);
-  h[H_NUM_UNITS] = static_cast<int32_t>(out->units.size() / kUnitFields);
-  h[H_NUM_SLOTS] = static_cast<int32_t>(out->slot_unit.size());
-  h[H_LKV] = static_cast<int32_t>(l_chunk);
-  h[H_PAGE_SIZE] = ps;
-  h[H_CAUSAL] = in.causal;
-  h[H_HQO] = in.num_qo_heads;
-  h[H_HKV] = in.num_kv_heads;
-  h[H_HEAD_DIM] = in.head_dim;
-  h[H_BATCH] = B;
+  out->units.assign(size_t(s.n_units) * kUnitFields, 0);
+  out->slot_unit.assign(size_t(s.n_slots), 0);
+  out->loads.assign(C, 0);
+  std::vector<int32_t> work(W * kItemFields), order(W), cta_of(W), count(C);
+  std::vector<int64_t> cost(W);
+  std::vector<std::pair<int64_t, int32_t>> heap(C);
+  PlanStorage ps{out->cta_indptr.data(), out->items.data(), out->units.data(), out->slot_unit.data(),
+                 out->loads.data(), work.data(), cost.data(), order.data(), cta_of.data(), count.data(),
+                 heap.data()};
+  plan_fill(in, cm, s, ps, out->header);
   return FI_OK;
 }
 

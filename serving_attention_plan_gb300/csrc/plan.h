@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <vector>
 
 namespace fi {
@@ -77,6 +78,36 @@ struct Plan {
 
 // Returns an fi_status code (0 = ok).
 int build_plan(const PlanInput& in, const CostModel& cost, Plan* out);
+
+// The same planner in two passes over caller-owned storage, for callers that must not allocate:
+// plan_shape fixes the path, tile, #CTA, chunk bound and the exact counts of items, split rows and
+// slots; plan_fill then writes the plan into the given arrays (it allocates nothing).  build_plan is
+// these two passes over vectors, so every caller gets the same plan bit for bit.
+struct PlanShape {
+  int path, tile_tokens, rows_tile, group, num_ctas;
+  int64_t l_chunk;
+  int64_t n_items, n_units, n_slots;
+};
+
+struct PlanStorage {
+  // outputs, in the layout of Plan
+  int32_t* cta_indptr;  // [num_ctas + 1]
+  int32_t* items;       // [n_items * kItemFields], CTA queue order
+  int32_t* units;       // [n_units * kUnitFields]
+  int32_t* slot_unit;   // [n_slots]
+  int64_t* loads;       // [num_ctas] accumulated cost per CTA (may be null)
+  // work arrays of the fill pass
+  int32_t* work;        // [n_items * kItemFields], enumeration order
+  int64_t* cost;        // [n_items]
+  int32_t* order;       // [n_items]
+  int32_t* cta_of;      // [n_items]
+  int32_t* count;       // [num_ctas]
+  std::pair<int64_t, int32_t>* heap;  // [num_ctas] (load, CTA id)
+};
+
+int plan_shape(const PlanInput& in, const CostModel& cost, PlanShape* shape);
+void plan_fill(const PlanInput& in, const CostModel& cost, const PlanShape& shape, const PlanStorage& st,
+               int32_t* header);
 
 // Checks that only depend on the inputs (same rules as build_plan's validation).
 int validate_input(const PlanInput& in);

@@ -194,3 +194,16 @@ def test_cpp_planner_matches_oracle_with_window(lib, seed):
         assert ei.value.status == 3
         return
     _compare(qo, kv, last, hq, hk, ps, True, n_cta, window_left=w)
+
+
+def test_key_positions_beyond_int32_items_rejected(lib):
+    """Item fields are int32: a KV length above 2^30 (page ids may repeat, page sizes are unbounded) is
+    UNSUPPORTED rather than wrapped.  Both the workspace planner and the allocation-free entry point run
+    this same planner code, so both reject it."""
+    ps = 1 << 20
+    qo = np.array([0, 1]); kv = np.array([0, 1025]); last = np.array([ps])  # 1025 pages of 2^20 keys
+    with pytest.raises(B.FiError) as ei:
+        B.plan_compute(qo, kv, last, 8, 2, ps, False, 4)
+    assert ei.value.status == 3
+    kv = np.array([0, 1024]); last = np.array([1])                          # 2^30 - 2^20 + 1 keys: fine
+    assert B.plan_compute(qo, kv, last, 8, 2, ps, False, 4)[0] == 0x46495031
