@@ -18,10 +18,10 @@ the design notes):
     head in group) pairs.  If every request has l_q * g <= 8 rows, the whole
     batch takes the decode path with one tile per (request, KV head)
     covering all its query tokens, and rows_tile is the smallest of 1, 2, 4, 8
-    that fits; otherwise the tensor-core path with 128-row tiles,
-    tile_tokens = 128 // g.
-  * #CTA = k * (SM budget), k fixed per path: 1 for decode tiles, 2 for
-    tensor-core tiles (核心机制 7, paper App. D.3: #CTA = k x #SM).
+    that fits; otherwise the tensor-core path with 256-row tiles,
+    tile_tokens = 256 // g.
+  * #CTA = k * (SM budget), k fixed per path: 1 for both paths (核心机制 7,
+    paper App. D.3: #CTA = k x #SM).
   * KV heads count as separate units in the L_kv sum; L_kv is raised to l_min
     (default 256) and rounded up to a whole number of pages.
   * A unit (request, KV head, query tile) sees e keys: l_kv, or under the causal
@@ -48,10 +48,10 @@ import numpy as np
 
 PATH_DECODE = 0
 PATH_TENSOR = 1
-TC_ROWS = 128
+TC_ROWS = 256
 DECODE_MAX_ROWS = 8
 DECODE_CTAS_PER_SM = 1
-TC_CTAS_PER_SM = 2
+TC_CTAS_PER_SM = 1
 NOT_CAUSAL_DIAG = 1 << 30
 PLAN_MAGIC = 0x46495031
 HEADER_LEN = 16
@@ -87,7 +87,7 @@ class Plan:
 
 
 def choose_path(l_q, group: int):
-    """Tile choice (核心机制 4, paper §3.2.2): decode tiles for <= 8 rows, 128-row tensor-core tiles otherwise."""
+    """Tile choice (核心机制 4, paper §3.2.2): decode tiles for <= 8 rows, 256-row tensor-core tiles otherwise."""
     max_rows = int(max((int(x) for x in l_q), default=0)) * group
     if max_rows <= DECODE_MAX_ROWS:
         tile_tokens = max(1, int(max((int(x) for x in l_q), default=1)))
@@ -96,7 +96,7 @@ def choose_path(l_q, group: int):
             rows *= 2
         return PATH_DECODE, tile_tokens, rows
     if group > TC_ROWS:
-        raise ValueError("group size above 128 rows")
+        raise ValueError("group size above 256 rows")
     return PATH_TENSOR, TC_ROWS // group, TC_ROWS
 
 

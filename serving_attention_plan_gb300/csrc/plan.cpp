@@ -11,7 +11,7 @@
 //     stay below 2 * #CTA tiles.
 //   核心机制 4 (paper §3.2.2): tiles of at most 8 rows take the decode kernel
 //     (the page runs them on CUDA cores, since an MMA needs at least 16 query
-//     rows), larger ones 128-row tensor-core tiles.
+//     rows), larger ones 256-row tensor-core tiles (two 128-row MMA tiles per KV tile).
 //
 // Rules fixed where the page is silent (the same ones the test-side
 // restatement uses, so the two must agree bit for bit):
@@ -23,8 +23,8 @@
 //     number of pages;
 //   * a unit sees e keys (under the causal mask: those of its last token) and is
 //     cut into n = ceil(e / L_kv) chunks of cs = pages(ceil(e / n)) tokens;
-//   * #CTA = k * (SM budget) with k fixed per path (kDecodeCtasPerSm = 1,
-//     kTcCtasPerSm = 2: two tensor-core CTAs share an SM);
+//   * #CTA = k * (SM budget) with k fixed per path (kDecodeCtasPerSm = kTcCtasPerSm = 1: one
+//     persistent CTA per SM on either path);
 //   * item cost = alpha * rows + beta * chunk length;
 //   * sort by cost descending, ties by enumeration order; the queue pops the
 //     least-loaded CTA, ties to the lowest CTA id.
@@ -140,7 +140,7 @@ int plan_shape(const PlanInput& in, const CostModel& cm, PlanShape* s) {
   } else {
     if (g > kTcRows) return FI_ERR_UNSUPPORTED;
     // tensor-core tiles read whole 128-key tiles page by page through TMA boxes
-    if (ps % 8 != 0 || kTcRows % ps != 0) return FI_ERR_UNSUPPORTED;
+    if (ps % 8 != 0 || kTcKeys % ps != 0) return FI_ERR_UNSUPPORTED;
     s->path = kPathTensor;
     s->tile_tokens = kTcRows / g;
     s->rows_tile = kTcRows;

@@ -15,10 +15,11 @@ namespace fi {
 constexpr int kHeadDim = 128;
 constexpr int kPathDecode = 0;
 constexpr int kPathTensor = 1;
-constexpr int kTcRows = 128;          // rows of a tensor-core tile (tcgen05 M)
+constexpr int kTcRows = 256;          // rows of a tensor-core tile: two 128-row tcgen05 tiles sharing each KV tile
+constexpr int kTcKeys = 128;          // keys of a tensor-core KV tile
 constexpr int kDecodeMaxRows = 8;     // largest tile the CUDA-core decode path takes
 constexpr int kDecodeCtasPerSm = 1;   // persistent CTAs per SM of each path (#CTA = k * #SM)
-constexpr int kTcCtasPerSm = 2;
+constexpr int kTcCtasPerSm = 1;
 constexpr int32_t kNotCausalDiag = 1 << 30;
 constexpr int32_t kPlanMagic = 0x46495031;
 constexpr int kHeaderLen = 16;

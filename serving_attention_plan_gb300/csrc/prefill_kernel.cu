@@ -22,21 +22,27 @@
 //     refuses for this grid: it counts one TMEM-allocating CTA per SM, although
 //     two run side by side.)
 //
-// Two CTAs per SM (each holds 256 of the SM's 512 TMEM columns and ~97 KB of
-// shared memory), 8 warps = 2 warpgroups each:
-//   warps 0-3  softmax + epilogue; thread t owns row t = TMEM lane t
-//   warp 4     TMA producer (Q per item, K and V per 128-key tile)
-//   warp 5     TMEM allocation and MMA issue (one thread)
-//   warps 6-7  idle (they complete the second warpgroup, which hands its registers to the first)
-// The two CTAs of an SM run independent item streams, so one CTA's softmax,
-// epilogue and item changes overlap the other's MMAs.
-// TMEM: S = Q K^T in columns [0,128) (fp32), overwritten in place by P (bf16
-// pairs, columns [0,64)) which is the A operand of O += P V; O accumulates in
-// columns [128,256).  P stays in tensor memory, so P.V reads only V from shared
-// memory (an MMA with both operands in shared memory uses its full bandwidth).
-// Online softmax in base 2 with a lazy rescale: O and l are rescaled only when
-// a row's running maximum grows by more than 8 (a factor 256), which keeps
-// exp2 arguments <= 8 and changes the result only by rounding.
+// One CTA per SM (all 512 TMEM columns, ~200 KB of shared memory), 16 warps = 4 warpgroups.
+// A work item is 256 rows (256/g tokens x g heads) as two 128-row MMA tiles, Q0 (rows 0-127)
+// and Q1 (rows 128-255), that share every KV tile: each 128-key K and V tile is fetched once for
+// 256 query rows, which halves the L2 traffic and the TMA box count per flop.
+//   warps 0-3       softmax of Q0: thread t owns row t (TMEM lane t)
+//   warps 4-7       softmax of Q1
+//   warps 8-11      epilogue: O / l and LSE of both halves of a finished item, to the output or
+//                   a partial slot
+//   warp 12         TMA producer of K (two stages) and of each item's Q tile
+//   warp 13         TMA producer of V (two stages)
+//   warp 14         TMEM allocation and issue of S_h = Q_h K^T (one thread)
+//   warp 15         issue of O_h += P_h V (one thread)
+// TMEM: S0, S1 (columns 0-255, fp32) and O0, O1 (256-511).  The softmax of half h overwrites the
+// first 64 columns of S_h with its P (bf16 pairs), the A operand of O_h += P_h V, so P.V reads
+// only V from shared memory.  The MMA order per KV tile is QK0, QK1, PV0, PV1: while one half's
+// softmax runs, the tensor pipe works on the other half.  QK and P.V come from two issuing threads,
+// so neither's waits stall the other; O is handed to the epilogue as soon as the item's last P.V
+// of that half completes.
+// Online softmax in base 2 with a lazy rescale: O and l are rescaled only when a row's running
+// maximum grows by more than 8 (a factor 256), which keeps exp2 arguments <= 8 and changes the
+// result only by rounding.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -53,18 +59,25 @@
 namespace fi {
 namespace {
 
-constexpr int kTile = 128;                  // rows of a Q tile, keys of a KV tile
+constexpr int kTile = 128;                  // rows of an MMA tile (one half of an item), keys of a KV tile
 constexpr int kHalfBytes = kTile * 128;     // one 64-dim half of a 128-row bf16 tile (16 KB)
 constexpr int kTileBytes = 2 * kHalfBytes;  // full 128 x 128 bf16 tile
-constexpr int kThreads = 256;
-// Register split after launch (2 CTAs x 256 threads x 128): the softmax warpgroup takes 184,
-// the producer/MMA warpgroup keeps 72: 128 * 184 + 128 * 72 = 32768 = 256 * 128.
-constexpr uint32_t kSoftmaxRegs = 184;
-constexpr uint32_t kControlRegs = 72;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColO = 128;
+constexpr int kItemRows = 2 * kTile;        // rows of a work item (kTcRows)
+constexpr int kQHalfBytes = kItemRows * 128;  // one 64-dim half of the item's Q (32 KB)
+constexpr int kThreads = 512;
+// Register split after launch (512 threads x 128): the two softmax warpgroups take 176 each (a
+// row of 128 scores in registers), the epilogue warpgroup 104 (it streams O out 32 columns at a
+// time), the producer/MMA warpgroup 56: 128 * (176 + 176 + 104 + 56) = 65536 = 512 * 128.
+constexpr uint32_t kSoftmaxRegs = 176;
+constexpr uint32_t kEpilogueRegs = 104;
+constexpr uint32_t kControlRegs = 56;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;      // S_h at columns 128 h
+constexpr uint32_t kColO = 256;    // O_h at columns 256 + 128 h
+constexpr int kKvStages = 2;       // K and V shared-memory stages each
 constexpr float kRescaleThreshold = 8.0f;
+constexpr unsigned kFull = 0xffffffffu;
+static_assert(kItemRows == kTcRows, "a tensor-core work item is two 128-row MMA tiles");
 
 struct PrefillParams {
   const int32_t* cta_indptr;
@@ -92,10 +105,14 @@ struct PrefillParams {
 };
 
 struct PrefillSmem {
-  uint8_t q[kTileBytes];  // [2 halves][128 rows][128 B], 128B-swizzled
-  uint8_t k[kTileBytes];
-  uint8_t v[kTileBytes];
-  uint64_t q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, p_full, o_done, o_free;
+  uint8_t q[2 * kQHalfBytes];        // item Q: [2 dim halves][256 rows][128 B], 128B-swizzled
+  uint8_t k[kKvStages][kTileBytes];  // [stage][2 dim halves][128 keys][128 B]
+  uint8_t v[kKvStages][kTileBytes];
+  float stat_m[2][kItemRows];        // [item parity][row]: running max at the end of the item
+  float stat_l[2][kItemRows];        // [item parity][row]: row sum
+  uint64_t q_full, q_empty, k_full[kKvStages], k_empty[kKvStages], v_full[kKvStages], v_empty[kKvStages];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];  // per half of the item
+  uint64_t stat_full[2], stat_empty[2];                  // per item parity
   uint32_t tmem_base;
   int abort;
 };
@@ -118,30 +135,26 @@ struct Item {
 };
 
 // ---------------------------------------------------------------------------------------------
-// warp 4: TMA producer
+// warps 12 (K and the item's Q) and 13 (V): TMA producers
 // ---------------------------------------------------------------------------------------------
-template <bool kNhd>
-__device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                         const CUtensorMap* tm_v, int begin, int end) {
+template <bool kNhd, bool kIsK>
+__device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
+                         int begin, int end) {
   const int lane = threadIdx.x & 31;
   const int ps = p.page_size;
   const int ppt = kTile / ps;  // pages per KV tile (<= 16)
   const int oob_page = p.num_pages * p.hkv;
-  int tt = 0, nq = 0;
+  uint8_t* ring = kIsK ? &sm.k[0][0] : &sm.v[0][0];
+  uint64_t* full = kIsK ? sm.k_full : sm.v_full;
+  uint64_t* empty = kIsK ? sm.k_empty : sm.v_empty;
+  int tt = 0, nq = 0;  // KV tiles and Q tiles issued
   bool ok = true;
   for (int pos = begin; pos < end && ok; ++pos) {
     Item it;
     it.load(p.items, pos);
     const int n_tiles = it.tiles();
     if (n_tiles == 0) continue;
-    if (nq > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_empty, (nq - 1) & 1, p.err, &sm.abort));
-    if (!ok) break;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&sm.q_full, p.q_tile_bytes);
-      tc::tma_load_3d(sm.q, tm_q, 0, it.kv_head * p.group, it.q_start, &sm.q_full);
-      tc::tma_load_3d(sm.q + kHalfBytes, tm_q, 64, it.kv_head * p.group, it.q_start, &sm.q_full);
-    }
-    for (int t = 0; t < n_tiles; ++t) {
+    for (int t = 0; t < n_tiles && ok; ++t) {
       const int base = it.kv_lo + t * kTile;
       // out-of-range page(-head) coordinate: the box reads as zeros
       int z = kNhd ? p.num_pages : oob_page;
@@ -156,49 +169,56 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
           }
         }
       }
-      // one page of one KV head: HND box (64 dims, page_size tokens, 1 page-head), NHD box
-      // (64 dims, 1 head, page_size tokens, 1 page)
-      auto load_page = [&](uint8_t* dst, const CUtensorMap* tm, int x, uint64_t* bar) {
-        if constexpr (kNhd)
-          tc::tma_load_4d(dst, tm, x, it.kv_head, 0, z, bar);
-        else
-          tc::tma_load_3d(dst, tm, x, 0, z, bar);
-      };
-      if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_empty, (tt - 1) & 1, p.err, &sm.abort));
+      const int st = tt % kKvStages;
+      if (tt >= kKvStages)
+        ok = __all_sync(kFull, mbar_wait(&empty[st], ((tt / kKvStages) - 1) & 1, p.err, &sm.abort));
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sm.k_full, kTileBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
       __syncwarp();
       if (lane < ppt) {
-        load_page(sm.k + lane * ps * 128, tm_k, 0, &sm.k_full);
-        load_page(sm.k + kHalfBytes + lane * ps * 128, tm_k, 64, &sm.k_full);
-      }
-      if (tt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_empty, (tt - 1) & 1, p.err, &sm.abort));
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&sm.v_full, kTileBytes);
-      __syncwarp();
-      if (lane < ppt) {
-        load_page(sm.v + lane * ps * 128, tm_v, 0, &sm.v_full);
-        load_page(sm.v + kHalfBytes + lane * ps * 128, tm_v, 64, &sm.v_full);
+        // one page of one KV head: HND box (64 dims, page_size tokens, 1 page-head), NHD box
+        // (64 dims, 1 head, page_size tokens, 1 page)
+        uint8_t* dst = ring + st * kTileBytes + lane * ps * 128;
+        if constexpr (kNhd) {
+          tc::tma_load_4d(dst, tm_kv, 0, it.kv_head, 0, z, &full[st]);
+          tc::tma_load_4d(dst + kHalfBytes, tm_kv, 64, it.kv_head, 0, z, &full[st]);
+        } else {
+          tc::tma_load_3d(dst, tm_kv, 0, 0, z, &full[st]);
+          tc::tma_load_3d(dst + kHalfBytes, tm_kv, 64, 0, z, &full[st]);
+        }
       }
       ++tt;
+      if constexpr (kIsK) {
+        // the item's Q, after its first K tile (so that load is not held up behind the wait for
+        // the previous item's last QK to free the Q buffer)
+        if (t == 0) {
+          if (nq >= 1) ok = __all_sync(kFull, mbar_wait(&sm.q_empty, (nq - 1) & 1, p.err, &sm.abort));
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.q_full, p.q_tile_bytes);
+            tc::tma_load_3d(sm.q, tm_q, 0, it.kv_head * p.group, it.q_start, &sm.q_full);
+            tc::tma_load_3d(sm.q + kQHalfBytes, tm_q, 64, it.kv_head * p.group, it.q_start, &sm.q_full);
+          }
+          ++nq;
+        }
+      }
     }
-    ++nq;
   }
   // never leave with tensor copies still landing in this CTA's shared memory
-  if (nq > 0) mbar_wait_bounded(&sm.q_full, (nq - 1) & 1);
-  if (tt > 0) {
-    mbar_wait_bounded(&sm.k_full, (tt - 1) & 1);
-    mbar_wait_bounded(&sm.v_full, (tt - 1) & 1);
+  if constexpr (kIsK) {
+    if (nq > 0) mbar_wait_bounded(&sm.q_full, (nq - 1) & 1);
   }
+  for (int k = max(0, tt - kKvStages); k < tt; ++k) mbar_wait_bounded(&full[k % kKvStages], (k / kKvStages) & 1);
 }
 
 // ---------------------------------------------------------------------------------------------
-// warp 5, one thread: MMA issue
+// MMA issue, two threads: warp 14 issues S_h = Q_h K^T, warp 15 issues O_h += P_h V.  Every
+// dependency between them goes through a barrier (S_h free = the half's last P.V done; P_h ready
+// = the softmax's arrivals), so each thread's waits overlap the other's issue.
 // ---------------------------------------------------------------------------------------------
-__device__ void mma_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
-  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kTile, 0, 0);  // A = Q (K-major), B = K (K-major)
-  constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P (TMEM), B = V (MN-major)
-  const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k), v_addr = smem_u32(sm.v);
+__device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kTile, 0, 0);  // A = Q_h (K-major), B = K (K-major)
+  const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k[0]);
   int tt = 0, nq = 0;
   for (int pos = begin; pos < end; ++pos) {
     Item it;
@@ -206,47 +226,75 @@ __device__ void mma_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tme
     const int n_tiles = it.tiles();
     if (n_tiles == 0) continue;
     if (!mbar_wait(&sm.q_full, nq & 1, p.err, &sm.abort)) return;
-    for (int t = 0; t < n_tiles; ++t) {
-      if (!mbar_wait(&sm.k_full, tt & 1, p.err, &sm.abort)) return;
-      if (tt > 0 && !mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort)) return;  // S/P columns free
-      tc::fence_after_sync();
+    for (int t = 0; t < n_tiles; ++t, ++tt) {
+      const int ks_ = tt % kKvStages;
+      if (!mbar_wait(&sm.k_full[ks_], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh) {
+      for (int h = 0; h < 2; ++h) {
+        // S_h last held P_h(tt - 1): its P.V must have completed
+        if (tt >= 1 && !mbar_wait(&sm.pv_done[h], (tt - 1) & 1, p.err, &sm.abort)) return;
+        tc::fence_after_sync();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          // K-major, 128B swizzle: a 16-element k step is 32 B inside the 128-B row; 8-row groups 1024 B apart
-          const uint64_t a = tc::smem_desc(q_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
-          const uint64_t b = tc::smem_desc(k_addr + kh * kHalfBytes + ks * 32, 16, 1024, tc::kLayoutSw128);
-          tc::mma_ss(tmem + kColS, a, b, idesc_qk, (kh | ks) != 0 ? 1u : 0u);
+        for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // K-major, 128B swizzle: a 16-element k step is 32 B inside the 128-B row; 8-row
+            // groups 1024 B apart; Q_h is rows 128 h .. 128 h + 127 of the item's Q
+            const uint64_t a = tc::smem_desc(q_addr + kh * kQHalfBytes + h * kHalfBytes + kk * 32, 16, 1024,
+                                             tc::kLayoutSw128);
+            const uint64_t b = tc::smem_desc(k_addr + ks_ * kTileBytes + kh * kHalfBytes + kk * 32, 16, 1024,
+                                             tc::kLayoutSw128);
+            tc::mma_ss(tmem + kColS + uint32_t(h * kTile), a, b, idesc_qk, (kh | kk) != 0 ? 1u : 0u);
+          }
         }
+        tc::commit(&sm.s_full[h]);
       }
-      tc::commit(&sm.s_full);
-      tc::commit(&sm.k_empty);
+      tc::commit(&sm.k_empty[ks_]);
       if (t == n_tiles - 1) tc::commit(&sm.q_empty);
-      if (!mbar_wait(&sm.p_full, tt & 1, p.err, &sm.abort)) return;
-      if (!mbar_wait(&sm.v_full, tt & 1, p.err, &sm.abort)) return;
-      if (t == 0 && nq > 0 && !mbar_wait(&sm.o_free, (nq - 1) & 1, p.err, &sm.abort)) return;
-      tc::fence_after_sync();
+    }
+    ++nq;
+  }
+}
+
+__device__ void pv_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P_h (TMEM), B = V (MN-major)
+  const uint32_t v_addr = smem_u32(sm.v[0]);
+  int tt = 0, nq = 0;
+  for (int pos = begin; pos < end; ++pos) {
+    Item it;
+    it.load(p.items, pos);
+    const int n_tiles = it.tiles();
+    if (n_tiles == 0) continue;
+    for (int t = 0; t < n_tiles; ++t, ++tt) {
+      const int vs = tt % kKvStages;
+      if (!mbar_wait(&sm.v_full[vs], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        // V as B (K = keys, N = dims), MN-major 128B swizzle: a 16-key step is two 8-row
-        // groups (2048 B); the second 64-dim half is the leading-dimension step (16 KB)
-        const uint64_t b = tc::smem_desc(v_addr + ks * 2048, kHalfBytes, 1024, tc::kLayoutSw128);
-        tc::mma_ts(tmem + kColO, tmem + kColS + ks * 8, b, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait(&sm.p_full[h], tt & 1, p.err, &sm.abort)) return;
+        // the item's first P.V overwrites O_h once the epilogue has read the previous item's O_h out
+        if (t == 0 && nq > 0 && !mbar_wait(&sm.o_free[h], (nq - 1) & 1, p.err, &sm.abort)) return;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          // V as B (K = keys, N = dims), MN-major 128B swizzle: a 16-key step is two 8-row groups
+          // (2048 B); the second 64-dim half is the leading-dimension step (16 KB)
+          const uint64_t b = tc::smem_desc(v_addr + vs * kTileBytes + ks * 2048, kHalfBytes, 1024, tc::kLayoutSw128);
+          tc::mma_ts(tmem + kColO + uint32_t(h * kTile), tmem + kColS + uint32_t(h * kTile) + ks * 8, b, idesc_pv,
+                     (t > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::commit(&sm.pv_done[h]);
       }
-      tc::commit(&sm.o_done);
-      tc::commit(&sm.v_empty);
-      ++tt;
+      tc::commit(&sm.v_empty[vs]);
     }
     ++nq;
   }
 }
 
 // ---------------------------------------------------------------------------------------------
-// warps 0-3: softmax, epilogue and the merge of split rows
+// warps 0-7: softmax of the two halves; warps 8-11: epilogue and the output of an item
 // ---------------------------------------------------------------------------------------------
 
-// Output row of (token, head) for tile row `row`.
+// Output row of (token, head) for item row `row`.
 __device__ __forceinline__ size_t out_row(const PrefillParams& p, const Item& it, int row) {
   return (size_t)(it.q_start + row / p.group) * p.hqo + it.kv_head * p.group + row % p.group;
 }
@@ -267,7 +315,6 @@ __device__ __forceinline__ void store_bf16_32(__nv_bfloat16* dst_ptr, const floa
 
 __device__ __forceinline__ float lse_out(float lse2) { return (lse2 == -INFINITY) ? -INFINITY : lse2 * kLn2; }
 
-
 // Hardware tanh (relative error about 2^-11, so a capped logit is within about 7e-4 * cap): one
 // instruction per score, where the exp2-based tanh would double the softmax's per-score work.
 __device__ __forceinline__ float tanh_fast(float x) {
@@ -276,17 +323,17 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return y;
 }
 
-// One KV tile: scores -> (soft-cap) -> mask keys outside [lo, lim) -> online-softmax update -> P
-// into the S columns of TMEM.
+// One KV tile of half h: scores -> (soft-cap) -> mask keys outside [lo, lim) -> online-softmax
+// update -> P into the first 64 columns of S_h.
 template <bool kMasked, bool kCap>
-__device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lo, int lim, float scale, float& m,
-                                             float& l, bool first, PrefillSmem& sm, int tt, const PrefillParams& p,
-                                             bool& alive) {
+__device__ __forceinline__ void softmax_tile(const uint32_t t_s, const uint32_t t_o, int lo, int lim, float scale,
+                                             float& m, float& l, bool first, PrefillSmem& sm, uint64_t* pv_done,
+                                             int pv_parity, const PrefillParams& p, bool& alive) {
   uint32_t s[kTile];
-  tc::tmem_ld32(t_lane + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
-  tc::tmem_ld32(t_lane + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-  tc::tmem_ld32(t_lane + kColS + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
-  tc::tmem_ld32(t_lane + kColS + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
+  tc::tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+  tc::tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+  tc::tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
+  tc::tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
   tc::tmem_wait_ld();
   if (kCap) {
     // capped logits in the log2 domain; the scale is then already applied
@@ -335,109 +382,146 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_lane, int lo, int 
   const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
   const float2 s0123 = __fadd2_rn(s01, s23);
   l += s0123.x + s0123.y;
-  tc::tmem_st32(t_lane + kColS + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
-  tc::tmem_st32(t_lane + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+  tc::tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+  tc::tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
   tc::tmem_wait_st();
-  if (__any_sync(0xffffffffu, need)) {
-    // O was last written by the previous tile's P.V: wait for it, then rescale in place
-    alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort));
+  if (__any_sync(kFull, need)) {
+    // O_h was last written by the previous tile's P.V: wait for it, then rescale in place
+    alive = alive && __all_sync(kFull, mbar_wait(pv_done, pv_parity, p.err, &sm.abort));
     tc::fence_after_sync();
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
-      tc::tmem_ld32(t_lane + kColO + 32 * c, o);
+      tc::tmem_ld32(t_o + 32 * c, o);
       tc::tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-      tc::tmem_st32(t_lane + kColO + 32 * c, o);
+      tc::tmem_st32(t_o + 32 * c, o);
     }
     tc::tmem_wait_st();
   }
 }
 
-// kWin / kCap: the plan has a sliding window / a logit soft-cap (compiled out of the plain kernel).
+// Softmax warpgroup of half h (rows 128 h .. 128 h + 127 of each item).
 template <bool kWin, bool kCap>
-__device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
-  const int row = threadIdx.x;  // 0..127 == TMEM lane
-  const int warp = row >> 5;
-  const int lane = row & 31;
-  const uint32_t t_lane = tmem + (uint32_t(warp * 32) << 16);
+__device__ void softmax_group(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end, int h) {
+  const int r = threadIdx.x & (kTile - 1);  // == TMEM lane
+  const int row = h * kTile + r;             // row of the item
+  const int lane = threadIdx.x & 31;
+  const uint32_t lane_base = tmem + (uint32_t((r >> 5) * 32) << 16);
+  const uint32_t t_s = lane_base + kColS + uint32_t(h * kTile);
+  const uint32_t t_o = lane_base + kColO + uint32_t(h * kTile);
   const float scale = p.scale_log2;
-  int tt = 0;
+  int tt = 0, nit = 0;
   bool alive = true;
-  for (int pos = begin; pos < end; ++pos) {
+  for (int pos = begin; pos < end; ++pos, ++nit) {
     Item it;
     it.load(p.items, pos);
     const int n_tiles = it.tiles();
-    const int rows_valid = it.q_len * p.group;
     const int u = row / p.group;
     float m = -INFINITY, l = 0.f;
-
-    for (int t = 0; t < n_tiles; ++t) {
+    for (int t = 0; t < n_tiles; ++t, ++tt) {
       const int base = it.kv_lo + t * kTile;
       const int lim = max(0, min(kTile, min(it.kv_hi - base, it.diag + u + 1 - base)));
       // sliding window: keys below diag + u - window_left are masked
       const int lo = kWin ? min(kTile, max(0, it.diag + u - p.window_left - base)) : 0;
-      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.s_full, tt & 1, p.err, &sm.abort));
+      alive = alive && __all_sync(kFull, mbar_wait(&sm.s_full[h], tt & 1, p.err, &sm.abort));
       if (alive) {
         tc::fence_after_sync();
-        if (__all_sync(0xffffffffu, lim >= kTile && lo <= 0))
-          softmax_tile<false, kCap>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
+        if (__all_sync(kFull, lim >= kTile && lo <= 0))
+          softmax_tile<false, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, &sm.pv_done[h], (tt - 1) & 1, p,
+                                    alive);
         else
-          softmax_tile<true, kCap>(t_lane, lo, lim, scale, m, l, t == 0, sm, tt, p, alive);
+          softmax_tile<true, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, &sm.pv_done[h], (tt - 1) & 1, p,
+                                   alive);
         tc::fence_before_sync();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full);
-      ++tt;
+      if (lane == 0) mbar_arrive(&sm.p_full[h]);
     }
+    // the item's statistics for the epilogue
+    const int ib = nit & 1;
+    if (nit >= 2)
+      alive = alive && __all_sync(kFull, mbar_wait(&sm.stat_empty[ib], ((nit >> 1) - 1) & 1, p.err, &sm.abort));
+    sm.stat_m[ib][row] = m;
+    sm.stat_l[ib][row] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.stat_full[ib]);
+  }
+}
 
-    // ---- epilogue: O / l and LSE, to the output or to a partial slot --------------------------
-    float lse2 = -INFINITY, inv = 0.f;
-    if (l > 0.f) {
-      lse2 = m + fast_log2(l);
-      inv = 1.f / l;
-    }
-    uint32_t o[kHeadDim];
+// Epilogue group: for each item and each half, O / l and LSE to the output (merged with a given
+// state) or to the item's partial slot.
+__device__ void epilogue_group(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  const int r = threadIdx.x & (kTile - 1);  // == TMEM lane
+  const int lane = threadIdx.x & 31;
+  const uint32_t lane_base = tmem + (uint32_t((r >> 5) * 32) << 16);
+  int tt = 0, nit = 0;
+  bool alive = true;
+  for (int pos = begin; pos < end; ++pos, ++nit) {
+    Item it;
+    it.load(p.items, pos);
+    const int n_tiles = it.tiles();
+    const int rows_valid = it.q_len * p.group;
+    const int ib = nit & 1;
+    alive = alive && __all_sync(kFull, mbar_wait(&sm.stat_full[ib], (nit >> 1) & 1, p.err, &sm.abort));
+    float m2[2], l2[2];
 #pragma unroll
-    for (int j = 0; j < kHeadDim; ++j) o[j] = 0u;
-    if (n_tiles > 0) {
-      alive = alive && __all_sync(0xffffffffu, mbar_wait(&sm.o_done, (tt - 1) & 1, p.err, &sm.abort));
-      if (alive) {
-        tc::fence_after_sync();
-        tc::tmem_ld32(t_lane + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(o + 0));
-        tc::tmem_ld32(t_lane + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
-        tc::tmem_ld32(t_lane + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(o + 64));
-        tc::tmem_ld32(t_lane + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(o + 96));
-        tc::tmem_wait_ld();
-      }
-      // O is in registers: the next item's first P.V may overwrite it while this one is written out
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free);
+    for (int h = 0; h < 2; ++h) {
+      m2[h] = sm.stat_m[ib][h * kTile + r];
+      l2[h] = sm.stat_l[ib][h * kTile + r];
     }
-    if (row < rows_valid) {
-      if (it.slot < 0) {
-        const size_t orow = out_row(p, it, row);
-        __nv_bfloat16* dst = p.o + orow * kHeadDim;
-        float wa = inv, wb = 0.f;  // weights of this state (unnormalised O) and of the given one
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.stat_empty[ib]);
+    const int last = tt + n_tiles - 1;
+    tt += n_tiles;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      const int row = h * kTile + r;
+      float lse2 = -INFINITY, inv = 0.f;
+      if (l2[h] > 0.f) {
+        lse2 = m2[h] + fast_log2(l2[h]);
+        inv = 1.f / l2[h];
+      }
+      const bool live = n_tiles > 0;
+      if (live) alive = alive && __all_sync(kFull, mbar_wait(&sm.pv_done[h], last & 1, p.err, &sm.abort));
+      tc::fence_after_sync();
+      // weights of this state (unnormalised O) and of the given one, and the output's LSE
+      float wa = inv, wb = 0.f;
+      size_t orow = 0;
+      const bool write = row < rows_valid;
+      if (write && it.slot < 0) {
+        orow = out_row(p, it, row);
         if (p.o_prev) {
           const float p2 = p.lse_prev[orow] * kLog2e;
-          const float m2 = fmaxf(lse2, p2);
-          if (m2 == -INFINITY) {
+          const float mm = fmaxf(lse2, p2);
+          if (mm == -INFINITY) {
             wa = 0.f;
           } else {
-            const float a = fast_exp2(lse2 - m2), b = fast_exp2(p2 - m2);
+            const float a = fast_exp2(lse2 - mm), b = fast_exp2(p2 - mm);
             wa = a * inv / (a + b);
             wb = b / (a + b);
-            lse2 = m2 + fast_log2(a + b);
+            lse2 = mm + fast_log2(a + b);
           }
         }
+      }
+      const uint32_t t_o = lane_base + kColO + uint32_t(h * kTile);
+      // O_h streamed out 32 columns at a time
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        if (live && alive) {
+          tc::tmem_ld32(t_o + 32 * c, o);
+          tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+        if (!write) continue;
+        if (it.slot < 0) {
           float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[32 * c + j]) * wa;
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) * wa;
           if (wb != 0.f) {
             const uint4* src = reinterpret_cast<const uint4*>(p.o_prev + orow * kHeadDim + 32 * c);
 #pragma unroll
@@ -445,32 +529,41 @@ __device__ void softmax_epilogue(const PrefillParams& p, PrefillSmem& sm, uint32
               const uint4 raw = src[q4];
               const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const float2 f = bf16x2_to_f2(w4[h]);
-                v[8 * q4 + 2 * h] += wb * f.x;
-                v[8 * q4 + 2 * h + 1] += wb * f.y;
+              for (int hh = 0; hh < 4; ++hh) {
+                const float2 f = bf16x2_to_f2(w4[hh]);
+                v[8 * q4 + 2 * hh] += wb * f.x;
+                v[8 * q4 + 2 * hh + 1] += wb * f.y;
               }
             }
           }
-          store_bf16_32(dst + 32 * c, v);
-        }
-        p.lse[orow] = lse_out(lse2);
-      } else {
-        const size_t srow = (size_t)it.slot * p.slot_rows + row;
-        float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kHeadDim);
+          store_bf16_32(p.o + orow * kHeadDim + 32 * c, v);
+        } else {
+          const size_t srow = (size_t)it.slot * p.slot_rows + row;
+          float4* dst = reinterpret_cast<float4*>(p.part_o + srow * kHeadDim + 32 * c);
 #pragma unroll
-        for (int j = 0; j < kHeadDim / 4; ++j)
-          dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                               __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
-        p.part_lse[srow] = lse2;
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                 __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        }
+      }
+      if (live) {
+        // O_h has been read: the next item's first P.V may overwrite it
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_free[h]);
+      }
+      if (write) {
+        if (it.slot < 0)
+          p.lse[orow] = lse_out(lse2);
+        else
+          p.part_lse[(size_t)it.slot * p.slot_rows + row] = lse2;
       }
     }
-
   }
 }
 
 template <bool kWin, bool kCap, bool kNhd>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ unsigned char smem_raw[];
@@ -483,23 +576,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    mbar_init(&sm.k_full, 1);
-    mbar_init(&sm.k_empty, 1);
-    mbar_init(&sm.v_full, 1);
-    mbar_init(&sm.v_empty, 1);
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 4);
-    mbar_init(&sm.o_done, 1);
-    mbar_init(&sm.o_free, 4);
+    for (int b = 0; b < kKvStages; ++b) {
+      mbar_init(&sm.k_full[b], 1);
+      mbar_init(&sm.k_empty[b], 1);
+      mbar_init(&sm.v_full[b], 1);
+      mbar_init(&sm.v_empty[b], 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sm.s_full[h], 1);
+      mbar_init(&sm.p_full[h], 4);      // one arrival per warp of the half's softmax group
+      mbar_init(&sm.pv_done[h], 1);
+      mbar_init(&sm.o_free[h], 4);      // one arrival per epilogue warp
+      mbar_init(&sm.stat_full[h], 8);   // one arrival per softmax warp (both groups)
+      mbar_init(&sm.stat_empty[h], 4);  // one arrival per epilogue warp
+    }
     sm.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && (threadIdx.x & 31) == 0) {
+  if (warp == 12 && (threadIdx.x & 31) == 0) {
     tc::tma_prefetch_desc(&tm_q);
     tc::tma_prefetch_desc(&tm_k);
     tc::tma_prefetch_desc(&tm_v);
   }
-  if (warp == 5) {
+  if (warp == 14) {
     tc::tmem_alloc(&sm.tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -511,20 +610,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if ((tmem & 0xFFFFu) + kTmemCols > 512u) {  // not an address this CTA can use: report, do nothing
     if (threadIdx.x == 0) atomicOr(p.err, FI_DEVERR_TMEM);
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     tc::regs_increase<kSoftmaxRegs>();
-    softmax_epilogue<kWin, kCap>(p, sm, tmem, begin, end);
+    softmax_group<kWin, kCap>(p, sm, tmem, begin, end, warp >> 2);
+  } else if (warp < 12) {
+    static_assert(kEpilogueRegs < 128 && kControlRegs < 128 && kSoftmaxRegs > 128,
+                  "setmaxnreg.inc only raises and setmaxnreg.dec only lowers the launch count (128)");
+    tc::regs_decrease<kEpilogueRegs>();
+    epilogue_group(p, sm, tmem, begin, end);
   } else {
     tc::regs_decrease<kControlRegs>();
-    if (warp == 4) {
-      producer<kNhd>(p, sm, &tm_q, &tm_k, &tm_v, begin, end);
-    } else if (warp == 5 && (threadIdx.x & 31) == 0) {
-      mma_issuer(p, sm, tmem, begin, end);
+    if (warp == 12) {
+      producer<kNhd, true>(p, sm, &tm_q, &tm_k, begin, end);
+    } else if (warp == 13) {
+      producer<kNhd, false>(p, sm, &tm_q, &tm_v, begin, end);
+    } else if (warp == 14 && (threadIdx.x & 31) == 0) {
+      qk_issuer(p, sm, tmem, begin, end);
+    } else if (warp == 15 && (threadIdx.x & 31) == 0) {
+      pv_issuer(p, sm, tmem, begin, end);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 14) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -656,7 +764,7 @@ bool make_map_nhd(CUtensorMap* m, const void* base, uint64_t hkv, uint64_t page_
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (encode_fn() == nullptr) return record_cuda_error(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
-  if (a.page_size % 8 != 0 || kTile % a.page_size != 0 || a.group > kTile || a.group * a.tile_tokens > kTile)
+  if (a.page_size % 8 != 0 || kTile % a.page_size != 0 || a.group > kItemRows || a.group * a.tile_tokens > kItemRows)
     return FI_ERR_UNSUPPORTED;
   if (a.total_q < 1 || a.num_pages < 1) return FI_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(a.q) % 16 || reinterpret_cast<uintptr_t>(a.k) % 16 ||

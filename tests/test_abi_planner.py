@@ -97,7 +97,7 @@ def test_workload_plans_match(lib, name):
     if name == "skewed_long_decode":
         assert a["header"][7] == 8          # the long request splits on each of its 8 KV heads
     if name == "ragged_causal_prefill":
-        assert a["header"][1] == 1 and a["header"][2] == 32
+        assert a["header"][1] == 1 and a["header"][2] == 64   # 256-row tiles: 64 tokens x g = 4
 
 
 @pytest.mark.parametrize("name", W.KERNEL_DIST_WORKLOADS)

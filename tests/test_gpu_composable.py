@@ -64,7 +64,7 @@ CASES = [
     # (hq, hk, page, q range, kv range, SM budget, head fraction)
     (8, 1, 16, (1, 1), (0, 4000), 5, 0.5),        # decode path, g = 8, split rows in both parts
     (64, 8, 1, (1, 1), (1, 600), 0, 0.3),         # decode path, g = 8, page 1
-    (8, 2, 16, (20, 80), (0, 1500), 16, 0.5),     # tensor-core path, split rows (contraction kernel merges)
+    (8, 2, 16, (20, 80), (0, 1500), 32, 0.5),     # tensor-core path, split rows (contraction kernel merges)
     (16, 4, 32, (40, 90), (100, 700), 0, 0.7),    # tensor-core path, direct writes merge in the epilogue
 ]
 

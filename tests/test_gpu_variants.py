@@ -73,9 +73,9 @@ def test_variant_parity(case):
 def test_variant_reruns_bit_identical():
     b = as_nhd(W.random_small_batch(4100, batch=3, num_qo_heads=8, num_kv_heads=2, page_size=16, causal=True,
                                     q_len_range=(40, 90), kv_len_range=(3000, 6000), scale=1.5))
-    o1, l1, ws = run_variant(b, 2000, 4.0, "NHD", 8)
+    o1, l1, ws = run_variant(b, 2000, 4.0, "NHD", 16)
     assert ws.info()[7] > 0          # windowed rows still long enough to be split
-    o2, l2, _ = run_variant(b, 2000, 4.0, "NHD", 8)
+    o2, l2, _ = run_variant(b, 2000, 4.0, "NHD", 16)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
     ro, rl = A.batch_attention(b, layout="NHD", window_left=2000, soft_cap=4.0)
     assert_close(o1, l1, ro, rl)

@@ -64,7 +64,7 @@ def test_coverage_and_bounds(seed):
     if int(lq.max(initial=0)) * g <= 8:
         assert p.path == P.PATH_DECODE and p.rows_tile >= int(lq.max(initial=1)) * g
     else:
-        assert p.path == P.PATH_TENSOR and p.tile_tokens * g <= 128 and p.rows_tile == 128
+        assert p.path == P.PATH_TENSOR and p.tile_tokens * g <= P.TC_ROWS and p.rows_tile == P.TC_ROWS
     # chunk bound: a whole number of pages, at least l_min and at least total / #CTA
     total = sum(c["hk"] * -(-int(lq[i]) // p.tile_tokens) * int(lk[i]) for i in range(len(lq)))
     assert p.num_ctas == c["n_cta"] * (P.TC_CTAS_PER_SM if p.path == P.PATH_TENSOR else P.DECODE_CTAS_PER_SM)
