@@ -34,12 +34,14 @@
 //   warp 13         TMA producer of V (two stages)
 //   warp 14         TMEM allocation and issue of S_h = Q_h K^T (one thread)
 //   warp 15         issue of O_h += P_h V (one thread)
-// TMEM: S0, S1 (columns 0-255, fp32) and O0, O1 (256-511).  The softmax of half h overwrites the
-// first 64 columns of S_h with its P (bf16 pairs), the A operand of O_h += P_h V, so P.V reads
-// only V from shared memory.  The MMA order per KV tile is QK0, QK1, PV0, PV1: while one half's
-// softmax runs, the tensor pipe works on the other half.  QK and P.V come from two issuing threads,
-// so neither's waits stall the other; O is handed to the epilogue as soon as the item's last P.V
-// of that half completes.
+// The MMAs work on 64-key sub-tiles of each 128-key K/V tile.  TMEM: two score buffers per half,
+// S_h,0 and S_h,1 (64 fp32 columns each, columns 0-255), and O0, O1 (256-511).  The softmax of half
+// h overwrites the first 32 columns of a sub-tile's S buffer with its P (bf16 pairs), the A operand
+// of O_h += P_h V, so P.V reads only V from shared memory.  With two S buffers per half, the QK of
+// sub-tile u + 1 waits only for the P.V of u - 1, so it runs while the softmax works on u, and the
+// two halves' MMAs fill each other's gaps.  QK and P.V come from two issuing threads, so neither's
+// waits stall the other; O is handed to the epilogue as soon as the item's last P.V of that half
+// completes.
 // Online softmax in base 2 with a lazy rescale: O and l are rescaled only when a row's running
 // maximum grows by more than 8 (a factor 256), which keeps exp2 arguments <= 8 and changes the
 // result only by rounding.
@@ -72,7 +74,8 @@ constexpr uint32_t kSoftmaxRegs = 176;
 constexpr uint32_t kEpilogueRegs = 104;
 constexpr uint32_t kControlRegs = 56;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;      // S_h at columns 128 h
+constexpr int kSub = 64;           // keys of an MMA sub-tile (two per K/V tile)
+constexpr uint32_t kColS = 0;      // S_h,b at columns 128 h + 64 b
 constexpr uint32_t kColO = 256;    // O_h at columns 256 + 128 h
 constexpr int kKvStages = 2;       // K and V shared-memory stages each
 constexpr float kRescaleThreshold = 8.0f;
@@ -111,7 +114,8 @@ struct PrefillSmem {
   float stat_m[2][kItemRows];        // [item parity][row]: running max at the end of the item
   float stat_l[2][kItemRows];        // [item parity][row]: row sum
   uint64_t q_full, q_empty, k_full[kKvStages], k_empty[kKvStages], v_full[kKvStages], v_empty[kKvStages];
-  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];  // per half of the item
+  uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // [half][S buffer]
+  uint64_t o_free[2];                                   // per half of the item
   uint64_t stat_full[2], stat_empty[2];                  // per item parity
   uint32_t tmem_base;
   int abort;
@@ -132,6 +136,7 @@ struct Item {
     slot = b.w;
   }
   __device__ __forceinline__ int tiles() const { return (kv_hi - kv_lo + kTile - 1) / kTile; }
+  __device__ __forceinline__ int subs() const { return (kv_hi - kv_lo + kSub - 1) / kSub; }
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -217,37 +222,41 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
 // = the softmax's arrivals), so each thread's waits overlap the other's issue.
 // ---------------------------------------------------------------------------------------------
 __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
-  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kTile, 0, 0);  // A = Q_h (K-major), B = K (K-major)
+  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kSub, 0, 0);  // A = Q_h (K-major), B = K rows (K-major)
   const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k[0]);
-  int tt = 0, nq = 0;
+  int tt = 0, uu = 0, nq = 0;  // K/V tiles, sub-tiles, items
   for (int pos = begin; pos < end; ++pos) {
     Item it;
     it.load(p.items, pos);
-    const int n_tiles = it.tiles();
+    const int n_tiles = it.tiles(), n_sub = it.subs();
     if (n_tiles == 0) continue;
     if (!mbar_wait(&sm.q_full, nq & 1, p.err, &sm.abort)) return;
     for (int t = 0; t < n_tiles; ++t, ++tt) {
       const int ks_ = tt % kKvStages;
       if (!mbar_wait(&sm.k_full[ks_], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
+      for (int sub = 0; sub < 2 && 2 * t + sub < n_sub; ++sub, ++uu) {
+        const int b = uu & 1;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // S_h last held P_h(tt - 1): its P.V must have completed
-        if (tt >= 1 && !mbar_wait(&sm.pv_done[h], (tt - 1) & 1, p.err, &sm.abort)) return;
-        tc::fence_after_sync();
+        for (int h = 0; h < 2; ++h) {
+          // S_h,b last held P_h(uu - 2): its P.V must have completed
+          if (uu >= 2 && !mbar_wait(&sm.pv_done[h][b], ((uu >> 1) - 1) & 1, p.err, &sm.abort)) return;
+          tc::fence_after_sync();
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh) {
+          for (int kh = 0; kh < 2; ++kh) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // K-major, 128B swizzle: a 16-element k step is 32 B inside the 128-B row; 8-row
-            // groups 1024 B apart; Q_h is rows 128 h .. 128 h + 127 of the item's Q
-            const uint64_t a = tc::smem_desc(q_addr + kh * kQHalfBytes + h * kHalfBytes + kk * 32, 16, 1024,
-                                             tc::kLayoutSw128);
-            const uint64_t b = tc::smem_desc(k_addr + ks_ * kTileBytes + kh * kHalfBytes + kk * 32, 16, 1024,
-                                             tc::kLayoutSw128);
-            tc::mma_ss(tmem + kColS + uint32_t(h * kTile), a, b, idesc_qk, (kh | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              // K-major, 128B swizzle: a 16-element k step is 32 B inside the 128-B row; 8-row
+              // groups 1024 B apart; Q_h is rows 128 h .. of the item's Q, the sub-tile's keys are
+              // rows 64 sub .. of the K tile
+              const uint64_t a = tc::smem_desc(q_addr + kh * kQHalfBytes + h * kHalfBytes + kk * 32, 16, 1024,
+                                               tc::kLayoutSw128);
+              const uint64_t bd = tc::smem_desc(k_addr + ks_ * kTileBytes + kh * kHalfBytes + sub * (kSub * 128) + kk * 32,
+                                                16, 1024, tc::kLayoutSw128);
+              tc::mma_ss(tmem + kColS + uint32_t(h * kTile + b * kSub), a, bd, idesc_qk, (kh | kk) != 0 ? 1u : 0u);
+            }
           }
+          tc::commit(&sm.s_full[h][b]);
         }
-        tc::commit(&sm.s_full[h]);
       }
       tc::commit(&sm.k_empty[ks_]);
       if (t == n_tiles - 1) tc::commit(&sm.q_empty);
@@ -259,30 +268,35 @@ __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem
 __device__ void pv_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
   constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P_h (TMEM), B = V (MN-major)
   const uint32_t v_addr = smem_u32(sm.v[0]);
-  int tt = 0, nq = 0;
+  int tt = 0, uu = 0, nq = 0;
   for (int pos = begin; pos < end; ++pos) {
     Item it;
     it.load(p.items, pos);
-    const int n_tiles = it.tiles();
+    const int n_tiles = it.tiles(), n_sub = it.subs();
     if (n_tiles == 0) continue;
     for (int t = 0; t < n_tiles; ++t, ++tt) {
       const int vs = tt % kKvStages;
       if (!mbar_wait(&sm.v_full[vs], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
+      for (int sub = 0; sub < 2 && 2 * t + sub < n_sub; ++sub, ++uu) {
+        const int b = uu & 1;
+        const bool first = t == 0 && sub == 0;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait(&sm.p_full[h], tt & 1, p.err, &sm.abort)) return;
-        // the item's first P.V overwrites O_h once the epilogue has read the previous item's O_h out
-        if (t == 0 && nq > 0 && !mbar_wait(&sm.o_free[h], (nq - 1) & 1, p.err, &sm.abort)) return;
-        tc::fence_after_sync();
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(&sm.p_full[h][b], (uu >> 1) & 1, p.err, &sm.abort)) return;
+          // the item's first P.V overwrites O_h once the epilogue has read the previous item's O_h out
+          if (first && nq > 0 && !mbar_wait(&sm.o_free[h], (nq - 1) & 1, p.err, &sm.abort)) return;
+          tc::fence_after_sync();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          // V as B (K = keys, N = dims), MN-major 128B swizzle: a 16-key step is two 8-row groups
-          // (2048 B); the second 64-dim half is the leading-dimension step (16 KB)
-          const uint64_t b = tc::smem_desc(v_addr + vs * kTileBytes + ks * 2048, kHalfBytes, 1024, tc::kLayoutSw128);
-          tc::mma_ts(tmem + kColO + uint32_t(h * kTile), tmem + kColS + uint32_t(h * kTile) + ks * 8, b, idesc_pv,
-                     (t > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kSub / 16; ++ks) {
+            // V as B (K = keys, N = dims), MN-major 128B swizzle: a 16-key step is two 8-row groups
+            // (2048 B); the second 64-dim half is the leading-dimension step (16 KB)
+            const uint64_t bd = tc::smem_desc(v_addr + vs * kTileBytes + sub * (kSub * 128) + ks * 2048, kHalfBytes,
+                                              1024, tc::kLayoutSw128);
+            tc::mma_ts(tmem + kColO + uint32_t(h * kTile), tmem + kColS + uint32_t(h * kTile + b * kSub) + ks * 8, bd,
+                       idesc_pv, (!first || ks > 0) ? 1u : 0u);
+          }
+          tc::commit(&sm.pv_done[h][b]);
         }
-        tc::commit(&sm.pv_done[h]);
       }
       tc::commit(&sm.v_empty[vs]);
     }
@@ -323,23 +337,21 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return y;
 }
 
-// One KV tile of half h: scores -> (soft-cap) -> mask keys outside [lo, lim) -> online-softmax
-// update -> P into the first 64 columns of S_h.
+// One 64-key sub-tile of half h: scores -> (soft-cap) -> mask keys outside [lo, lim) -> online
+// softmax update -> P into the first 32 columns of the sub-tile's S buffer.
 template <bool kMasked, bool kCap>
-__device__ __forceinline__ void softmax_tile(const uint32_t t_s, const uint32_t t_o, int lo, int lim, float scale,
-                                             float& m, float& l, bool first, PrefillSmem& sm, uint64_t* pv_done,
-                                             int pv_parity, const PrefillParams& p, bool& alive) {
-  uint32_t s[kTile];
+__device__ __forceinline__ void softmax_sub(const uint32_t t_s, const uint32_t t_o, int lo, int lim, float scale,
+                                            float& m, float& l, bool first, PrefillSmem& sm, uint64_t* pv_done,
+                                            int pv_parity, const PrefillParams& p, bool& alive) {
+  uint32_t s[kSub];
   tc::tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
   tc::tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-  tc::tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
-  tc::tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
   tc::tmem_wait_ld();
   if (kCap) {
     // capped logits in the log2 domain; the scale is then already applied
     const float in_scale = scale / p.cap_log2;
 #pragma unroll
-    for (int j = 0; j < kTile; ++j) s[j] = __float_as_uint(p.cap_log2 * tanh_fast(__uint_as_float(s[j]) * in_scale));
+    for (int j = 0; j < kSub; ++j) s[j] = __float_as_uint(p.cap_log2 * tanh_fast(__uint_as_float(s[j]) * in_scale));
     scale = 1.f;
   }
   // row maximum of the (scaled) scores with 8 independent partial maxima
@@ -347,7 +359,7 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_s, const uint32_t 
 #pragma unroll
   for (int j = 0; j < 8; ++j) mx8[j] = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < kTile; ++j) {
+  for (int j = 0; j < kSub; ++j) {
     if (kMasked) s[j] = (j < lim && j >= lo) ? s[j] : __float_as_uint(-INFINITY);
     mx8[j & 7] = fmaxf(mx8[j & 7], __uint_as_float(s[j]));
   }
@@ -373,7 +385,7 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_s, const uint32_t 
 #pragma unroll
   for (int j = 0; j < 4; ++j) sum4[j] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int j = 0; j < kTile / 2; ++j) {
+  for (int j = 0; j < kSub / 2; ++j) {
     const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), sc2, nm2);
     const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
     sum4[j & 3] = __fadd2_rn(sum4[j & 3], pp);
@@ -383,10 +395,9 @@ __device__ __forceinline__ void softmax_tile(const uint32_t t_s, const uint32_t 
   const float2 s0123 = __fadd2_rn(s01, s23);
   l += s0123.x + s0123.y;
   tc::tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
-  tc::tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
   tc::tmem_wait_st();
   if (__any_sync(kFull, need)) {
-    // O_h was last written by the previous tile's P.V: wait for it, then rescale in place
+    // O_h was last written by the previous sub-tile's P.V: wait for it, then rescale in place
     alive = alive && __all_sync(kFull, mbar_wait(pv_done, pv_parity, p.err, &sm.abort));
     tc::fence_after_sync();
 #pragma unroll
@@ -409,35 +420,37 @@ __device__ void softmax_group(const PrefillParams& p, PrefillSmem& sm, uint32_t 
   const int row = h * kTile + r;             // row of the item
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = tmem + (uint32_t((r >> 5) * 32) << 16);
-  const uint32_t t_s = lane_base + kColS + uint32_t(h * kTile);
   const uint32_t t_o = lane_base + kColO + uint32_t(h * kTile);
   const float scale = p.scale_log2;
-  int tt = 0, nit = 0;
+  int uu = 0, nit = 0;
   bool alive = true;
   for (int pos = begin; pos < end; ++pos, ++nit) {
     Item it;
     it.load(p.items, pos);
-    const int n_tiles = it.tiles();
+    const int n_sub = it.subs();
     const int u = row / p.group;
     float m = -INFINITY, l = 0.f;
-    for (int t = 0; t < n_tiles; ++t, ++tt) {
-      const int base = it.kv_lo + t * kTile;
-      const int lim = max(0, min(kTile, min(it.kv_hi - base, it.diag + u + 1 - base)));
+    for (int t = 0; t < n_sub; ++t, ++uu) {
+      const int b = uu & 1;
+      const uint32_t t_s = lane_base + kColS + uint32_t(h * kTile + b * kSub);
+      const int base = it.kv_lo + t * kSub;
+      const int lim = max(0, min(kSub, min(it.kv_hi - base, it.diag + u + 1 - base)));
       // sliding window: keys below diag + u - window_left are masked
-      const int lo = kWin ? min(kTile, max(0, it.diag + u - p.window_left - base)) : 0;
-      alive = alive && __all_sync(kFull, mbar_wait(&sm.s_full[h], tt & 1, p.err, &sm.abort));
+      const int lo = kWin ? min(kSub, max(0, it.diag + u - p.window_left - base)) : 0;
+      alive = alive && __all_sync(kFull, mbar_wait(&sm.s_full[h][b], (uu >> 1) & 1, p.err, &sm.abort));
       if (alive) {
         tc::fence_after_sync();
-        if (__all_sync(kFull, lim >= kTile && lo <= 0))
-          softmax_tile<false, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, &sm.pv_done[h], (tt - 1) & 1, p,
-                                    alive);
+        // the P.V that last wrote O_h: sub-tile uu - 1, in the other S buffer
+        uint64_t* prev_pv = &sm.pv_done[h][b ^ 1];
+        const int prev_parity = ((uu - 1) >> 1) & 1;
+        if (__all_sync(kFull, lim >= kSub && lo <= 0))
+          softmax_sub<false, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, prev_pv, prev_parity, p, alive);
         else
-          softmax_tile<true, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, &sm.pv_done[h], (tt - 1) & 1, p,
-                                   alive);
+          softmax_sub<true, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, prev_pv, prev_parity, p, alive);
         tc::fence_before_sync();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[h]);
+      if (lane == 0) mbar_arrive(&sm.p_full[h][b]);
     }
     // the item's statistics for the epilogue
     const int ib = nit & 1;
@@ -461,7 +474,7 @@ __device__ void epilogue_group(const PrefillParams& p, PrefillSmem& sm, uint32_t
   for (int pos = begin; pos < end; ++pos, ++nit) {
     Item it;
     it.load(p.items, pos);
-    const int n_tiles = it.tiles();
+    const int n_tiles = it.subs();  // sub-tiles
     const int rows_valid = it.q_len * p.group;
     const int ib = nit & 1;
     alive = alive && __all_sync(kFull, mbar_wait(&sm.stat_full[ib], (nit >> 1) & 1, p.err, &sm.abort));
@@ -484,7 +497,7 @@ __device__ void epilogue_group(const PrefillParams& p, PrefillSmem& sm, uint32_t
         inv = 1.f / l2[h];
       }
       const bool live = n_tiles > 0;
-      if (live) alive = alive && __all_sync(kFull, mbar_wait(&sm.pv_done[h], last & 1, p.err, &sm.abort));
+      if (live) alive = alive && __all_sync(kFull, mbar_wait(&sm.pv_done[h][last & 1], (last >> 1) & 1, p.err, &sm.abort));
       tc::fence_after_sync();
       // weights of this state (unnormalised O) and of the given one, and the output's LSE
       float wa = inv, wb = 0.f;
@@ -583,9 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.v_empty[b], 1);
     }
     for (int h = 0; h < 2; ++h) {
-      mbar_init(&sm.s_full[h], 1);
-      mbar_init(&sm.p_full[h], 4);      // one arrival per warp of the half's softmax group
-      mbar_init(&sm.pv_done[h], 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&sm.s_full[h][b], 1);
+        mbar_init(&sm.p_full[h][b], 4);  // one arrival per warp of the half's softmax group
+        mbar_init(&sm.pv_done[h][b], 1);
+      }
       mbar_init(&sm.o_free[h], 4);      // one arrival per epilogue warp
       mbar_init(&sm.stat_full[h], 8);   // one arrival per softmax warp (both groups)
       mbar_init(&sm.stat_empty[h], 4);  // one arrival per epilogue warp
