@@ -589,32 +589,40 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
         return bench_variant(name, torch, dev, hbm_peak, bf16_peak, steps, warmup)
     w = W.by_name(name)
     if name == "shared_prefix_decode":
-        pre, suf = Case(w.prefix, torch, dev), None
-        suf = Case.__new__(Case)
-        suf.b, suf.torch, suf.q, suf.k, suf.v = w.suffix, torch, pre.q, pre.k, pre.v
-        suf.o = torch.empty_like(pre.o)
-        suf.lse = torch.empty_like(pre.lse)
-        suf.ws = B.Workspace(w.suffix.batch_size, w.suffix.total_q, int(w.suffix.kv_indptr[-1]), 32, 8)
-        suf.plan()
+        # one composable plan: the prefix block row (tensor cores, chunks to slots) and the suffix rows
+        # (decode tiles, each merging its chunks and the prefix slots of its rows): two launches
+        pre = Case(w.prefix, torch, dev)
+        ws = B.Workspace(w.suffix.batch_size, w.suffix.total_q, max(int(w.suffix.kv_indptr[-1]),
+                                                                   int(w.prefix.kv_indptr[-1])), 32, 8)
+        ws.plan_composable((w.prefix.qo_indptr, w.prefix.kv_indptr, w.prefix.kv_indices, w.prefix.last_page_len),
+                           (w.suffix.qo_indptr, w.suffix.kv_indptr, w.suffix.kv_indices, w.suffix.last_page_len),
+                           16, False)
         o, lse = torch.empty_like(pre.o), torch.empty_like(pre.lse)
 
-        def suffix_merged():
-            # suffix attention, each row written as prefix state ⊕ suffix state (fi_run_merge)
-            suf.ws.run_merge(suf.q, suf.k, suf.v, pre.o, pre.lse, o, lse)
-
         def step():
-            pre.run()
-            suffix_merged()
+            ws.run(pre.q, pre.k, pre.v, o, lse)
 
         ms = time_launches(torch, step, steps, warmup)
-        parts = {"prefix_attention_and_contraction": time_launches(torch, pre.run, steps, warmup) * 1e3,
-                 "suffix_decode_merged": time_launches(torch, suffix_merged, steps, warmup) * 1e3,
-                 "suffix_decode_alone": time_launches(torch, suf.run, steps, warmup) * 1e3}
+        errs = ws.get_error()
+        # the same step as two plans (prefix attention + its contraction, then the suffix decode with
+        # the prefix state folded in by fi_run_merge): three launches
+        suf = Case.__new__(Case)
+        suf.b, suf.torch, suf.q, suf.k, suf.v = w.suffix, torch, pre.q, pre.k, pre.v
+        suf.o, suf.lse = torch.empty_like(pre.o), torch.empty_like(pre.lse)
+        suf.ws = B.Workspace(w.suffix.batch_size, w.suffix.total_q, int(w.suffix.kv_indptr[-1]), 32, 8)
+        suf.plan()
+
+        def two_plans():
+            pre.run()
+            suf.ws.run_merge(suf.q, suf.k, suf.v, pre.o, pre.lse, suf.o, suf.lse)
+
+        ms_two = time_launches(torch, two_plans, steps, warmup)
         nbytes = kv_bytes(w.prefix) + kv_bytes(w.suffix)
         return {"us_per_batch": ms * 1e3, "kv_gbs_unique": nbytes / (ms * 1e-3) / 1e9,
-                "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "launches_per_step": 3,
-                "us_each_alone": parts,
-                "prefix_plan": pre.ws.info().tolist()[:10], "suffix_plan": suf.ws.info().tolist()[:10]}
+                "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / hbm_peak, "launches_per_step": 2,
+                "plan": "one composable plan (fi_plan_composable): prefix on tcgen05 tiles, suffix decode merging "
+                        "the prefix slots", "device_errors": errs,
+                "us_two_plans_three_launches": ms_two * 1e3, "composable_plan": ws.info().tolist()[:10]}
     c = Case(w, torch, dev)
     cold = kv_bytes(w) < 2 * L2_BYTES  # inputs that L2 could hold: flush it before every launch
     ms = (time_launches_cold if cold else time_launches)(torch, c.run, steps, warmup)

@@ -177,6 +177,40 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
             int page_size, int causal, void* stream);
 
 /*
+ * fi_plan_composable -- inspector step for a batch given in composable formats: a shared
+ * sub-matrix plus per-request rows, planned together with one reduction map.
+ *
+ * Source: 核心机制 2 "可组合格式" (paper §3.1.2, Fig. 3): a KV-cache whose requests share a
+ * prefix is the sum of two block-sparse matrices over the same query rows: the shared part, whose
+ * block rows span all query tokens of a group (Br = the group's tokens), and the per-request part
+ * (Br = 1); their attention states combine with ⊕ (术语与记号 "Attention State 与 ⊕", §2.2).
+ * 核心机制 6-7 (§3.3.1, App. D): both parts are cut into chunks and queued as one plan whose
+ * reduction map spans both formats.
+ *
+ *   shared_*       HOST int32, as for fi_plan: block row i covers query tokens
+ *                  shared_qo_indptr[i] .. shared_qo_indptr[i+1] - 1 (the same token numbering as
+ *                  qo_indptr; shared_qo_indptr[shared_batch] <= qo_indptr[batch]) and owns pages
+ *                  shared_kv_indices[shared_kv_indptr[i] .. shared_kv_indptr[i+1]).  Every key of a
+ *                  block row is visible to all of its tokens.
+ *   qo_indptr .. last_page_len, batch, causal   the per-request part, as for fi_plan (causal masks
+ *                  align to the end of each request's own KV)
+ *
+ * Output row t is (state of t over its block row's shared keys) ⊕ (state over its own keys).  The
+ * shared part takes 256-row tensor-core tiles and writes every chunk to a partial slot; the
+ * per-request part takes decode tiles (every request must have at most 8 rows = query tokens x group
+ * size, else UNSUPPORTED), and each of its rows merges its own chunks and the shared slots that hold
+ * its rows, in the plan's fixed order.  fi_run then makes two launches, the second chained to the
+ * first by programmatic dependent launch.  The workspace's variant must be the default (bf16 HND
+ * pages, no window, no soft-cap), else UNSUPPORTED; fi_run_merge with a given state is UNSUPPORTED
+ * for these plans.  fi_plan_info reports path 2.  Other behaviour and errors as fi_plan.
+ */
+int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const int32_t* shared_kv_indptr,
+                       const int32_t* shared_kv_indices, const int32_t* shared_last_page_len, int shared_batch,
+                       const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                       int page_size, int causal, void* stream);
+
+/*
  * fi_run -- executor step: one persistent kernel (attention + merge of split rows).
  *
  * Source: 核心机制 6-7 (paper §3.3.1, App. D): attention and the contraction
@@ -254,7 +288,8 @@ int fi_get_error(fi_workspace* ws, int32_t* err_bits);
 
 /*
  * fi_plan_info -- copy the current plan's 16-int32 header to host memory:
- *   [0] magic 0x46495031  [1] path (0 decode tiles, 1 tensor-core tiles)
+ *   [0] magic 0x46495031  [1] path (0 decode tiles, 1 tensor-core tiles, 2 composable: the
+ *                         remaining fields are those of the per-request part)
  *   [2] tokens per tile   [3] rows per tile  [4] group size g  [5] #CTA
  *   [6] work items  [7] split rows  [8] partial slots  [9] L_kv (tokens)
  *   [10] page_size  [11] causal  [12] num_qo_heads  [13] num_kv_heads
@@ -283,6 +318,24 @@ int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const in
                     int num_qo_heads, int num_kv_heads, int head_dim, int page_size, int causal, int num_sms,
                     int64_t alpha, int64_t beta, int32_t l_min, int32_t window_left, int32_t* out,
                     int64_t capacity, int64_t* out_len);
+
+/*
+ * fi_plan_composable_compute -- the composable planner alone, on the host, with no device work.
+ *
+ * Inputs as fi_plan_composable (no page ids), with the SM budget and the default cost model.
+ * Writes the shared part's plan (as fi_plan_compute lays a plan out, every unit listed), then the
+ * per-request part's plan (its header's slot count covers both parts' slots; slot_to_split_row has
+ * -1 for the shared slots; unit fields 5 and 6 are the unit's first ext entry and count), then the
+ * ext list: per entry {shared slot, (row offset + 512) | (rows of the shared tile << 16)}.  An item
+ * whose slot field is -(2 + u) writes its rows directly after merging unit u's ext entries.
+ *   out, capacity, out_len   as fi_plan_compute
+ * Errors: INVALID_ARG, UNSUPPORTED, CAPACITY.
+ */
+int fi_plan_composable_compute(const int32_t* shared_qo_indptr, const int32_t* shared_kv_indptr,
+                               const int32_t* shared_last_page_len, int shared_batch, const int32_t* qo_indptr,
+                               const int32_t* kv_indptr, const int32_t* last_page_len, int batch, int num_qo_heads,
+                               int num_kv_heads, int head_dim, int page_size, int causal, int num_sms, int32_t* out,
+                               int64_t capacity, int64_t* out_len);
 
 /*
  * fi_decode_noalloc -- the CUDA-core decode path without any allocation.

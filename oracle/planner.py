@@ -86,10 +86,11 @@ class Plan:
     loads: list            # accumulated cost per CTA
 
 
-def choose_path(l_q, group: int):
-    """Tile choice (核心机制 4, paper §3.2.2): decode tiles for <= 8 rows, 256-row tensor-core tiles otherwise."""
+def choose_path(l_q, group: int, force_tensor: bool = False):
+    """Tile choice (核心机制 4, paper §3.2.2): decode tiles for <= 8 rows, 256-row tensor-core tiles otherwise
+    (or always, for the shared part of a composable plan)."""
     max_rows = int(max((int(x) for x in l_q), default=0)) * group
-    if max_rows <= DECODE_MAX_ROWS:
+    if max_rows <= DECODE_MAX_ROWS and not force_tensor:
         tile_tokens = max(1, int(max((int(x) for x in l_q), default=1)))
         rows = 1
         while rows < tile_tokens * group:
@@ -102,9 +103,11 @@ def choose_path(l_q, group: int):
 
 def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: int, page_size: int,
          causal: bool, num_sms: int, head_dim: int = 128, alpha: int = 1, beta: int = 1,
-         l_min: int = 256, window_left: int = -1) -> Plan:
+         l_min: int = 256, window_left: int = -1, force_tensor: bool = False, all_slots: bool = False) -> Plan:
     """window_left >= 0: sliding window (causal plans only); each tile reads only the keys its
-    tokens' windows reach, from the first token's window start rounded down to a page."""
+    tokens' windows reach, from the first token's window start rounded down to a page.
+    force_tensor: tensor-core tiles whatever the rows; all_slots: every unit, split or not, writes its
+    chunks' partial states to slots (both used by the shared part of a composable plan)."""
     if window_left >= 0 and not causal:
         raise ValueError("the sliding window is read with causal masks")
     qo = [int(x) for x in qo_indptr]
@@ -121,7 +124,7 @@ def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: i
         l_kv.append((n_p - 1) * page_size + last[i] if n_p > 0 else 0)
 
     # a2: path and tile
-    path, tile_tokens, rows_tile = choose_path(l_q, g)
+    path, tile_tokens, rows_tile = choose_path(l_q, g, force_tensor)
     num_ctas = (TC_CTAS_PER_SM if path == PATH_TENSOR else DECODE_CTAS_PER_SM) * num_sms
 
     def extent(i, q0, qn):
@@ -165,10 +168,10 @@ def plan(qo_indptr, kv_indptr, last_page_len, num_qo_heads: int, num_kv_heads: i
                     cs = _ceil_div(_ceil_div(e - lo_e, n), page_size) * page_size
                     n = _ceil_div(e - lo_e, cs)
                 unit = -1
-                if n > 1:
+                if n > 1 or all_slots:
                     unit = len(units)
                     units.append(dict(first_slot=len(slot_unit), n_chunks=n, q_start=qo[i] + q0, q_len=qn,
-                                      kv_head=h))
+                                      kv_head=h, ext_first=0, ext_count=0))
                     slot_unit.extend([unit] * n)
                 for c in range(n):
                     lo, hi = lo_e + c * cs, min(e, lo_e + (c + 1) * cs)
@@ -214,7 +217,8 @@ def serialize(p: Plan) -> np.ndarray:
                            it["diag"], it["slot"]]
     flat_units = []
     for u in p.units:
-        flat_units += [u["first_slot"], u["n_chunks"], u["q_start"], u["q_len"], u["kv_head"], 0, 0, 0]
+        flat_units += [u["first_slot"], u["n_chunks"], u["q_start"], u["q_len"], u["kv_head"], u.get("ext_first", 0),
+                       u.get("ext_count", 0), 0]
     return np.array(header + indptr + flat_items + flat_units + list(p.slot_unit), dtype=np.int64).astype(np.int32)
 
 
@@ -233,3 +237,115 @@ def deserialize(buf) -> dict:
     slot_unit = buf[o:o + n_slots]
     o += n_slots
     return dict(header=h, cta_indptr=indptr, items=items, units=units, slot_unit=slot_unit, length=o)
+
+
+# ---------------------------------------------------------------------------
+# Composable formats (核心机制 2, paper §3.1.2, Figure 3)
+# ---------------------------------------------------------------------------
+EXT_ROW_BIAS = 512
+TC_KEY_COST = (4, 3)   # a 256-row tensor-core key costs about 4/3 of a decode key of SM time
+
+
+def plan_composable(shared, unique, num_qo_heads: int, num_kv_heads: int, page_size: int, causal: bool,
+                    num_sms: int, head_dim: int = 128):
+    """One plan over two BSR sub-matrices of the same query rows, with one reduction map.
+
+    `shared` and `unique` are (qo_indptr, kv_indptr, last_page_len).  The shared part (block rows such
+    as a prefix shared by a group of requests) sees all of its keys, takes tensor-core tiles and writes
+    every chunk to a slot.  The per-request part takes decode tiles; its slots are numbered after the
+    shared ones.  Each of its units lists, in order, the shared slots holding states of its rows: one
+    entry (slot, packed) per chunk of every shared tile that holds some of its tokens, packed =
+    (row offset + 512) | (rows of the shared tile << 16).  Split units get the list first, in unit
+    order; then every single-chunk item (queue order) whose rows have shared states gets a unit of its
+    own (first slot -1, one chunk) and the slot field -(2 + unit).
+    """
+    # SM budget split (both parts run at once on disjoint SMs): the shared part gets
+    # round(num_sms * c_a / (c_a + c_b)) CTAs, at least 1 and leaving at least 1, where c_a = 4 x its
+    # keys and c_b = 3 x the per-request keys (a key of a 256-row tensor-core tile costs about 4/3 of a
+    # decode key of SM time)
+    def keys(qo, kv, last):
+        qo, kv, last = [int(x) for x in qo], [int(x) for x in kv], [int(x) for x in last]
+        tot = 0
+        for i in range(len(qo) - 1):
+            n_p = kv[i + 1] - kv[i]
+            if qo[i + 1] > qo[i] and n_p > 0:
+                tot += num_kv_heads * ((n_p - 1) * page_size + last[i])
+        return tot
+    n_a = num_sms
+    if num_sms > 1:
+        c_a, c_b = TC_KEY_COST[0] * keys(*shared), TC_KEY_COST[1] * keys(*unique)
+        n_a = (2 * num_sms * c_a + (c_a + c_b)) // (2 * (c_a + c_b)) if c_a + c_b > 0 else 1
+        n_a = min(max(n_a, 1), num_sms - 1)
+    a = plan(*shared, num_qo_heads, num_kv_heads, page_size, False, n_a, head_dim, force_tensor=True,
+             all_slots=True)
+    # one adjustment toward one chunk per CTA: fewer chunks than CTAs -> one CTA per chunk; more but at
+    # most twice as many -> as many CTAs as chunks (leaving one SM); then the shared part is planned again
+    items = len(a.items)
+    if items < n_a:
+        n_adj = max(items, 1)
+    elif num_sms > 1 and n_a < items <= 2 * n_a:
+        n_adj = min(items, num_sms - 1)
+    else:
+        n_adj = n_a
+    if n_adj != n_a:
+        n_a = n_adj
+        a = plan(*shared, num_qo_heads, num_kv_heads, page_size, False, n_a, head_dim, force_tensor=True,
+                 all_slots=True)
+    n_b = num_sms - n_a if num_sms > 1 else 1
+    b = plan(*unique, num_qo_heads, num_kv_heads, page_size, causal, n_b, head_dim)
+    if b.path != PATH_DECODE:
+        raise ValueError("the per-request part must take decode tiles")
+    g = num_qo_heads // num_kv_heads
+    s_a = len(a.slot_unit)
+    for it in b.items:
+        if it["slot"] >= 0:
+            it["slot"] += s_a
+    for u in b.units:
+        u["first_slot"] += s_a
+    b.slot_unit = [-1] * s_a + list(b.slot_unit)
+    a_qo = [int(x) for x in shared[0]]
+    base = [0]
+    for i in range(len(a_qo) - 1):
+        base.append(base[-1] + num_kv_heads * _ceil_div(a_qo[i + 1] - a_qo[i], a.tile_tokens))
+    ext = []
+
+    def add_ext(q0, qn, h):
+        count = 0
+        for i in range(len(a_qo) - 1):
+            lo, hi = max(q0, a_qo[i]), min(q0 + qn, a_qo[i + 1])
+            if lo >= hi:
+                continue
+            n_tiles = _ceil_div(a_qo[i + 1] - a_qo[i], a.tile_tokens)
+            for j in range((lo - a_qo[i]) // a.tile_tokens, (hi - 1 - a_qo[i]) // a.tile_tokens + 1):
+                u = a.units[base[i] + h * n_tiles + j]
+                packed = ((q0 - u["q_start"]) * g + EXT_ROW_BIAS) | ((u["q_len"] * g) << 16)
+                for c in range(u["n_chunks"]):
+                    ext.append((u["first_slot"] + c, packed))
+                    count += 1
+        return count
+
+    for u in b.units:
+        u["ext_first"] = len(ext)
+        u["ext_count"] = add_ext(u["q_start"], u["q_len"], u["kv_head"])
+    for q in b.queues:
+        for k in q:
+            it = b.items[k]
+            if it["slot"] != -1:
+                continue
+            first = len(ext)
+            cnt = add_ext(it["q_start"], it["q_len"], it["kv_head"])
+            if cnt == 0:
+                continue
+            b.units.append(dict(first_slot=-1, n_chunks=1, q_start=it["q_start"], q_len=it["q_len"],
+                                kv_head=it["kv_head"], ext_first=first, ext_count=cnt))
+            it["slot"] = -(2 + len(b.units) - 1)
+    return a, b, ext
+
+
+def serialize_composable(a: Plan, b: Plan, ext) -> np.ndarray:
+    """shared plan | per-request plan (its header's slot count = all slots) | ext pairs."""
+    sa = serialize(a)
+    sb = serialize(b)
+    sb[8] = len(b.slot_unit)
+    flat_ext = [v for pair in ext for v in pair]
+    return np.concatenate([sa, sb, np.array(flat_ext, dtype=np.int64).astype(np.int32)])

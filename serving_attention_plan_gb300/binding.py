@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
     L.fi_workspace_set_variant.argtypes = [c_void_p, c_int32, ctypes.c_float, c_int32]
     L.fi_workspace_set_kv_dtype.argtypes = [c_void_p, c_int32, ctypes.c_float, ctypes.c_float]
     L.fi_plan.argtypes = [c_void_p, P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]
+    L.fi_plan_composable.argtypes = [c_void_p, P32, P32, P32, P32, c_int, P32, P32, P32, P32, c_int, c_int, c_int,
+                                     c_int, c_int, c_int, c_void_p]
     L.fi_run.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     L.fi_run_merge.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p]
@@ -58,6 +60,8 @@ def lib() -> ctypes.CDLL:
     L.fi_plan_info.argtypes = [c_void_p, P32]
     L.fi_plan_compute.argtypes = [P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int64, c_int64,
                                   c_int32, c_int32, P32, c_int64, POINTER(c_int64)]
+    L.fi_plan_composable_compute.argtypes = [P32, P32, P32, c_int, P32, P32, P32, c_int, c_int, c_int, c_int, c_int,
+                                             c_int, c_int, P32, c_int64, POINTER(c_int64)]
     L.fi_decode_noalloc.argtypes = [P32, P32, P32, P32, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                                     c_void_p, c_int, c_void_p, c_void_p, c_void_p]
     L.fi_decode_noalloc_get_error.argtypes = [P32]
@@ -69,7 +73,8 @@ def lib() -> ctypes.CDLL:
     for name in ("fi_workspace_create", "fi_workspace_destroy", "fi_workspace_set_cost_model",
                  "fi_workspace_set_variant", "fi_workspace_set_kv_dtype", "fi_plan", "fi_run",
                  "fi_run_merge", "fi_merge_states", "fi_get_error", "fi_plan_info", "fi_plan_compute", "fi_device_sm_count",
-                 "fi_decode_noalloc", "fi_decode_noalloc_get_error"):
+                 "fi_decode_noalloc", "fi_decode_noalloc_get_error", "fi_plan_composable_compute",
+                 "fi_plan_composable"):
         getattr(L, name).restype = c_int
     _LIB = L
     return L
@@ -121,6 +126,23 @@ def plan_compute(qo_indptr, kv_indptr, last_page_len, num_qo_heads, num_kv_heads
     return out[: n.value]
 
 
+def plan_composable_compute(shared, unique, num_qo_heads, num_kv_heads, page_size, causal, num_sms,
+                            head_dim=128) -> np.ndarray:
+    """The composable planner alone (no GPU): shared and unique are (qo_indptr, kv_indptr, last_page_len)."""
+    L = lib()
+    sq, sk, sl = (_i32(x) for x in shared)
+    uq, uk, ul = (_i32(x) for x in unique)
+    n = c_int64(0)
+    args = [_p32(sq), _p32(sk), _p32(sl), sq.shape[0] - 1, _p32(uq), _p32(uk), _p32(ul), uq.shape[0] - 1,
+            num_qo_heads, num_kv_heads, head_dim, page_size, int(causal), num_sms]
+    st = L.fi_plan_composable_compute(*args, None, 0, ctypes.byref(n))
+    if st not in (FI_OK, 2):
+        _check(st, "fi_plan_composable_compute")
+    out = np.zeros(max(int(n.value), 1), dtype=np.int32)
+    _check(L.fi_plan_composable_compute(*args, _p32(out), out.shape[0], ctypes.byref(n)), "fi_plan_composable_compute")
+    return out[: n.value]
+
+
 def device_sm_count() -> int:
     v = c_int(0)
     _check(lib().fi_device_sm_count(ctypes.byref(v)), "fi_device_sm_count")
@@ -167,6 +189,17 @@ class Workspace:
             idx = np.zeros(1, np.int32)
         _check(lib().fi_plan(self._h, _p32(qo), _p32(kv), _p32(idx), _p32(last), qo.shape[0] - 1, self.num_qo_heads,
                              self.num_kv_heads, self.head_dim, page_size, int(causal), _stream_ptr(stream)), "fi_plan")
+
+    def plan_composable(self, shared, unique, page_size, causal, stream=None):
+        """Composable plan: shared and unique are (qo_indptr, kv_indptr, kv_indices, last_page_len)."""
+        sq, sk, si, sl = (_i32(x) for x in shared)
+        uq, uk, ui, ul = (_i32(x) for x in unique)
+        si = si if si.size else np.zeros(1, np.int32)
+        ui = ui if ui.size else np.zeros(1, np.int32)
+        _check(lib().fi_plan_composable(self._h, _p32(sq), _p32(sk), _p32(si), _p32(sl), sq.shape[0] - 1, _p32(uq),
+                                        _p32(uk), _p32(ui), _p32(ul), uq.shape[0] - 1, self.num_qo_heads,
+                                        self.num_kv_heads, self.head_dim, page_size, int(causal), _stream_ptr(stream)),
+               "fi_plan_composable")
 
     def run(self, q, k_pages, v_pages, o, lse, stream=None):
         _check(lib().fi_run(self._h, _dptr(q), _dptr(k_pages), _dptr(v_pages), int(k_pages.shape[0]), _dptr(o),

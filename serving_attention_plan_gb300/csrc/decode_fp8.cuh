@@ -334,7 +334,7 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
       }
     }
     named_bar_sync(1, NW * 32);
-    decode_finish_item<R, NW, S>(p, sm, ctid, q_start, kv_head, rows_valid, slot_out);
+    decode_finish_item<R, NW, S, DecodeSmemFp8<R, NW, S>, false>(p, sm, ctid, q_start, kv_head, rows_valid, slot_out);
   }
 }
 

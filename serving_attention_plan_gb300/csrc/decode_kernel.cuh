@@ -59,6 +59,9 @@ struct DecodeParams {
   const float* lse_prev;
   float* part_o;    // [slots][slot_rows][128] fp32, normalised O
   float* part_lse;  // [slots][slot_rows] fp32, log2 domain
+  const int2* ext;  // composable plans: shared-part slots each unit merges (see build_composable_plan)
+  float* def_o;     // composable plans: a unit's own state before that merge, [unit][8 rows][128]
+  float* def_lse;   //   and its log2-domain LSE, [unit][8 rows]
   uint32_t* counters;
   int32_t* err;
   long long page_stride;   // elements per page (H_kv * page_size * 128)
@@ -82,6 +85,7 @@ constexpr int kIdxDepth = 4;  // page-index prefetch distance of the bulk produc
 constexpr int kIdxSlots = 8;  // page-index ring of the LDGSTS loader (stages)
 constexpr int kRedHalf = 336; // words between the two halves of the transpose scratch
 constexpr int kRedRow = 20;   // words per lane row of the transpose scratch
+constexpr int kMaxDeferred = 64;  // deferred composable merges a CTA keeps (more are merged at once)
 
 // kMma: the tensor-core consumer needs neither the transpose scratch nor the probability buffer.
 template <int R, int NW, int S, bool kMma = false>
@@ -104,6 +108,8 @@ struct DecodeSmem {
   // first for the slot's previous stage keeps every parity wait unambiguous.
   int slot_consumed[S];
   int slot_filled[S];
+  int deferred[kMaxDeferred];  // composable plans: units whose merge with the shared states waits for the end
+  int n_deferred;
   int flag;
   int abort;
 };
@@ -320,12 +326,94 @@ __device__ __forceinline__ void load_q_rows(const DecodeParams& p, int q_start, 
   }
 }
 
+// Composable plans: the state (O, lse2) of row r of a unit merged (⊕, in list order) with the states
+// the shared part's tensor-core launch left for the same row in its slots.  That launch precedes this
+// one in the stream (chained by programmatic dependent launch), so its slots are read after
+// griddepcontrol.wait, which returns once it has completed.  Called by a whole warp for one row
+// (lane = dq): lane e reads entry e's LSE, the weights come from warp reductions, and the lanes'
+// partial outputs are loaded kMergeBatch at a time, so the slots' latencies overlap.
+constexpr int kMergeBatch = 8;
+__device__ __forceinline__ void merge_ext(const DecodeParams& p, int unit, int r, int dq, float4& O, float& lse2) {
+  const int ef = __ldg(p.units + unit * kUnitFields + 5), ec = __ldg(p.units + unit * kUnitFields + 6);
+  if (ec == 0) return;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // pass 1: the largest LSE (lanes take entries e = lane, lane + 32, ...)
+  float M = lse2;
+  for (int e = dq; e < ec; e += 32) {
+    const int2 x = __ldg(p.ext + ef + e);
+    const int row = (x.y & 0xFFFF) - kExtRowBias + r;
+    if (row >= 0 && row < (x.y >> 16)) M = fmaxf(M, __ldcg(p.part_lse + (size_t)x.x * p.slot_rows + row));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (M == -INFINITY) {
+    O = make_float4(0.f, 0.f, 0.f, 0.f);
+    lse2 = -INFINITY;
+    return;
+  }
+  const float w0 = (lse2 == -INFINITY) ? 0.f : fast_exp2(lse2 - M);
+  float L = 0.f;
+  float4 acc = make_float4(w0 * O.x, w0 * O.y, w0 * O.z, w0 * O.w);
+  for (int eb = 0; eb < ec; eb += 32) {
+    // this lane's entry of the batch of 32: its slot row and weight
+    const int e = eb + dq;
+    size_t srow = 0;
+    float w = 0.f;
+    if (e < ec) {
+      const int2 x = __ldg(p.ext + ef + e);
+      const int row = (x.y & 0xFFFF) - kExtRowBias + r;
+      if (row >= 0 && row < (x.y >> 16)) {
+        srow = (size_t)x.x * p.slot_rows + row;
+        w = fast_exp2(__ldcg(p.part_lse + srow) - M);
+      }
+    }
+    L += w;
+    const int nb = min(32, ec - eb);
+    for (int j = 0; j < nb; j += kMergeBatch) {
+      float4 a[kMergeBatch];
+      float wj[kMergeBatch];
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k) {
+        const int src = (j + k) & 31;
+        wj[k] = __shfl_sync(0xffffffffu, w, src);
+        const unsigned long long sr = __shfl_sync(0xffffffffu, (unsigned long long)srow, src);
+        a[k] = (j + k < nb && wj[k] != 0.f)
+                   ? __ldcg(reinterpret_cast<const float4*>(p.part_o + sr * kHeadDim + 4 * dq))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < kMergeBatch; ++k) {
+        acc.x += wj[k] * a[k].x;
+        acc.y += wj[k] * a[k].y;
+        acc.z += wj[k] * a[k].z;
+        acc.w += wj[k] * a[k].w;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  L += w0;
+  const float inv = 1.f / L;
+  O = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  lse2 = M + fast_log2(L);
+}
+
 // End of a work item, all NW consumer warps: merge their (O, m, l) states from shared memory in
 // warp order, then write the row (single chunk) or its partial state, and if this chunk is the
 // last of a split row to finish, contract all of the row's slots in plan order.
-template <int R, int NW, int S, class SM>
+// Composable plans (kDefer): a row that also has states of the shared part (written by the
+// concurrent tensor-core launch) is kept in the unit's deferred buffer and merged with them at the
+// end of the CTA's queue (decode_deferred_merges); with the CTA's list full it is merged at once.
+template <int R, int NW, int S, class SM, bool kDefer = true>
 __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, SM& sm, int ctid, int q_start, int kv_head,
                                                    int rows_valid, int slot_out) {
+  // one decision for all threads: read before this item changes the list
+  bool defer_ok = false;
+  if constexpr (kDefer) defer_ok = sm.n_deferred < kMaxDeferred;
+  auto keep = [&](int unit, int r, int dq, const float4& O, float lse2) {
+    *reinterpret_cast<float4*>(p.def_o + ((size_t)unit * kDecodeMaxRows + r) * kHeadDim + 4 * dq) = O;
+    if (dq == 0) p.def_lse[(size_t)unit * kDecodeMaxRows + r] = lse2;
+  };
   for (int u = ctid; u < R * 32; u += NW * 32) {
     const int r = u >> 5, dq = u & 31;
     float M = -INFINITY;
@@ -357,6 +445,13 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, SM& sm
         const int head = kv_head * p.group + r % p.group;
         const size_t orow = (size_t)tok * p.hqo + head;
         float lse_w = lse2;
+        if (slot_out <= -2) {  // composable: the shared part's states of these rows
+          if (defer_ok) {
+            keep(-slot_out - 2, r, dq, O, lse2);
+            continue;
+          }
+          merge_ext(p, -slot_out - 2, r, dq, O, lse_w);
+        }
         if (p.o_prev)
           merge_prev4(O, lse_w, *reinterpret_cast<const uint2*>(p.o_prev + orow * kHeadDim + 4 * dq), p.lse_prev[orow]);
         uint2 packed;
@@ -370,6 +465,9 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, SM& sm
         if (dq == 0) p.part_lse[srow] = lse2;
       }
     }
+  }
+  if constexpr (kDefer) {
+    if (slot_out <= -2 && defer_ok && ctid == 0) sm.deferred[sm.n_deferred++] = -slot_out - 2;
   }
 
   if (slot_out >= 0) {
@@ -387,6 +485,7 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, SM& sm
     if (sm.flag) {
       const int first = __ldg(p.units + unit * kUnitFields + U_FIRST_SLOT);
       const int n_chunks = __ldg(p.units + unit * kUnitFields + U_N_CHUNKS);
+      const bool has_ext = p.ext != nullptr && __ldg(p.units + unit * kUnitFields + 6) > 0;
       for (int u = ctid; u < R * 32; u += NW * 32) {
         const int r = u >> 5, dq = u & 31;
         if (r >= rows_valid) continue;
@@ -415,6 +514,13 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, SM& sm
         const int head = kv_head * p.group + r % p.group;
         const size_t orow = (size_t)tok * p.hqo + head;
         float lse_w = (M == -INFINITY) ? -INFINITY : M + fast_log2(L);
+        if (has_ext) {  // composable: as for single-chunk rows
+          if (defer_ok) {
+            keep(unit, r, dq, O, lse_w);
+            continue;
+          }
+          merge_ext(p, unit, r, dq, O, lse_w);
+        }
         if (p.o_prev)
           merge_prev4(O, lse_w, *reinterpret_cast<const uint2*>(p.o_prev + orow * kHeadDim + 4 * dq), p.lse_prev[orow]);
         uint2 packed;
@@ -424,9 +530,39 @@ __device__ __forceinline__ void decode_finish_item(const DecodeParams& p, SM& sm
         if (dq == 0) p.lse[orow] = lse_w * kLn2;
       }
       if (ctid == 0) p.counters[unit] = 0u;
+      if constexpr (kDefer) {
+        if (has_ext && defer_ok && ctid == 0) sm.deferred[sm.n_deferred++] = unit;
+      }
     }
   }
   named_bar_sync(1, NW * 32);
+}
+
+// Composable plans, after the CTA's last item, all NW consumer warps: wait once for the shared part's
+// launch to complete, then merge every deferred unit's rows (kept by decode_finish_item) with the
+// shared states of the same rows and write the outputs; a warp per row.
+template <int R, int NW, int S, class SM>
+__device__ __forceinline__ void decode_deferred_merges(const DecodeParams& p, SM& sm, int w) {
+  const int nd = sm.n_deferred;  // final: the last decode_finish_item ended with a barrier
+  if (nd == 0) return;
+  const int lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int task = w; task < nd * R; task += NW) {
+    const int unit = sm.deferred[task / R], r = task % R;
+    const int q_start = __ldg(p.units + unit * kUnitFields + U_Q_START);
+    const int q_len = __ldg(p.units + unit * kUnitFields + U_Q_LEN);
+    const int kv_head = __ldg(p.units + unit * kUnitFields + U_KV_HEAD);
+    if (r >= q_len * p.group) continue;
+    float4 O = __ldcg(reinterpret_cast<const float4*>(p.def_o + ((size_t)unit * kDecodeMaxRows + r) * kHeadDim) + lane);
+    float lse2 = __ldcg(p.def_lse + (size_t)unit * kDecodeMaxRows + r);
+    merge_ext(p, unit, r, lane, O, lse2);
+    const size_t orow = (size_t)(q_start + r / p.group) * p.hqo + kv_head * p.group + r % p.group;
+    uint2 packed;
+    packed.x = f2_to_bf16x2(O.x, O.y);
+    packed.y = f2_to_bf16x2(O.z, O.w);
+    *reinterpret_cast<uint2*>(p.o + orow * kHeadDim + 4 * lane) = packed;
+    if (lane == 0) p.lse[orow] = lse2 * kLn2;
+  }
 }
 
 template <int R, int NW, int S, bool kVar, bool kMs>
@@ -614,6 +750,7 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
     named_bar_sync(1, NW * 32);
     decode_finish_item<R, NW, S>(p, sm, ctid, q_start, kv_head, q_len * p.group, slot_out);
   }
+  if (p.ext) decode_deferred_merges<R, NW, S>(p, sm, w);
 }
 
 // Tensor-core consumer (warp-level m16n8k16 MMA, bf16 in, fp32 accumulate), used with the
@@ -807,6 +944,7 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
     named_bar_sync(1, NW * 32);
     decode_finish_item<R, NW, S>(p, sm, ctid, q_start, kv_head, rows_valid, slot_out);
   }
+  if (p.ext) decode_deferred_merges<R, NW, S>(p, sm, w);
 }
 
 // kMma selects the tensor-core consumer (LDGSTS loader only, whose copies it swizzles).
@@ -839,6 +977,7 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
     }
     sm.abort = 0;
     sm.flag = 0;
+    sm.n_deferred = 0;
     fence_mbar_init();
   }
   if constexpr (kMma) {

@@ -27,8 +27,11 @@ struct DecodeConfig {
   static constexpr int kStages = kMma ? 12 : (R >= 8 ? 11 : 9);
 };
 
+// pdl: launched with programmatic stream serialisation, so it may start while the previous kernel
+// on the stream (a composable plan's shared-part launch) finishes; it waits for that kernel with
+// griddepcontrol.wait before it reads the kernel's slots.
 template <int R, int kCopiers, int kFlags>
-int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream) {
+int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream, bool pdl = false) {
   constexpr bool kMma = kCopiers > 0;
   constexpr int kDecodeWarps = DecodeConfig<R, kMma>::kWarps;
   constexpr int kDecodeStages = DecodeConfig<R, kMma>::kStages;
@@ -41,7 +44,22 @@ int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream) {
     attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
   });
   if (attr_err != cudaSuccess) return record_cuda_error(attr_err, "cudaFuncSetAttribute(decode)");
-  kernel<<<grid, (kDecodeWarps + (kCopiers ? 1 + kCopiers : 1)) * 32, sizeof(Smem), stream>>>(p);
+  const unsigned threads = unsigned((kDecodeWarps + (kCopiers ? 1 + kCopiers : 1)) * 32);
+  if (pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = sizeof(Smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel launch (programmatic)");
+  }
+  kernel<<<grid, threads, sizeof(Smem), stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel launch");
 }

@@ -50,8 +50,11 @@ struct fi_workspace {
   fi::Variant variant;       // as set for the next fi_plan
   fi::Variant plan_variant;  // the one the current plan was made with (used by fi_run)
 
-  // segment byte offsets; [0, plan_bytes) is mirrored in pinned host memory
+  // segment byte offsets; [0, plan_bytes) is mirrored in pinned host memory.  The a_* segments and
+  // the ext list hold the shared part of a composable plan.
   size_t off_header = 0, off_cta = 0, off_items = 0, off_units = 0, off_slot_unit = 0, off_kv = 0, plan_bytes = 0;
+  size_t off_a_header = 0, off_a_cta = 0, off_a_items = 0, off_a_kv = 0, off_ext = 0;
+  int64_t max_ext = 0;
   size_t off_counters = 0, off_err = 0, off_part_lse = 0, off_part_o = 0, dev_bytes = 0;
   char* dbuf = nullptr;
   char* hbuf = nullptr;
@@ -59,7 +62,9 @@ struct fi_workspace {
   bool copy_pending = false;
 
   bool has_plan = false;
+  bool composable = false;
   int32_t header[fi::kHeaderLen] = {0};
+  int32_t a_header[fi::kHeaderLen] = {0};
   int32_t max_page = -1;
   int64_t plan_nnz = 0;
   int32_t plan_total_q = 0;
@@ -71,13 +76,14 @@ namespace {
 // The page layout and the attention variant are template flags, so the plain HND path compiles
 // without a trace of them.
 template <int R>
-int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream, bool var) {
+int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream, bool var, bool pdl = false) {
   using fi::kDecodeCopiers;
   constexpr int kV = fi::kDecodeVariant;
   if (p.page_shift >= 0)
-    return var ? fi::launch_decode_as<R, kDecodeCopiers, kV>(grid, p, stream)
-               : fi::launch_decode_as<R, kDecodeCopiers, 0>(grid, p, stream);
-  return var ? fi::launch_decode_as<R, 0, kV>(grid, p, stream) : fi::launch_decode_as<R, 0, 0>(grid, p, stream);
+    return var ? fi::launch_decode_as<R, kDecodeCopiers, kV>(grid, p, stream, pdl)
+               : fi::launch_decode_as<R, kDecodeCopiers, 0>(grid, p, stream, pdl);
+  return var ? fi::launch_decode_as<R, 0, kV>(grid, p, stream, pdl)
+             : fi::launch_decode_as<R, 0, 0>(grid, p, stream, pdl);
 }
 
 bool var_on(const fi::Variant& v) { return v.window_left >= 0 || v.soft_cap > 0.f; }
@@ -131,10 +137,13 @@ int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int nu
   ws->head_dim = head_dim;
   ws->num_sms = num_sms;
   ws->max_ctas = std::max(fi::kTcCtasPerSm, fi::kDecodeCtasPerSm) * num_sms;
-  // App. D.3 bound: partial tiles < 2 * #CTA, hence split rows < #CTA.
+  // App. D.3 bound: partial tiles < 2 * #CTA, hence split rows < #CTA; a composable plan's decode
+  // part adds a unit record per (request, KV head) whose rows merge shared states
   ws->max_slots = 2 * int64_t(ws->max_ctas);
-  ws->max_units = ws->max_ctas;
+  ws->max_units = ws->max_ctas + int64_t(num_kv_heads) * max_batch;
   ws->max_items = int64_t(num_kv_heads) * max_total_q + ws->max_slots;
+  // each shared slot holds 256 rows, so at most 256 per-request units list it
+  ws->max_ext = ws->max_slots * fi::kTcRows;
 
   size_t off = 0;
   auto seg = [&](size_t bytes) {
@@ -148,6 +157,11 @@ int fi_workspace_create(int max_batch, int max_total_q, int max_kv_pages, int nu
   ws->off_units = seg(sizeof(int32_t) * fi::kUnitFields * ws->max_units);
   ws->off_slot_unit = seg(sizeof(int32_t) * ws->max_slots);
   ws->off_kv = seg(sizeof(int32_t) * size_t(max_kv_pages));
+  ws->off_a_header = seg(sizeof(int32_t) * fi::kHeaderLen);
+  ws->off_a_cta = seg(sizeof(int32_t) * (ws->max_ctas + 1));
+  ws->off_a_items = seg(sizeof(int32_t) * fi::kItemFields * ws->max_items);
+  ws->off_a_kv = seg(sizeof(int32_t) * size_t(max_kv_pages));
+  ws->off_ext = seg(sizeof(int32_t) * 2 * ws->max_ext);
   ws->plan_bytes = off;
   ws->off_counters = seg(sizeof(uint32_t) * ws->max_units);
   ws->off_err = seg(sizeof(int32_t) * 4);
@@ -276,6 +290,95 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   ws->plan_nnz = nnz;
   ws->plan_total_q = qo_indptr[batch];
   ws->has_plan = true;
+  ws->composable = false;
+  ws->plan_variant = ws->variant;
+  return FI_OK;
+}
+
+int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const int32_t* shared_kv_indptr,
+                       const int32_t* shared_kv_indices, const int32_t* shared_last_page_len, int shared_batch,
+                       const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* kv_indices,
+                       const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads, int head_dim,
+                       int page_size, int causal, void* stream) {
+  if (ws == nullptr) return FI_ERR_INVALID_ARG;
+  if (num_qo_heads != ws->hqo || num_kv_heads != ws->hkv || head_dim != ws->head_dim) return FI_ERR_INVALID_ARG;
+  if (batch > ws->max_batch || shared_batch > ws->max_batch) return FI_ERR_CAPACITY;
+  const fi::Variant& var = ws->variant;
+  if (var.window_left >= 0 || var.soft_cap > 0.f || var.kv_layout != FI_KV_LAYOUT_HND ||
+      var.kv_dtype != FI_KV_DTYPE_BF16)
+    return FI_ERR_UNSUPPORTED;  // composable plans run the plain bf16 HND kernels
+  fi::PlanInput a{shared_qo_indptr, shared_kv_indptr, shared_last_page_len, shared_batch, num_qo_heads, num_kv_heads,
+                  head_dim, page_size, 0, ws->num_sms};
+  fi::PlanInput b{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size, causal,
+                  ws->num_sms};
+  int st = fi::validate_input(a);
+  if (st == FI_OK) st = fi::validate_input(b);
+  if (st != FI_OK) return st;
+  const int64_t nnz_a = shared_kv_indptr[shared_batch], nnz_b = kv_indptr[batch];
+  if (qo_indptr[batch] > ws->max_total_q || nnz_a > ws->max_kv_pages || nnz_b > ws->max_kv_pages)
+    return FI_ERR_CAPACITY;
+  if ((nnz_a > 0 && shared_kv_indices == nullptr) || (nnz_b > 0 && kv_indices == nullptr)) return FI_ERR_INVALID_ARG;
+  int32_t max_page = -1;
+  for (int64_t k = 0; k < nnz_a; ++k) {
+    if (shared_kv_indices[k] < 0) return FI_ERR_INVALID_ARG;
+    max_page = std::max(max_page, shared_kv_indices[k]);
+  }
+  for (int64_t k = 0; k < nnz_b; ++k) {
+    if (kv_indices[k] < 0) return FI_ERR_INVALID_ARG;
+    max_page = std::max(max_page, kv_indices[k]);
+  }
+  fi::ComposablePlan cp;
+  st = fi::build_composable_plan(a, b, ws->cost, &cp);
+  if (st != FI_OK) return st;
+  const fi::Plan& pa = cp.shared;
+  const fi::Plan& pb = cp.unique;
+  if (pa.header[fi::H_NUM_ITEMS] > ws->max_items || pb.header[fi::H_NUM_ITEMS] > ws->max_items ||
+      pb.header[fi::H_NUM_UNITS] > ws->max_units || pb.header[fi::H_NUM_SLOTS] > ws->max_slots ||
+      int64_t(cp.ext.size() / 2) > ws->max_ext)
+    return FI_ERR_CAPACITY;
+  // the per-request units' own states wait for the merge past the used slots of the partial region
+  if (int64_t(pb.header[fi::H_NUM_UNITS]) * fi::kDecodeMaxRows >
+      (ws->max_slots - pb.header[fi::H_NUM_SLOTS]) * int64_t(fi::kTcRows))
+    return FI_ERR_CAPACITY;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ws->copy_pending) {
+    FI_CUDA(cudaEventSynchronize(ws->copy_done));
+    ws->copy_pending = false;
+  }
+  char* h = ws->hbuf;
+  struct Seg {
+    size_t off;
+    const void* src;
+    size_t bytes;
+  } segs[] = {
+      {ws->off_header, pb.header, sizeof(pb.header)},
+      {ws->off_cta, pb.cta_indptr.data(), pb.cta_indptr.size() * sizeof(int32_t)},
+      {ws->off_items, pb.items.data(), pb.items.size() * sizeof(int32_t)},
+      {ws->off_units, pb.units.data(), pb.units.size() * sizeof(int32_t)},
+      {ws->off_slot_unit, pb.slot_unit.data(), pb.slot_unit.size() * sizeof(int32_t)},
+      {ws->off_kv, kv_indices, size_t(nnz_b) * sizeof(int32_t)},
+      {ws->off_a_header, pa.header, sizeof(pa.header)},
+      {ws->off_a_cta, pa.cta_indptr.data(), pa.cta_indptr.size() * sizeof(int32_t)},
+      {ws->off_a_items, pa.items.data(), pa.items.size() * sizeof(int32_t)},
+      {ws->off_a_kv, shared_kv_indices, size_t(nnz_a) * sizeof(int32_t)},
+      {ws->off_ext, cp.ext.data(), cp.ext.size() * sizeof(int32_t)},
+  };
+  for (const Seg& sg : segs) {
+    if (sg.bytes == 0) continue;
+    std::memcpy(h + sg.off, sg.src, sg.bytes);
+    FI_CUDA(cudaMemcpyAsync(ws->dbuf + sg.off, h + sg.off, sg.bytes, cudaMemcpyHostToDevice, s));
+  }
+  FI_CUDA(cudaEventRecord(ws->copy_done, s));
+  ws->copy_pending = true;
+  std::memcpy(ws->header, pb.header, sizeof(pb.header));
+  ws->header[fi::H_PATH] = fi::kPathComposable;
+  std::memcpy(ws->a_header, pa.header, sizeof(pa.header));
+  ws->max_page = max_page;
+  ws->plan_nnz = nnz_a + nnz_b;
+  ws->plan_total_q = qo_indptr[batch];
+  ws->has_plan = true;
+  ws->composable = true;
   ws->plan_variant = ws->variant;
   return FI_OK;
 }
@@ -300,6 +403,84 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
   const int ps = h[fi::H_PAGE_SIZE];
   const float scale_log2 = fi::kLog2e / std::sqrt(float(ws->head_dim));
   char* d = ws->dbuf;
+
+  if (ws->composable) {
+    if (o_prev != nullptr) return FI_ERR_UNSUPPORTED;
+    // 1: the shared sub-matrix on tensor-core tiles, every chunk to a slot (no contraction launch)
+    const int32_t* ha = ws->a_header;
+    if (ha[fi::H_NUM_ITEMS] > 0) {
+      fi::PrefillArgs a{};
+      a.cta_indptr = reinterpret_cast<const int32_t*>(d + ws->off_a_cta);
+      a.items = reinterpret_cast<const int32_t*>(d + ws->off_a_items);
+      a.units = reinterpret_cast<const int32_t*>(d + ws->off_units);
+      a.slot_unit = reinterpret_cast<const int32_t*>(d + ws->off_slot_unit);
+      a.kv_indices = reinterpret_cast<const int32_t*>(d + ws->off_a_kv);
+      a.q = q;
+      a.k = k_pages;
+      a.v = v_pages;
+      a.o = o;
+      a.lse = lse;
+      a.part_o = reinterpret_cast<float*>(d + ws->off_part_o);
+      a.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
+      a.header = reinterpret_cast<const int32_t*>(d + ws->off_a_header);
+      a.err = reinterpret_cast<int32_t*>(d + ws->off_err);
+      a.num_pages = num_pages;
+      a.page_size = ps;
+      a.hqo = ws->hqo;
+      a.hkv = ws->hkv;
+      a.group = ha[fi::H_GROUP];
+      a.tile_tokens = ha[fi::H_TILE_TOKENS];
+      a.total_q = ws->plan_total_q;
+      a.num_ctas = ha[fi::H_NUM_CTAS];
+      a.scale_log2 = scale_log2;
+      a.window_left = -1;
+      a.cap_log2 = 0.f;
+      a.nhd = 0;
+      a.contract = 0;
+      const int st = fi::launch_prefill(a, s);
+      if (st != FI_OK) return st;
+    }
+    // 2: the per-request rows on decode tiles; each merges its own chunks and the shared slots
+    fi::DecodeParams p{};
+    p.cta_indptr = reinterpret_cast<const int32_t*>(d + ws->off_cta);
+    p.items = reinterpret_cast<const int32_t*>(d + ws->off_items);
+    p.units = reinterpret_cast<const int32_t*>(d + ws->off_units);
+    p.slot_unit = reinterpret_cast<const int32_t*>(d + ws->off_slot_unit);
+    p.kv_indices = reinterpret_cast<const int32_t*>(d + ws->off_kv);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k_pages);
+    p.v = static_cast<const __nv_bfloat16*>(v_pages);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.part_o = reinterpret_cast<float*>(d + ws->off_part_o);
+    p.part_lse = reinterpret_cast<float*>(d + ws->off_part_lse);
+    p.ext = reinterpret_cast<const int2*>(d + ws->off_ext);
+    // deferred own states: the partial region past the plan's slots (capacity checked at plan time)
+    const size_t used_rows = size_t(h[fi::H_NUM_SLOTS]) * fi::kTcRows;
+    p.def_o = reinterpret_cast<float*>(d + ws->off_part_o) + used_rows * fi::kHeadDim;
+    p.def_lse = reinterpret_cast<float*>(d + ws->off_part_lse) + used_rows;
+    p.counters = reinterpret_cast<uint32_t*>(d + ws->off_counters);
+    p.err = reinterpret_cast<int32_t*>(d + ws->off_err);
+    p.page_stride = (long long)ws->hkv * ps * fi::kHeadDim;
+    p.head_stride = (long long)ps * fi::kHeadDim;
+    p.window_left = -1;
+    p.v_scale = 1.f;
+    p.num_pages = num_pages;
+    p.page_size = ps;
+    p.page_shift = (ps & (ps - 1)) == 0 ? __builtin_ctz(unsigned(ps)) : -1;
+    p.hqo = ws->hqo;
+    p.group = h[fi::H_GROUP];
+    p.slot_rows = fi::kTcRows;
+    p.scale_log2 = scale_log2;
+    const bool pdl = ha[fi::H_NUM_ITEMS] > 0;
+    switch (h[fi::H_ROWS_TILE]) {
+      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s, false, pdl);
+      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s, false, pdl);
+      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s, false, pdl);
+      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s, false, pdl);
+      default: return FI_ERR_UNSUPPORTED;
+    }
+  }
 
   if (h[fi::H_PATH] == fi::kPathDecode) {
     fi::DecodeParams p{};

@@ -132,7 +132,7 @@ int plan_shape(const PlanInput& in, const CostModel& cm, PlanShape* s) {
   }
 
   // a2: path and tile
-  if (max_lq * g <= kDecodeMaxRows) {
+  if (!in.force_tensor && max_lq * g <= kDecodeMaxRows) {
     s->path = kPathDecode;
     s->tile_tokens = static_cast<int>(std::max<int64_t>(1, max_lq));
     s->rows_tile = 1;
@@ -171,7 +171,7 @@ int plan_shape(const PlanInput& in, const CostModel& cm, PlanShape* s) {
   int64_t W = 0, U = 0, S = 0;
   for_each_unit(in, *s, [&](int, int, int64_t, int64_t, int64_t, int64_t, int64_t, int64_t n, int64_t) {
     W += n;
-    if (n > 1) {
+    if (n > 1 || in.all_slots) {
       U += 1;
       S += n;
     }
@@ -191,7 +191,7 @@ void plan_fill(const PlanInput& in, const CostModel& cm, const PlanShape& s, con
   for_each_unit(in, s, [&](int i, int h, int64_t q0, int64_t qn, int64_t lo_e, int64_t e, int64_t cs, int64_t n,
                            int64_t diag) {
     int32_t first_slot = -1;
-    if (n > 1) {
+    if (n > 1 || in.all_slots) {
       first_slot = static_cast<int32_t>(S);
       int32_t* u = st.units + U * kUnitFields;
       u[U_FIRST_SLOT] = first_slot;
@@ -294,6 +294,125 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
   return FI_OK;
 }
 
+int build_composable_plan(const PlanInput& shared_in, const PlanInput& unique_in, const CostModel& cm,
+                          ComposablePlan* out) {
+  if (shared_in.num_qo_heads != unique_in.num_qo_heads || shared_in.num_kv_heads != unique_in.num_kv_heads ||
+      shared_in.head_dim != unique_in.head_dim || shared_in.page_size != unique_in.page_size ||
+      shared_in.num_sms != unique_in.num_sms)
+    return FI_ERR_INVALID_ARG;
+  if (shared_in.batch < 0 || unique_in.batch < 0 || shared_in.qo_indptr == nullptr || unique_in.qo_indptr == nullptr)
+    return FI_ERR_INVALID_ARG;
+  // the shared rows are query tokens of the per-request part
+  if (shared_in.qo_indptr[shared_in.batch] > unique_in.qo_indptr[unique_in.batch]) return FI_ERR_INVALID_ARG;
+  PlanInput a = shared_in, b = unique_in;
+  a.causal = 0;  // every shared key precedes the requests' own keys: all of it is visible
+  a.window_left = -1;
+  a.force_tensor = 1;
+  a.all_slots = 1;
+  b.force_tensor = 0;
+  b.all_slots = 0;
+  int st = validate_input(a);
+  if (st == FI_OK) st = validate_input(b);
+  if (st != FI_OK) return st;
+  // split the SM budget: both parts run at once on disjoint SMs
+  int64_t keys_a = 0, keys_b = 0;
+  for (int i = 0; i < a.batch; ++i)
+    if (len_q(a, i) > 0) keys_a += int64_t(a.num_kv_heads) * len_kv(a, i);
+  for (int i = 0; i < b.batch; ++i)
+    if (len_q(b, i) > 0) keys_b += int64_t(b.num_kv_heads) * len_kv(b, i);
+  const int sms = shared_in.num_sms;
+  int n_a = sms;
+  if (sms > 1) {
+    const int64_t c_a = int64_t(kTcKeyCostNum) * keys_a, c_b = int64_t(kTcKeyCostDen) * keys_b;
+    n_a = c_a + c_b > 0 ? static_cast<int>((2 * int64_t(sms) * c_a + (c_a + c_b)) / (2 * (c_a + c_b))) : 1;
+    n_a = std::min(std::max(n_a, 1), sms - 1);
+  }
+  a.num_sms = n_a;
+  st = build_plan(a, cm, &out->shared);
+  if (st != FI_OK) return st;
+  // more shared chunks than CTAs would give some CTAs two: take as many CTAs as chunks (leaving at
+  // least one SM) and plan the shared part once more
+  // one adjustment toward one chunk per CTA: fewer chunks than CTAs leaves SMs idle, so take one
+  // CTA per chunk; more (but at most twice as many) would give some CTAs two, so take as many CTAs
+  // as chunks, leaving at least one SM
+  const int items_a = out->shared.header[H_NUM_ITEMS];
+  const int n_adj = items_a < n_a ? std::max(items_a, 1)
+                    : (sms > 1 && items_a > n_a && items_a <= 2 * n_a) ? std::min(items_a, sms - 1) : n_a;
+  if (n_adj != n_a) {
+    n_a = n_adj;
+    a.num_sms = n_a;
+    st = build_plan(a, cm, &out->shared);
+    if (st != FI_OK) return st;
+  }
+  b.num_sms = sms > 1 ? sms - n_a : 1;
+  st = build_plan(b, cm, &out->unique);
+  if (st != FI_OK) return st;
+  if (out->unique.header[H_PATH] != kPathDecode) return FI_ERR_UNSUPPORTED;  // per-request rows must be decode tiles
+  const int g = a.num_qo_heads / a.num_kv_heads;
+  const int32_t s_a = out->shared.header[H_NUM_SLOTS];
+  const int tok_a = out->shared.header[H_TILE_TOKENS];
+
+  // per-request slots come after the shared ones
+  Plan& u = out->unique;
+  for (size_t k = 0; k < u.items.size(); k += kItemFields)
+    if (u.items[k + I_SLOT] >= 0) u.items[k + I_SLOT] += s_a;
+  for (size_t k = 0; k < u.units.size(); k += kUnitFields) u.units[k + U_FIRST_SLOT] += s_a;
+  std::vector<int32_t> slot_unit(size_t(s_a), -1);
+  slot_unit.insert(slot_unit.end(), u.slot_unit.begin(), u.slot_unit.end());
+  u.slot_unit = std::move(slot_unit);
+
+  // shared units in enumeration order: block row i, KV head h, tile j
+  std::vector<int64_t> unit_base(size_t(a.batch) + 1, 0);
+  for (int i = 0; i < a.batch; ++i) {
+    const int64_t lq = int64_t(a.qo_indptr[i + 1]) - a.qo_indptr[i];
+    unit_base[i + 1] = unit_base[i] + int64_t(a.num_kv_heads) * ((lq + tok_a - 1) / tok_a);
+  }
+  const std::vector<int32_t>& ua = out->shared.units;
+  // ext entries of per-request rows [q0, q0 + qn) of KV head h: every chunk of every shared tile
+  // that holds some of those tokens, block rows and tiles in order
+  auto add_ext = [&](int32_t q0, int32_t qn, int32_t h) -> int32_t {
+    int32_t count = 0;
+    for (int i = 0; i < a.batch; ++i) {
+      const int32_t lo = std::max(q0, a.qo_indptr[i]), hi = std::min(q0 + qn, a.qo_indptr[i + 1]);
+      if (lo >= hi) continue;
+      const int64_t n_tiles = (int64_t(a.qo_indptr[i + 1]) - a.qo_indptr[i] + tok_a - 1) / tok_a;
+      const int64_t j0 = (lo - a.qo_indptr[i]) / tok_a, j1 = (hi - 1 - a.qo_indptr[i]) / tok_a;
+      for (int64_t j = j0; j <= j1; ++j) {
+        const int32_t* rec = &ua[size_t(unit_base[i] + int64_t(h) * n_tiles + j) * kUnitFields];
+        const int32_t offset = (q0 - rec[U_Q_START]) * g;
+        const int32_t packed = (offset + kExtRowBias) | ((rec[U_Q_LEN] * g) << 16);
+        for (int32_t c = 0; c < rec[U_N_CHUNKS]; ++c) {
+          out->ext.push_back(rec[U_FIRST_SLOT] + c);
+          out->ext.push_back(packed);
+          ++count;
+        }
+      }
+    }
+    return count;
+  };
+  // split units first (unit order), then single-chunk items with shared states (queue order)
+  for (size_t k = 0; k < u.units.size(); k += kUnitFields) {
+    const int32_t first = static_cast<int32_t>(out->ext.size() / 2);
+    const int32_t cnt = add_ext(u.units[k + U_Q_START], u.units[k + U_Q_LEN], u.units[k + U_KV_HEAD]);
+    u.units[k + 5] = first;
+    u.units[k + 6] = cnt;
+  }
+  for (size_t k = 0; k < u.items.size(); k += kItemFields) {
+    if (u.items[k + I_SLOT] != -1) continue;
+    const int32_t first = static_cast<int32_t>(out->ext.size() / 2);
+    const int32_t cnt = add_ext(u.items[k + I_Q_START], u.items[k + I_Q_LEN], u.items[k + I_KV_HEAD]);
+    if (cnt == 0) continue;
+    const int32_t unit = static_cast<int32_t>(u.units.size() / kUnitFields);
+    const int32_t rec[kUnitFields] = {-1, 1, u.items[k + I_Q_START], u.items[k + I_Q_LEN], u.items[k + I_KV_HEAD],
+                                      first, cnt, 0};
+    u.units.insert(u.units.end(), rec, rec + kUnitFields);
+    u.items[k + I_SLOT] = -(2 + unit);
+  }
+  u.header[H_NUM_UNITS] = static_cast<int32_t>(u.units.size() / kUnitFields);
+  u.header[H_NUM_SLOTS] = s_a + u.header[H_NUM_SLOTS];
+  return FI_OK;
+}
+
 }  // namespace fi
 
 extern "C" int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indptr, const int32_t* last_page_len,
@@ -321,5 +440,40 @@ extern "C" int fi_plan_compute(const int32_t* qo_indptr, const int32_t* kv_indpt
     if (!v->empty()) std::memcpy(o, v->data(), v->size() * sizeof(int32_t));
     o += v->size();
   }
+  return FI_OK;
+}
+
+extern "C" int fi_plan_composable_compute(const int32_t* shared_qo_indptr, const int32_t* shared_kv_indptr,
+                                          const int32_t* shared_last_page_len, int shared_batch,
+                                          const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                          const int32_t* last_page_len, int batch, int num_qo_heads, int num_kv_heads,
+                                          int head_dim, int page_size, int causal, int num_sms, int32_t* out,
+                                          int64_t capacity, int64_t* out_len) {
+  if (out_len == nullptr) return FI_ERR_INVALID_ARG;
+  fi::PlanInput a{shared_qo_indptr, shared_kv_indptr, shared_last_page_len, shared_batch, num_qo_heads, num_kv_heads,
+                  head_dim, page_size, 0, num_sms};
+  fi::PlanInput b{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size, causal,
+                  num_sms};
+  fi::ComposablePlan cp;
+  const int st = fi::build_composable_plan(a, b, fi::CostModel(), &cp);
+  if (st != FI_OK) return st;
+  const fi::Plan* parts[2] = {&cp.shared, &cp.unique};
+  int64_t need = 0;
+  for (const fi::Plan* p : parts)
+    need += fi::kHeaderLen + static_cast<int64_t>(p->cta_indptr.size() + p->items.size() + p->units.size() +
+                                                  p->slot_unit.size());
+  need += static_cast<int64_t>(cp.ext.size());
+  *out_len = need;
+  if (out == nullptr || capacity < need) return FI_ERR_CAPACITY;
+  int32_t* o = out;
+  for (const fi::Plan* p : parts) {
+    std::memcpy(o, p->header, sizeof(p->header));
+    o += fi::kHeaderLen;
+    for (const auto* v : {&p->cta_indptr, &p->items, &p->units, &p->slot_unit}) {
+      if (!v->empty()) std::memcpy(o, v->data(), v->size() * sizeof(int32_t));
+      o += v->size();
+    }
+  }
+  if (!cp.ext.empty()) std::memcpy(o, cp.ext.data(), cp.ext.size() * sizeof(int32_t));
   return FI_OK;
 }

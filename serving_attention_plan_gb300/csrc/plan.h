@@ -15,6 +15,7 @@ namespace fi {
 constexpr int kHeadDim = 128;
 constexpr int kPathDecode = 0;
 constexpr int kPathTensor = 1;
+constexpr int kPathComposable = 2;  // header[H_PATH] of a composable plan (both paths, one reduction map)
 constexpr int kTcRows = 256;          // rows of a tensor-core tile: two 128-row tcgen05 tiles sharing each KV tile
 constexpr int kTcKeys = 128;          // keys of a tensor-core KV tile
 constexpr int kDecodeMaxRows = 8;     // largest tile the CUDA-core decode path takes
@@ -55,6 +56,8 @@ struct PlanInput {
   int causal;
   int num_sms;  // SM budget; the plan's #CTA is k * num_sms with k fixed per path
   int window_left = -1;  // >= 0: sliding window (causal plans): token at position p sees keys p - w .. p
+  int force_tensor = 0;  // 1: tensor-core tiles even when every request fits a decode tile
+  int all_slots = 0;     // 1: every unit, split or not, writes its chunks' partial states to slots
 };
 
 // Attention variant of a plan (问题背景 挑战二; 核心机制 5, paper §3.2.3): a sliding window on
@@ -107,6 +110,33 @@ struct PlanStorage {
 };
 
 int plan_shape(const PlanInput& in, const CostModel& cost, PlanShape* shape);
+
+// Composable formats (核心机制 2, paper §3.1.2, Fig. 3): a shared sub-matrix (block rows such as a
+// prefix shared by a group of requests, Br = the group's query tokens) and a per-request sub-matrix
+// (Br = 1) over the same query rows, in one plan with one reduction map.  The shared part takes
+// tensor-core tiles and writes every chunk to a partial slot; the per-request part takes decode
+// tiles, its slots are numbered after the shared part's, and each of its units lists the shared
+// slots that hold states of its rows (ext: pairs {slot, packed}, packed = (row offset + 512) |
+// (rows of the shared tile << 16); the unit's row r is row `offset + r` of that slot when it lies in
+// [0, rows)).  A single-chunk unit with shared states gets a unit record too (first slot -1) and its
+// item's slot field is -(2 + unit).  Unit fields 5 and 6 hold the unit's first ext entry and count.
+constexpr int kExtRowBias = 512;
+// SM budget split of a composable plan: the shared part gets N_tc = round(num_sms * c_a / (c_a + c_b))
+// CTAs (at least 1, and at least 1 left for the other part when num_sms > 1), then set once to its
+// number of chunks when that is smaller, or larger but at most twice as large (one chunk per CTA);
+// the per-request part gets the rest; both run at once, one CTA per SM.  c_a = kTcKeyCostNum *
+// (keys the shared units see) and c_b = kTcKeyCostDen * (keys the per-request units see): a key of a
+// 256-row tensor-core tile costs about 4/3 of a decode key in SM time (measured on GB300 with the
+// shared-prefix batch: 0.025 us*SM per key on tensor-core tiles, 0.019 on decode tiles).
+constexpr int kTcKeyCostNum = 4;
+constexpr int kTcKeyCostDen = 3;
+struct ComposablePlan {
+  Plan shared;
+  Plan unique;
+  std::vector<int32_t> ext;  // [n_ext * 2]
+};
+int build_composable_plan(const PlanInput& shared, const PlanInput& unique, const CostModel& cost,
+                          ComposablePlan* out);
 void plan_fill(const PlanInput& in, const CostModel& cost, const PlanShape& shape, const PlanStorage& st,
                int32_t* header);
 

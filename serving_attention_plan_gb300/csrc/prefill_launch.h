@@ -36,6 +36,8 @@ struct PrefillArgs {
   int window_left;  // < 0: none
   float cap_log2;   // <= 0: no soft-cap; else cap * log2(e)
   int nhd;          // page layout NHD instead of HND
+  int contract = 1; // 0: no contraction kernel (a composable plan's shared part: its slots are merged
+                    // by the per-request decode launch)
 };
 
 // Returns an fi_status.

@@ -207,3 +207,56 @@ def test_key_positions_beyond_int32_items_rejected(lib):
     assert ei.value.status == 3
     kv = np.array([0, 1024]); last = np.array([1])                          # 2^30 - 2^20 + 1 keys: fine
     assert B.plan_compute(qo, kv, last, 8, 2, ps, False, 4)[0] == 0x46495031
+
+
+def _composable_case(rng):
+    """Random shared-prefix groups (tensor-core tiles) over decode requests with their own pages."""
+    g = int(rng.choice([1, 2, 4, 8]))
+    hk = int(rng.choice([1, 2, 8]))
+    ps = int(rng.choice([8, 16, 32]))
+    n_req = int(rng.integers(1, 40))
+    q_len = int(rng.integers(1, 8 // g + 1))
+    qo = np.arange(n_req + 1) * q_len
+    kv_lens = rng.integers(0, 900, size=n_req)
+    kv = np.concatenate([[0], np.cumsum((kv_lens + ps - 1) // ps)])
+    last = np.where(kv_lens > 0, kv_lens - (np.maximum((kv_lens + ps - 1) // ps, 1) - 1) * ps, 0)
+    # shared groups: contiguous runs of requests (some requests in none), each with its own prefix
+    cuts = sorted(set(rng.integers(0, n_req + 1, size=int(rng.integers(1, 4))).tolist()) | {0, n_req})
+    s_qo, s_kv, s_last = [0], [0], []
+    for lo, hi in zip(cuts[:-1], cuts[1:]):
+        if hi == lo:
+            continue
+        s_qo.append(int(qo[hi]) - int(qo[cuts[0]]) + s_qo[0])
+        plen = int(rng.integers(0, 3000))
+        s_kv.append(s_kv[-1] + (plen + ps - 1) // ps)
+        s_last.append(plen - (max((plen + ps - 1) // ps, 1) - 1) * ps if plen > 0 else 0)
+    return (np.array(s_qo), np.array(s_kv), np.array(s_last)), (qo, kv, last), g * hk, hk, ps
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_composable_plan_matches_oracle(lib, seed):
+    """Composable plans (shared sub-matrix on tensor-core tiles, per-request rows on decode tiles, one
+    reduction map with the shared slots each unit merges): C++ == restatement, bit for bit."""
+    rng = np.random.default_rng(900 + seed)
+    shared, unique, hq, hk, ps = _composable_case(rng)
+    n_cta = int(rng.choice([1, 5, 152]))
+    causal = bool(rng.integers(0, 2))
+    got = B.plan_composable_compute(shared, unique, hq, hk, ps, causal, n_cta)
+    a, b, ext = P.plan_composable(shared, unique, hq, hk, ps, causal, n_cta)
+    want = P.serialize_composable(a, b, ext)
+    assert np.array_equal(got, want)
+
+
+def test_shared_prefix_composable_plan(lib):
+    """The shared-prefix workload: 64 requests share one 8192-token prefix.  Every suffix unit lists
+    the prefix's chunk slots of its KV head, and the plan is the restatement's."""
+    sp = W.shared_prefix_decode()
+    shared = (sp.prefix.qo_indptr, sp.prefix.kv_indptr, sp.prefix.last_page_len)
+    unique = (sp.suffix.qo_indptr, sp.suffix.kv_indptr, sp.suffix.last_page_len)
+    got = B.plan_composable_compute(shared, unique, 32, 8, 16, False, 152)
+    a, b, ext = P.plan_composable(shared, unique, 32, 8, 16, False, 152)
+    assert np.array_equal(got, P.serialize_composable(a, b, ext))
+    assert a.path == P.PATH_TENSOR and b.path == P.PATH_DECODE
+    n_chunks = a.units[0]["n_chunks"]
+    assert all(u["ext_count"] == n_chunks for u in b.units)   # each suffix unit merges every prefix chunk of its head
+    assert len(ext) == len(b.units) * n_chunks

@@ -116,3 +116,110 @@ def test_run_merge_rejects_half_state():
     with pytest.raises(B.FiError) as ei:
         ws.run_merge(q, k, v, o, None, o, lse)
     assert ei.value.status == 1
+
+
+# ---- one composable plan: shared sub-matrix + per-request rows, one reduction map ----------------
+
+def composable_batch(seed, n_req, hq, hk, ps, q_len, own_range, n_groups, prefix_range, causal):
+    """Per-request rows with their own pages, plus groups of consecutive requests that share a prefix
+    (the shared sub-matrix), all pages drawn from one pool."""
+    rng = np.random.default_rng(seed)
+    own = rng.integers(own_range[0], own_range[1] + 1, size=n_req)
+    cuts = sorted(set(rng.integers(1, n_req, size=max(0, n_groups - 1)).tolist()) | {0, n_req})
+    plens = rng.integers(prefix_range[0], prefix_range[1] + 1, size=len(cuts) - 1)
+    n_shared = int(sum((int(x) + ps - 1) // ps for x in plens))
+    n_own = int(sum((int(x) + ps - 1) // ps for x in own))
+    b = W.make_paged_batch(rng, f"composable_{seed}", np.full(n_req, q_len), own, hq, hk, ps, causal,
+                           pool_pages=n_own + n_shared + 2, scale=0.7)
+    free = np.setdiff1d(np.arange(b.num_pages), b.kv_indices)
+    rng.shuffle(free)
+    s_qo, s_kv, s_last = [0], [0], []
+    for (lo, hi), plen in zip(zip(cuts[:-1], cuts[1:]), plens):
+        s_qo.append(int(b.qo_indptr[hi]))
+        n_p = (int(plen) + ps - 1) // ps
+        s_kv.append(s_kv[-1] + n_p)
+        s_last.append(int(plen) - (n_p - 1) * ps if n_p else 0)
+    shared = dataclasses.replace(b, qo_indptr=np.array(s_qo, np.int32), kv_indptr=np.array(s_kv, np.int32),
+                                 kv_indices=free[: s_kv[-1]].astype(np.int32),
+                                 last_page_len=np.array(s_last, np.int32), causal=False)
+    return shared, b
+
+
+def composable_reference(shared, unique):
+    """Oracle: each row's state over its group's shared keys ⊕ its state over its own keys."""
+    so, sl = A.batch_attention(shared)
+    po = np.zeros((unique.total_q,) + so.shape[1:])
+    pl = np.full((unique.total_q, so.shape[1]), -np.inf)
+    po[: so.shape[0]], pl[: sl.shape[0]] = so, sl
+    uo, ul = A.batch_attention(unique)
+    return A.merge_states(po, pl, uo, ul)
+
+
+def run_composable(shared, unique, num_sms=0, ws=None, dev=None):
+    from serving_attention_plan_gb300 import binding as B
+    torch = torch_mod()
+    if ws is None:
+        ws = B.Workspace(max(unique.batch_size, shared.batch_size), unique.total_q,
+                         max(int(unique.kv_indptr[-1]), int(shared.kv_indptr[-1]), 1), unique.num_qo_heads,
+                         unique.num_kv_heads, 128, num_sms)
+    q, k, v = dev if dev is not None else to_device(unique)
+    o, lse = alloc_out(unique)
+    ws.plan_composable((shared.qo_indptr, shared.kv_indptr, shared.kv_indices, shared.last_page_len),
+                       (unique.qo_indptr, unique.kv_indptr, unique.kv_indices, unique.last_page_len),
+                       unique.page_size, unique.causal)
+    ws.run(q, k, v, o, lse)
+    torch.cuda.synchronize()
+    assert ws.get_error() == 0
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ws
+
+
+def test_shared_prefix_one_plan_matches_flat_oracle():
+    """The shared-prefix workload as one composable plan (two launches): every row equals attention over
+    prefix ++ own suffix, and reruns are bit-identical."""
+    sp = W.shared_prefix_decode()
+    dev = to_device(sp.flat)
+    o, lse, ws = run_composable(sp.prefix, sp.suffix, dev=dev)
+    assert ws.info()[1] == 2
+    ro, rl = A.batch_attention(sp.flat)
+    assert_close(o, lse, ro, rl)
+    o2, l2, _ = run_composable(sp.prefix, sp.suffix, ws=ws, dev=dev)
+    assert np.array_equal(o, o2) and np.array_equal(lse, l2)
+
+
+COMPOSABLE_CASES = [
+    # (n_req, hq, hk, page, q_len, own range, groups, prefix range, causal, SM budget); the workspace holds
+    # 2 x budget partial slots, and every chunk of the shared part takes one
+    (9, 8, 2, 16, 1, (0, 300), 2, (0, 700), False, 0),
+    (20, 8, 2, 16, 1, (1, 900), 3, (100, 2000), False, 16),     # few CTAs: long shared rows split in chunks
+    (7, 8, 4, 8, 2, (2, 200), 2, (1, 400), True, 6),            # 2 query tokens (4 rows), causal own part
+    (33, 64, 8, 32, 1, (0, 500), 4, (0, 3000), False, 24),      # g = 8, page 32, empty prefixes possible
+    (5, 16, 16, 16, 4, (4, 100), 1, (50, 300), True, 10),       # g = 1, 4 tokens per request
+]
+
+
+@pytest.mark.parametrize("case", range(len(COMPOSABLE_CASES)))
+def test_composable_matches_oracle(case):
+    n_req, hq, hk, ps, ql, own, ng, pre, causal, n_sms = COMPOSABLE_CASES[case]
+    shared, unique = composable_batch(7000 + case, n_req, hq, hk, ps, ql, own, ng, pre, causal)
+    o, lse, ws = run_composable(shared, unique, num_sms=n_sms)
+    assert ws.info()[1] == 2
+    ro, rl = composable_reference(shared, unique)
+    assert_close(o, lse, ro, rl)
+
+
+def test_composable_unsupported_combinations():
+    from serving_attention_plan_gb300 import binding as B
+    shared, unique = composable_batch(7100, 6, 8, 2, 16, 1, (1, 100), 2, (10, 100), False)
+    ws = B.Workspace(8, 64, 64, 8, 2)
+    ws.set_variant(window_left=-1, logits_soft_cap=5.0)
+    with pytest.raises(B.FiError) as ei:
+        ws.plan_composable((shared.qo_indptr, shared.kv_indptr, shared.kv_indices, shared.last_page_len),
+                           (unique.qo_indptr, unique.kv_indptr, unique.kv_indices, unique.last_page_len), 16, False)
+    assert ei.value.status == 3
+    # per-request rows beyond a decode tile (here 3 tokens x g = 4 = 12 rows)
+    shared, unique = composable_batch(7101, 4, 8, 2, 16, 3, (3, 100), 1, (10, 100), True)
+    ws = B.Workspace(8, 64, 64, 8, 2)
+    with pytest.raises(B.FiError) as ei:
+        ws.plan_composable((shared.qo_indptr, shared.kv_indptr, shared.kv_indices, shared.last_page_len),
+                           (unique.qo_indptr, unique.kv_indptr, unique.kv_indices, unique.last_page_len), 16, True)
+    assert ei.value.status == 3
