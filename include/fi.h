@@ -237,7 +237,8 @@ int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const 
  * the tensor-core path they must also keep the total query count (the launch
  * holds a TMA descriptor of q whose extent is the plan's total_q).
  * Calls that share a workspace must not overlap on the GPU.
- * Errors: NO_PLAN, INVALID_ARG (null pointers, page id >= num_pages), CUDA.
+ * Errors: NO_PLAN, INVALID_ARG (null pointers, q / k_pages / v_pages not
+ * 16-byte aligned, page id >= num_pages), CUDA.
  */
 int fi_run(fi_workspace* ws, const void* q, const void* k_pages, const void* v_pages, int num_pages, void* o,
            float* lse, void* stream);
@@ -364,7 +365,8 @@ int fi_plan_composable_compute(const int32_t* shared_qo_indptr, const int32_t* s
  * and clear it with fi_decode_noalloc_get_error.
  * The first call on a device looks up the array's device address and sets the
  * kernel attribute (with that device current); make it before any stream
- * capture.  Errors: INVALID_ARG, CAPACITY (plan + page indices + slots do not
+ * capture.  Errors: INVALID_ARG (also for q / k_pages / v_pages that are not
+ * 16-byte aligned), CAPACITY (plan + page indices + slots do not
  * fit in the array), UNSUPPORTED (the batch needs tensor-core tiles, i.e. some
  * request has more than 8 rows = query tokens x group size, or a KV length
  * above 2^30), CUDA.

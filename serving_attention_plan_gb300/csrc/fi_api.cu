@@ -398,6 +398,9 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
   const bool any_rows = h[fi::H_NUM_ITEMS] > 0;
   if (any_rows && (q == nullptr || o == nullptr || lse == nullptr)) return FI_ERR_INVALID_ARG;
   if (ws->plan_nnz > 0 && (k_pages == nullptr || v_pages == nullptr)) return FI_ERR_INVALID_ARG;
+  // q, K and V rows move in 16-byte copies (and TMA boxes on the tensor-core path)
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pages) | reinterpret_cast<uintptr_t>(v_pages)) & 15)
+    return FI_ERR_INVALID_ARG;
   if (!any_rows) return FI_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int ps = h[fi::H_PAGE_SIZE];

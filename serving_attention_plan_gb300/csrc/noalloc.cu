@@ -162,6 +162,9 @@ extern "C" int fi_decode_noalloc(const int32_t* qo_indptr, const int32_t* kv_ind
   if (L.end > kNoAllocScratchBytes) return FI_ERR_CAPACITY;
   if (W > 0 && (q == nullptr || o == nullptr || lse == nullptr)) return FI_ERR_INVALID_ARG;
   if (nnz > 0 && (k_pages == nullptr || v_pages == nullptr)) return FI_ERR_INVALID_ARG;
+  // the kernel moves q, K and V rows with 16-byte copies
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pages) | reinterpret_cast<uintptr_t>(v_pages)) & 15)
+    return FI_ERR_INVALID_ARG;
 
   void* scratch = nullptr;
   st = device_setup(dev, &scratch);

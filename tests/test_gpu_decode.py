@@ -137,6 +137,35 @@ def test_out_of_range_page_rejected_on_host():
     assert ei.value.status == 1
 
 
+def test_unaligned_rows_rejected_on_host():
+    """q, K and V rows move in 16-byte copies: a base address off a 16-byte boundary is refused before
+    any launch, by fi_run and by fi_decode_noalloc."""
+    from serving_attention_plan_gb300 import binding as B
+    b = W.random_small_batch(81, batch=4, num_qo_heads=8, num_kv_heads=2, page_size=16, causal=False,
+                             kv_len_range=(16, 64))
+    q, k, v = to_device(b)
+    o, lse = alloc_out(b)
+    ws = B.Workspace(4, 4, 64, 8, 2)
+    ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 16, False)
+    torch = torch_mod()
+
+    def shifted(t):  # the same values, 8 bytes past a 16-byte boundary
+        flat = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+        out = flat[4:4 + t.numel()].view(t.shape)
+        out.copy_(t)
+        return out
+
+    q_off, k_off = shifted(q), shifted(k)
+    for qq, kk in ((q_off, k), (q, k_off)):
+        with pytest.raises(B.FiError) as ei:
+            ws.run(qq, kk, v, o, lse)
+        assert ei.value.status == 1
+    with pytest.raises(B.FiError) as ei:
+        B.decode_noalloc(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, 8, 2, 16, False, q_off, k, v, o,
+                         lse)
+    assert ei.value.status == 1
+
+
 def test_merge_states_kernel():
     torch = torch_mod()
     from serving_attention_plan_gb300 import binding as B
