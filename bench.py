@@ -523,6 +523,12 @@ def main():
         torch.distributed.destroy_process_group()
 
 
+# ncu DRAM-traffic entries (profiles/ncu_traffic.json) of the dominant kernel of each target workload
+TRAFFIC_KEYS = {"skewed_long_decode": "decode_kernel<R=8>/skewed_long_decode",
+                "ragged_causal_prefill": "prefill_kernel/ragged_causal_prefill",
+                "variant_llama3_8b_decode_fp8_e4m3": "decode_kernel_fp8<R=4>/llama3_8b_decode_fp8_e4m3"}
+
+
 def targets_summary(name, gbs, ms, hbm_peak, bf16_peak, peak_src, extra):
     """One short entry per workload (µs per batch, rate, fraction of the measured peak, the goal)."""
     r3 = lambda x: None if x is None else round(float(x), 3)
@@ -543,6 +549,8 @@ def targets_summary(name, gbs, ms, hbm_peak, bf16_peak, peak_src, extra):
                       "launches": e.get("launches_per_step")})
         elif "kv_gbs" in e:
             t.update({"GB/s": r3(e["kv_gbs"]), "frac_hbm": r3(e["frac_of_hbm_peak"])})
+        if k in TRAFFIC_KEYS:
+            t["traffic"] = ncu_traffic(TRAFFIC_KEYS[k])  # DRAM bytes of one launch (ncu), null if stale
         t["goal"] = goal
         out[k] = t
     out["peaks"] = {"hbm_gbs": hbm_peak, "bf16_tflops": bf16_peak, "source": peak_src}

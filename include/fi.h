@@ -24,6 +24,15 @@
  *     throws or exits across this boundary.  On a host-side error no output
  *     and no workspace state is changed.
  *   - head_dim must be 128.
+ *   - One workspace holds exactly one plan at a time: fi_plan and
+ *     fi_plan_composable replace it (a composable plan's shared and
+ *     per-request parts are one plan with one reduction map).  The plan, its
+ *     page-index copy, split counters and partial-output slots live in the
+ *     workspace's fixed segments, so a launch captured in a CUDA graph keeps
+ *     valid pointers across re-plans (核心机制 7, App. D.1); a second live plan
+ *     would need a second set of segments.  A caller that keeps several plans
+ *     live (e.g. the prefill and the decode batch of one step) creates one
+ *     workspace per plan.
  */
 #ifndef FI_H_
 #define FI_H_
@@ -75,8 +84,9 @@ typedef struct fi_workspace fi_workspace;
  *   num_sms         SM budget of the attention kernels; 0 selects every SM of
  *                   the device (App. E: the SMs attention may use are given by
  *                   the user).  Each path runs k persistent CTAs per SM
- *                   (App. D.3: #CTA = k * #SM): k = 1 for decode tiles, k = 2
- *                   for 128-row tensor-core tiles.
+ *                   (App. D.3: #CTA = k * #SM): k = 1 for decode tiles and for
+ *                   the 256-row tensor-core tiles (one CTA holds all 512 TMEM
+ *                   columns).
  *   out             receives the handle (owned by the caller; release with
  *                   fi_workspace_destroy)
  *
@@ -219,8 +229,11 @@ int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const 
  * the plan fixed (no atomic aggregation), so outputs are bit-identical from
  * run to run.  Decode tiles (<= 8 rows) run warp-level MMAs with the KV tokens
  * on the MMA's 16-row side (power-of-two page sizes) or CUDA cores (other page
- * sizes); 128-row tiles run on tcgen05 tensor cores (核心机制 4, paper §3.2.2).
- * A split row is merged by the last of its chunks to finish, summing the
+ * sizes); larger requests run 256-row tiles (two 128-row tcgen05 MMA tiles
+ * sharing each K/V tile) on the tensor cores (核心机制 4, paper §3.2.2).
+ * A decode split row is merged by the last of its chunks to finish; a
+ * tensor-core split row by a contraction kernel chained to the attention
+ * launch (programmatic dependent launch, one warp per row).  Both sum the
  * chunks in the plan's slot order.
  *
  *   q          DEVICE bf16 [total_q, num_qo_heads, 128]
@@ -364,8 +377,8 @@ int fi_plan_composable_compute(const int32_t* shared_qo_indptr, const int32_t* s
  * hold a device-side error word (FI_DEVERR_* bits) that calls only add to: read
  * and clear it with fi_decode_noalloc_get_error.
  * The first call on a device looks up the array's device address and sets the
- * kernel attribute (with that device current); make it before any stream
- * capture.  Errors: INVALID_ARG (also for q / k_pages / v_pages that are not
+ * kernel attribute (with that device current).
+ * Errors: INVALID_ARG (also for q / k_pages / v_pages that are not
  * 16-byte aligned), CAPACITY (plan + page indices + slots do not
  * fit in the array), UNSUPPORTED (the batch needs tensor-core tiles, i.e. some
  * request has more than 8 rows = query tokens x group size, or a KV length

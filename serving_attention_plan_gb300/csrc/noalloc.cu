@@ -21,7 +21,7 @@
 //     are serialised by a mutex;
 //   * the first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and sets the kernel's
-//     shared-memory attribute; make that first call before any stream capture.
+//     shared-memory attribute.
 #include <cuda_runtime.h>
 
 #include <algorithm>
