@@ -535,6 +535,7 @@ def targets_summary(name, gbs, ms, hbm_peak, bf16_peak, peak_src, extra):
     out = {name: {"us": r3(ms * 1e3), "GB/s": r3(gbs), "frac_hbm": r3(gbs / hbm_peak), "goal": ">=0.75 hbm"}}
     goals = {"skewed_long_decode": ">=0.75 hbm", "ragged_causal_prefill": ">=0.50 bf16",
              "shared_prefix_decode": "reported", "variant_llama3_8b_decode_fp8_e4m3": "reported",
+             "variant_ragged_causal_prefill_fp8_e4m3": "reported",
              "tiny_decode": "latency"}
     for k, goal in goals.items():
         e = extra.get(k)
@@ -542,8 +543,9 @@ def targets_summary(name, gbs, ms, hbm_peak, bf16_peak, peak_src, extra):
             out[k] = {"error": (e or {}).get("error", "not run")}
             continue
         t = {"us": r3(e["us_per_batch"])}
-        if "tflops" in e:
-            t.update({"TFLOP/s": r3(e["tflops"]), "frac_bf16": r3(e["frac_of_bf16_peak"])})
+        if "tflops" in e or "tflops_visible_pairs" in e:
+            t.update({"TFLOP/s": r3(e.get("tflops", e.get("tflops_visible_pairs"))),
+                      "frac_bf16": r3(e["frac_of_bf16_peak"])})
         elif "kv_gbs_unique" in e:
             t.update({"GB/s_unique_kv": r3(e["kv_gbs_unique"]), "frac_hbm": r3(e["frac_of_hbm_peak"]),
                       "launches": e.get("launches_per_step")})
@@ -563,6 +565,7 @@ VARIANT_WORKLOADS = {
     "variant_ragged_causal_prefill_window1024_softcap50": ("ragged_causal_prefill",
                                                             dict(window_left=1024, logits_soft_cap=50.0)),
     "variant_llama3_8b_decode_fp8_e4m3": ("llama3_8b_decode", dict(kv_dtype=("e4m3", 0.5, 0.5))),
+    "variant_ragged_causal_prefill_fp8_e4m3": ("ragged_causal_prefill", dict(kv_dtype=("e4m3", 0.25, 0.25))),
 }
 
 
@@ -652,10 +655,11 @@ def bench_other(name, torch, dev, hbm_peak, bf16_peak, steps=200, warmup=10):
 
 
 def path_name(w, hdr) -> str:
-    """Which kernel body the plan runs: 128-row tiles on tcgen05, or <= 8-row decode tiles whose
-    consumer is warp-level MMA (16-byte-copy loader, power-of-two pages) or CUDA cores (bulk loader)."""
+    """Which kernel body the plan runs: 256-row items (two 128-row MMA tiles) on tcgen05, or <= 8-row
+    decode tiles whose consumer is warp-level MMA (16-byte-copy loader, power-of-two pages) or CUDA
+    cores (bulk loader)."""
     if hdr[1] == 1:
-        return "128-row tiles, tcgen05"
+        return "256-row items, tcgen05"
     ps = int(w.page_size)
     return f"{int(hdr[3])}-row tiles, " + ("mma.sync" if ps & (ps - 1) == 0 else "CUDA cores")
 

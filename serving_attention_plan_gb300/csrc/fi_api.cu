@@ -246,9 +246,10 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
   if (st != FI_OK) return st;
   // NHD decode reads page rows with the 16-byte-copy loader (power-of-two pages); its kernels are
   // instantiated for 1, 2, 4, 8 and 16 KV heads
-  // e4m3 pages: decode tiles, power-of-two pages (the FP8 kernel's loader)
-  if (ws->variant.kv_dtype == FI_KV_DTYPE_E4M3 &&
-      (plan.header[fi::H_PATH] != fi::kPathDecode || (page_size & (page_size - 1)) != 0))
+  // e4m3 pages on decode tiles: power-of-two pages (the FP8 decode kernel's loader); tensor-core
+  // tiles widen e4m3 pages in their producer and take the page sizes of bf16 pages
+  if (ws->variant.kv_dtype == FI_KV_DTYPE_E4M3 && plan.header[fi::H_PATH] == fi::kPathDecode &&
+      (page_size & (page_size - 1)) != 0)
     return FI_ERR_UNSUPPORTED;
   if (ws->variant.kv_layout == FI_KV_LAYOUT_NHD && plan.header[fi::H_PATH] == fi::kPathDecode &&
       ((page_size & (page_size - 1)) != 0 || (num_kv_heads & (num_kv_heads - 1)) != 0 || num_kv_heads > 16))
@@ -304,9 +305,10 @@ int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const 
   if (num_qo_heads != ws->hqo || num_kv_heads != ws->hkv || head_dim != ws->head_dim) return FI_ERR_INVALID_ARG;
   if (batch > ws->max_batch || shared_batch > ws->max_batch) return FI_ERR_CAPACITY;
   const fi::Variant& var = ws->variant;
-  if (var.window_left >= 0 || var.soft_cap > 0.f || var.kv_layout != FI_KV_LAYOUT_HND ||
-      var.kv_dtype != FI_KV_DTYPE_BF16)
-    return FI_ERR_UNSUPPORTED;  // composable plans run the plain bf16 HND kernels
+  if (var.window_left >= 0 || var.soft_cap > 0.f || var.kv_layout != FI_KV_LAYOUT_HND)
+    return FI_ERR_UNSUPPORTED;  // composable plans run the plain HND kernels (bf16 or e4m3 pages)
+  if (var.kv_dtype == FI_KV_DTYPE_E4M3 && (page_size & (page_size - 1)) != 0)
+    return FI_ERR_UNSUPPORTED;  // the per-request rows' FP8 decode loader wants power-of-two pages
   fi::PlanInput a{shared_qo_indptr, shared_kv_indptr, shared_last_page_len, shared_batch, num_qo_heads, num_kv_heads,
                   head_dim, page_size, 0, ws->num_sms};
   fi::PlanInput b{qo_indptr, kv_indptr, last_page_len, batch, num_qo_heads, num_kv_heads, head_dim, page_size, causal,
@@ -436,6 +438,11 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
       a.total_q = ws->plan_total_q;
       a.num_ctas = ha[fi::H_NUM_CTAS];
       a.scale_log2 = scale_log2;
+      if (ws->plan_variant.kv_dtype == FI_KV_DTYPE_E4M3) {
+        a.fp8 = 1;
+        a.scale_log2 *= ws->plan_variant.k_scale;
+        a.v_scale = ws->plan_variant.v_scale;
+      }
       a.window_left = -1;
       a.cap_log2 = 0.f;
       a.nhd = 0;
@@ -475,6 +482,13 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     p.group = h[fi::H_GROUP];
     p.slot_rows = fi::kTcRows;
     p.scale_log2 = scale_log2;
+    if (ws->plan_variant.kv_dtype == FI_KV_DTYPE_E4M3) {
+      // the FP8 decode kernel merges each row's shared slots as it finishes the row (no deferred
+      // merges) and starts after the shared part's launch has completed (stream order)
+      p.scale_log2 *= ws->plan_variant.k_scale;
+      p.v_scale = ws->plan_variant.v_scale;
+      return fi::launch_decode_fp8(h[fi::H_ROWS_TILE], false, h[fi::H_NUM_CTAS], p, s);
+    }
     const bool pdl = ha[fi::H_NUM_ITEMS] > 0;
     switch (h[fi::H_ROWS_TILE]) {
       case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s, false, pdl);
@@ -564,6 +578,11 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
   a.window_left = ws->plan_variant.window_left;
   a.cap_log2 = ws->plan_variant.soft_cap > 0.f ? ws->plan_variant.soft_cap * fi::kLog2e : 0.f;
   a.nhd = ws->plan_variant.kv_layout == FI_KV_LAYOUT_NHD ? 1 : 0;
+  if (ws->plan_variant.kv_dtype == FI_KV_DTYPE_E4M3) {
+    a.fp8 = 1;
+    a.scale_log2 *= ws->plan_variant.k_scale;  // logits of the stored codes, scaled back to K
+    a.v_scale = ws->plan_variant.v_scale;
+  }
   return fi::launch_prefill(a, s);
 }
 

@@ -1,5 +1,5 @@
-// Tensor-core tile path: paged-KV attention for 128-row tiles on tcgen05, fused
-// with the merge of split-KV partial states.
+// Tensor-core tile path: paged-KV attention for 256-row work items on tcgen05, with the merge of
+// split-KV partial states.
 //
 // Page "FlashInfer：面向 LLM 推理服务的高效可定制注意力引擎":
 //   核心机制 3-4 (paper §3.2, §3.2.2): query tiles of >= 16 rows run on tensor
@@ -45,6 +45,12 @@
 // Online softmax in base 2 with a lazy rescale: O and l are rescaled only when a row's running
 // maximum grows by more than 8 (a factor 256), which keeps exp2 arguments <= 8 and changes the
 // result only by rounding.
+// FP8 (e4m3) KV pages (核心机制 8, paper App. F: the KV-cache in fp8, queries and outputs in 16-bit
+// floats): each page's code rows land by TMA, unswizzled, in the second 64-dim half of the stage;
+// the producer warp then widens them in place to the bf16 layout above (e4m3 -> f16 -> f32 -> the
+// upper 16 bits, exact: a code has at most 3 mantissa bits) and releases the stage to the MMA with
+// a second barrier.  K = k_scale * code is folded into the logit scale, V = v_scale * code into
+// the epilogue's 1 / l, so the MMAs and the softmax are the bf16 ones.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -102,7 +108,8 @@ struct PrefillParams {
   int group;
   int slot_rows;
   uint32_t q_tile_bytes;  // bytes of one Q tile as TMA writes it (2 halves x rows x 128 B)
-  float scale_log2;
+  float scale_log2;  // includes k_scale with e4m3 pages
+  float v_scale;     // 1 for bf16 pages
   int window_left;   // >= 0: a row at key position p sees keys p - window_left .. p
   float cap_log2;    // > 0: logit soft-cap in the log2 domain, s -> cap_log2 * tanh(s / cap_log2)
 };
@@ -114,6 +121,7 @@ struct PrefillSmem {
   float stat_m[2][kItemRows];        // [item parity][row]: running max at the end of the item
   float stat_l[2][kItemRows];        // [item parity][row]: row sum
   uint64_t q_full, q_empty, k_full[kKvStages], k_empty[kKvStages], v_full[kKvStages], v_empty[kKvStages];
+  uint64_t k_ready[kKvStages], v_ready[kKvStages];     // e4m3 pages: the stage widened to bf16
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // [half][S buffer]
   uint64_t o_free[2];                                   // per half of the item
   uint64_t stat_full[2], stat_empty[2];                  // per item parity
@@ -142,7 +150,51 @@ struct Item {
 // ---------------------------------------------------------------------------------------------
 // warps 12 (K and the item's Q) and 13 (V): TMA producers
 // ---------------------------------------------------------------------------------------------
-template <bool kNhd, bool kIsK>
+// Two e4m3 codes (bits 0-15) -> bf16x2, exactly: e4m3 -> f16 is exact, f16 -> f32 is exact, and the
+// f32 of a code has at most 3 mantissa bits, so its upper 16 bits are the bf16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+  uint32_t h;
+  const uint16_t v = static_cast<uint16_t>(two_codes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  float lo, hi;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<uint16_t>(h)));
+  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<uint16_t>(h >> 16)));
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+}
+
+// e4m3 pages: the stage's 128 keys x 128 codes arrived as 128-byte rows in its second 64-dim half;
+// rewrite them as bf16 in the MMA layout [2 dim halves][128 keys][128 B] (16-byte chunk c of row r
+// at position c ^ (r % 8)).  Eight lanes take one row, one 16-byte chunk of codes each; a row is
+// read whole before any lane writes, and writes go only to that row's place in each half (the
+// second half's row is the staged row itself), so rows never overlap.
+__device__ __forceinline__ void widen_stage(uint8_t* stage, int lane) {
+  const int c = lane & 7;  // staged chunk: dims 16c .. 16c + 15
+  const uint32_t base = smem_u32(stage);
+  const uint32_t half_off = uint32_t(c >> 2) * kHalfBytes;
+  const int m = (2 * c) & 7;  // output chunks m, m + 1 of that half
+#pragma unroll 4
+  for (int i = 0; i < kTile / 4; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    uint32_t w0, w1, w2, w3;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                 : "r"(base + kHalfBytes + uint32_t(r * 128 + 16 * c))
+                 : "memory");
+    __syncwarp();
+    const uint32_t row = base + half_off + uint32_t(r * 128);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + uint32_t(((m ^ (r & 7)) << 4))),
+                 "r"(e4m3x2_to_bf16x2(w0)), "r"(e4m3x2_to_bf16x2(w0 >> 16)), "r"(e4m3x2_to_bf16x2(w1)),
+                 "r"(e4m3x2_to_bf16x2(w1 >> 16))
+                 : "memory");
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + uint32_t((((m + 1) ^ (r & 7)) << 4))),
+                 "r"(e4m3x2_to_bf16x2(w2)), "r"(e4m3x2_to_bf16x2(w2 >> 16)), "r"(e4m3x2_to_bf16x2(w3)),
+                 "r"(e4m3x2_to_bf16x2(w3 >> 16))
+                 : "memory");
+    __syncwarp();
+  }
+}
+
+template <bool kNhd, bool kIsK, bool kFp8>
 __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_kv,
                          int begin, int end) {
   const int lane = threadIdx.x & 31;
@@ -152,8 +204,21 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
   uint8_t* ring = kIsK ? &sm.k[0][0] : &sm.v[0][0];
   uint64_t* full = kIsK ? sm.k_full : sm.v_full;
   uint64_t* empty = kIsK ? sm.k_empty : sm.v_empty;
+  uint64_t* ready = kIsK ? sm.k_ready : sm.v_ready;
   int tt = 0, nq = 0;  // KV tiles and Q tiles issued
+  int nw = 0;          // e4m3: tiles widened (one behind the loads, so a load is in flight while widening)
   bool ok = true;
+  // e4m3: wait for tile nw's codes, widen them, hand the stage to the MMA issuer
+  auto widen_next = [&]() {
+    const int st = nw % kKvStages;
+    ok = __all_sync(kFull, mbar_wait(&full[st], (nw / kKvStages) & 1, p.err, &sm.abort));
+    if (!ok) return;
+    widen_stage(ring + st * kTileBytes, lane);
+    fence_proxy_async_smem();  // the MMAs read the widened tile through the async proxy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ready[st]);
+    ++nw;
+  };
   for (int pos = begin; pos < end && ok; ++pos) {
     Item it;
     it.load(p.items, pos);
@@ -174,17 +239,29 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
           }
         }
       }
+      // e4m3: widen the previous tile before waiting for this one's stage, so the widening
+      // overlaps the MMAs of the tile before it
+      if constexpr (kFp8) {
+        if (nw < tt) widen_next();
+        if (!ok) break;
+      }
       const int st = tt % kKvStages;
       if (tt >= kKvStages)
         ok = __all_sync(kFull, mbar_wait(&empty[st], ((tt / kKvStages) - 1) & 1, p.err, &sm.abort));
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], kTileBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], kFp8 ? kTileBytes / 2 : kTileBytes);
       __syncwarp();
       if (lane < ppt) {
-        // one page of one KV head: HND box (64 dims, page_size tokens, 1 page-head), NHD box
-        // (64 dims, 1 head, page_size tokens, 1 page)
         uint8_t* dst = ring + st * kTileBytes + lane * ps * 128;
-        if constexpr (kNhd) {
+        if constexpr (kFp8) {
+          // one page of one KV head, 128 codes a row, into the second half (unswizzled)
+          if constexpr (kNhd)
+            tc::tma_load_4d(dst + kHalfBytes, tm_kv, 0, it.kv_head, 0, z, &full[st]);
+          else
+            tc::tma_load_3d(dst + kHalfBytes, tm_kv, 0, 0, z, &full[st]);
+        } else if constexpr (kNhd) {
+          // one page of one KV head: HND box (64 dims, page_size tokens, 1 page-head), NHD box
+          // (64 dims, 1 head, page_size tokens, 1 page)
           tc::tma_load_4d(dst, tm_kv, 0, it.kv_head, 0, z, &full[st]);
           tc::tma_load_4d(dst + kHalfBytes, tm_kv, 64, it.kv_head, 0, z, &full[st]);
         } else {
@@ -209,6 +286,9 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
       }
     }
   }
+  if constexpr (kFp8) {
+    while (ok && nw < tt) widen_next();
+  }
   // never leave with tensor copies still landing in this CTA's shared memory
   if constexpr (kIsK) {
     if (nq > 0) mbar_wait_bounded(&sm.q_full, (nq - 1) & 1);
@@ -221,7 +301,9 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
 // dependency between them goes through a barrier (S_h free = the half's last P.V done; P_h ready
 // = the softmax's arrivals), so each thread's waits overlap the other's issue.
 // ---------------------------------------------------------------------------------------------
+template <bool kFp8>
 __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  uint64_t* k_in = kFp8 ? sm.k_ready : sm.k_full;  // e4m3: the widened stage
   constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kSub, 0, 0);  // A = Q_h (K-major), B = K rows (K-major)
   const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k[0]);
   int tt = 0, uu = 0, nq = 0;  // K/V tiles, sub-tiles, items
@@ -233,7 +315,7 @@ __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem
     if (!mbar_wait(&sm.q_full, nq & 1, p.err, &sm.abort)) return;
     for (int t = 0; t < n_tiles; ++t, ++tt) {
       const int ks_ = tt % kKvStages;
-      if (!mbar_wait(&sm.k_full[ks_], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
+      if (!mbar_wait(&k_in[ks_], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
       for (int sub = 0; sub < 2 && 2 * t + sub < n_sub; ++sub, ++uu) {
         const int b = uu & 1;
 #pragma unroll
@@ -265,7 +347,9 @@ __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem
   }
 }
 
+template <bool kFp8>
 __device__ void pv_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
+  uint64_t* v_in = kFp8 ? sm.v_ready : sm.v_full;
   constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P_h (TMEM), B = V (MN-major)
   const uint32_t v_addr = smem_u32(sm.v[0]);
   int tt = 0, uu = 0, nq = 0;
@@ -276,7 +360,7 @@ __device__ void pv_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem
     if (n_tiles == 0) continue;
     for (int t = 0; t < n_tiles; ++t, ++tt) {
       const int vs = tt % kKvStages;
-      if (!mbar_wait(&sm.v_full[vs], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
+      if (!mbar_wait(&v_in[vs], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
       for (int sub = 0; sub < 2 && 2 * t + sub < n_sub; ++sub, ++uu) {
         const int b = uu & 1;
         const bool first = t == 0 && sub == 0;
@@ -494,7 +578,7 @@ __device__ void epilogue_group(const PrefillParams& p, PrefillSmem& sm, uint32_t
       float lse2 = -INFINITY, inv = 0.f;
       if (l2[h] > 0.f) {
         lse2 = m2[h] + fast_log2(l2[h]);
-        inv = 1.f / l2[h];
+        inv = p.v_scale / l2[h];  // V = v_scale * code with e4m3 pages
       }
       const bool live = n_tiles > 0;
       if (live) alive = alive && __all_sync(kFull, mbar_wait(&sm.pv_done[h][last & 1], (last >> 1) & 1, p.err, &sm.abort));
@@ -575,7 +659,7 @@ __device__ void epilogue_group(const PrefillParams& p, PrefillSmem& sm, uint32_t
   }
 }
 
-template <bool kWin, bool kCap, bool kNhd>
+template <bool kWin, bool kCap, bool kNhd, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -594,6 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.k_empty[b], 1);
       mbar_init(&sm.v_full[b], 1);
       mbar_init(&sm.v_empty[b], 1);
+      mbar_init(&sm.k_ready[b], 1);
+      mbar_init(&sm.v_ready[b], 1);
     }
     for (int h = 0; h < 2; ++h) {
       for (int b = 0; b < 2; ++b) {
@@ -636,13 +722,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     tc::regs_decrease<kControlRegs>();
     if (warp == 12) {
-      producer<kNhd, true>(p, sm, &tm_q, &tm_k, begin, end);
+      producer<kNhd, true, kFp8>(p, sm, &tm_q, &tm_k, begin, end);
     } else if (warp == 13) {
-      producer<kNhd, false>(p, sm, &tm_q, &tm_v, begin, end);
+      producer<kNhd, false, kFp8>(p, sm, &tm_q, &tm_v, begin, end);
     } else if (warp == 14 && (threadIdx.x & 31) == 0) {
-      qk_issuer(p, sm, tmem, begin, end);
+      qk_issuer<kFp8>(p, sm, tmem, begin, end);
     } else if (warp == 15 && (threadIdx.x & 31) == 0) {
-      pv_issuer(p, sm, tmem, begin, end);
+      pv_issuer<kFp8>(p, sm, tmem, begin, end);
     }
   }
   tc::fence_before_sync();
@@ -763,15 +849,29 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t d1, uint64_t d2, uint64
 }
 
 // NHD pages [pages, page_size, H_kv, 128]: dims (dim, head, token in page, page); a box is 64 dims
-// of one head and one page, i.e. page_size rows of 128 B, as the HND box lands.
-bool make_map_nhd(CUtensorMap* m, const void* base, uint64_t hkv, uint64_t page_size, uint64_t pages) {
-  const uint64_t row = uint64_t(kHeadDim) * 2;
+// of one head and one page, i.e. page_size rows of 128 B, as the HND box lands.  e4m3 pages (one
+// byte an element): a box is all 128 dims of a row, unswizzled, so it also lands as 128-B rows.
+bool make_map_nhd(CUtensorMap* m, const void* base, uint64_t hkv, uint64_t page_size, uint64_t pages, bool e4m3) {
+  const uint64_t row = uint64_t(kHeadDim) * (e4m3 ? 1 : 2);
   const cuuint64_t dims[4] = {uint64_t(kHeadDim), hkv, page_size, pages};
   const cuuint64_t strides[3] = {row, row * hkv, row * hkv * page_size};
-  const cuuint32_t box[4] = {64u, 1u, uint32_t(page_size), 1u};
+  const cuuint32_t box[4] = {e4m3 ? 128u : 64u, 1u, uint32_t(page_size), 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return encode_fn()(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     e4m3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// e4m3 HND pages: (dim, token in page, page * H_kv + head) with 1-byte elements; a box is one
+// page-head, page_size rows of 128 codes, unswizzled.
+bool make_map_e4m3(CUtensorMap* m, const void* base, uint64_t page_size, uint64_t page_heads) {
+  const cuuint64_t dims[3] = {uint64_t(kHeadDim), page_size, page_heads};
+  const cuuint64_t strides[2] = {uint64_t(kHeadDim), uint64_t(kHeadDim) * page_size};
+  const cuuint32_t box[3] = {128u, uint32_t(page_size), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -794,8 +894,12 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   // k, v: (dim, token in page, page * H_kv + head); a box is one page-head half
   const uint64_t page_heads = uint64_t(a.num_pages) * a.hkv;
   if (a.nhd) {
-    if (!make_map_nhd(&tk, a.k, uint64_t(a.hkv), uint64_t(a.page_size), uint64_t(a.num_pages)) ||
-        !make_map_nhd(&tv, a.v, uint64_t(a.hkv), uint64_t(a.page_size), uint64_t(a.num_pages)))
+    if (!make_map_nhd(&tk, a.k, uint64_t(a.hkv), uint64_t(a.page_size), uint64_t(a.num_pages), a.fp8 != 0) ||
+        !make_map_nhd(&tv, a.v, uint64_t(a.hkv), uint64_t(a.page_size), uint64_t(a.num_pages), a.fp8 != 0))
+      return FI_ERR_INVALID_ARG;
+  } else if (a.fp8) {
+    if (!make_map_e4m3(&tk, a.k, uint64_t(a.page_size), page_heads) ||
+        !make_map_e4m3(&tv, a.v, uint64_t(a.page_size), page_heads))
       return FI_ERR_INVALID_ARG;
   } else if (!make_map(&tk, a.k, uint64_t(a.page_size), page_heads, row_bytes, row_bytes * a.page_size,
                        uint32_t(a.page_size), 1u) ||
@@ -825,21 +929,29 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.slot_rows = kTcRows;
   p.q_tile_bytes = uint32_t(2 * 128 * a.group * a.tile_tokens);
   p.scale_log2 = a.scale_log2;
+  p.v_scale = a.v_scale;
   p.window_left = a.window_left;
   p.cap_log2 = a.cap_log2;
 
   const size_t smem = sizeof(PrefillSmem) + 1024;
-  // window, soft-cap and page layout are template flags: the plain HND kernel carries none of them
+  // window, soft-cap, page layout and e4m3 pages are template flags: the plain bf16 HND kernel
+  // carries none of them
   using Kernel = void (*)(PrefillParams, CUtensorMap, CUtensorMap, CUtensorMap);
-  const Kernel kernels[8] = {prefill_kernel<false, false, false>, prefill_kernel<false, false, true>,
-                             prefill_kernel<false, true, false>,  prefill_kernel<false, true, true>,
-                             prefill_kernel<true, false, false>,  prefill_kernel<true, false, true>,
-                             prefill_kernel<true, true, false>,   prefill_kernel<true, true, true>};
-  const Kernel kernel = kernels[(a.window_left >= 0 ? 4 : 0) + (a.cap_log2 > 0.f ? 2 : 0) + (a.nhd ? 1 : 0)];
+  const Kernel kernels[16] = {
+      prefill_kernel<false, false, false, false>, prefill_kernel<false, false, true, false>,
+      prefill_kernel<false, true, false, false>,  prefill_kernel<false, true, true, false>,
+      prefill_kernel<true, false, false, false>,  prefill_kernel<true, false, true, false>,
+      prefill_kernel<true, true, false, false>,   prefill_kernel<true, true, true, false>,
+      prefill_kernel<false, false, false, true>,  prefill_kernel<false, false, true, true>,
+      prefill_kernel<false, true, false, true>,   prefill_kernel<false, true, true, true>,
+      prefill_kernel<true, false, false, true>,   prefill_kernel<true, false, true, true>,
+      prefill_kernel<true, true, false, true>,    prefill_kernel<true, true, true, true>};
+  const Kernel kernel = kernels[(a.fp8 ? 8 : 0) + (a.window_left >= 0 ? 4 : 0) + (a.cap_log2 > 0.f ? 2 : 0) +
+                                (a.nhd ? 1 : 0)];
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [&] {
-    for (int i = 0; i < 8 && attr == cudaSuccess; ++i)
+    for (int i = 0; i < 16 && attr == cudaSuccess; ++i)
       attr = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   });
   if (attr != cudaSuccess) return record_cuda_error(attr, "cudaFuncSetAttribute(prefill_kernel)");

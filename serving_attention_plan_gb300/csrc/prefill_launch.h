@@ -32,7 +32,9 @@ struct PrefillArgs {
   int tile_tokens;
   int total_q;   // rows of q / o (capacity of the workspace)
   int num_ctas;
-  float scale_log2;
+  float scale_log2;  // with e4m3 pages: times k_scale
+  float v_scale = 1.f;  // e4m3 pages: V = v_scale * code
+  int fp8 = 0;          // K and V pages hold e4m3 codes
   int window_left;  // < 0: none
   float cap_log2;   // <= 0: no soft-cap; else cap * log2(e)
   int nhd;          // page layout NHD instead of HND
