@@ -120,11 +120,26 @@ struct StageCursorT {
   int pos, end;
   int st, nst;
   int page_base, kv_head, kv_lo, kv_hi;
+  // fields of item `pre`, read one item ahead so that crossing into the next item does not wait for
+  // a load in the loader's loop
+  int pre = -1;
+  int4 pa = {0, 0, 0, 0}, pb = {0, 0, 0, 0};
 
   __device__ __forceinline__ bool load(const int32_t* items) {
     while (pos < end) {
-      const int4 a = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields));
-      const int4 b = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields + 4));
+      int4 a, b;
+      if (pre == pos) {
+        a = pa;
+        b = pb;
+      } else {
+        a = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields));
+        b = __ldg(reinterpret_cast<const int4*>(items + size_t(pos) * kItemFields + 4));
+      }
+      if (pos + 1 < end) {
+        pa = __ldg(reinterpret_cast<const int4*>(items + size_t(pos + 1) * kItemFields));
+        pb = __ldg(reinterpret_cast<const int4*>(items + size_t(pos + 1) * kItemFields + 4));
+        pre = pos + 1;
+      }
       page_base = a.x;
       kv_head = a.w;
       kv_lo = b.x;
@@ -777,31 +792,51 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
   int stage_n = 0;
   bool alive = true;
 
+  // B fragments of Q^T for an item: row gq, dims 16ks + 2qd (+1) and 16ks + 8 + 2qd (+1); rows past
+  // the item's rows are zero
+  auto load_q = [&](const int4& a, uint32_t (&dst)[8][2]) {
+    const int r = gq;
+    if (r < R && r < a.z * p.group) {
+      const int tok = a.y + r / p.group;
+      const int head = a.w * p.group + r % p.group;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((size_t)tok * p.hqo + head) * kHeadDim);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        dst[ks][0] = __ldg(qrow + 8 * ks + qd);
+        dst[ks][1] = __ldg(qrow + 8 * ks + 4 + qd);
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) dst[ks][0] = dst[ks][1] = 0u;
+    }
+  };
+  // The next item's fields are read when an item starts and its query rows as soon as this warp has
+  // issued its last stage of the current item, so both loads overlap the end-of-item merge instead of
+  // stalling the next item's first stage (the copier warps stop when the ring is full).
+  int4 na = make_int4(0, 0, 0, 0), nb = make_int4(0, 0, 0, 0);
+  uint32_t qn[8][2];
+  if (begin < end) {
+    na = __ldg(reinterpret_cast<const int4*>(p.items + size_t(begin) * kItemFields));
+    nb = __ldg(reinterpret_cast<const int4*>(p.items + size_t(begin) * kItemFields + 4));
+    load_q(na, qn);
+  }
+
   for (int pos = begin; pos < end; ++pos) {
-    const int4 ia = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields));
-    const int4 ib = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos) * kItemFields + 4));
+    const int4 ia = na, ib = nb;
     const int q_start = ia.y, q_len = ia.z, kv_head = ia.w;
     const int kv_lo = ib.x, kv_hi = ib.y, diag = ib.z, slot_out = ib.w;
     const int nst = (kv_hi - kv_lo + kStageTokens - 1) / kStageTokens;
     const int rows_valid = q_len * p.group;
-
-    // B fragments of Q^T: row gq, dims 16ks + 2qd (+1) and 16ks + 8 + 2qd (+1)
     uint32_t qb[8][2];
-    {
-      const int r = gq;
-      if (r < R && r < rows_valid) {
-        const int tok = q_start + r / p.group;
-        const int head = kv_head * p.group + r % p.group;
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((size_t)tok * p.hqo + head) * kHeadDim);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          qb[ks][0] = __ldg(qrow + 8 * ks + qd);
-          qb[ks][1] = __ldg(qrow + 8 * ks + 4 + qd);
-        }
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) qb[ks][0] = qb[ks][1] = 0u;
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      qb[ks][0] = qn[ks][0];
+      qb[ks][1] = qn[ks][1];
+    }
+    const bool more = pos + 1 < end;
+    if (more) {
+      na = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos + 1) * kItemFields));
+      nb = __ldg(reinterpret_cast<const int4*>(p.items + size_t(pos + 1) * kItemFields + 4));
     }
     float o[8][4];
 #pragma unroll
@@ -918,6 +953,7 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
       }
     }
     stage_n += nst;
+    if (more) load_q(na, qn);  // lands while the item's states are merged
 
     // ---- merge the NW warp states of this item --------------------------------
 #pragma unroll
