@@ -148,8 +148,8 @@ int fi_workspace_set_variant(fi_workspace* ws, int32_t window_left, float logits
  * layout (HND or NHD) and q and o stay bf16.  Decode tiles compute in f16 MMAs
  * with fp32 accumulation and need a power-of-two page size (NHD pages, as for
  * bf16, also a power-of-two H_kv of at most 16).  Tensor-core tiles widen the
- * codes to bf16 in shared memory (exactly) and run their bf16 MMAs; they take
- * the page sizes of bf16 pages.  Composable plans (fi_plan_composable) take
+ * codes to f16 in shared memory (exactly), convert q to f16 there and run f16
+ * MMAs; they take the page sizes of bf16 pages.  Composable plans (fi_plan_composable) take
  * e4m3 HND pages of a power-of-two size.  fi_plan returns UNSUPPORTED
  * otherwise.  NaN codes in the pages give undefined rows.  Errors: INVALID_ARG.
  */

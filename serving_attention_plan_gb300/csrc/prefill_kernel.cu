@@ -47,10 +47,11 @@
 // result only by rounding.
 // FP8 (e4m3) KV pages (核心机制 8, paper App. F: the KV-cache in fp8, queries and outputs in 16-bit
 // floats): each page's code rows land by TMA, unswizzled, in the second 64-dim half of the stage;
-// the producer warp then widens them in place to the bf16 layout above (e4m3 -> f16 -> f32 -> the
-// upper 16 bits, exact: a code has at most 3 mantissa bits) and releases the stage to the MMA with
-// a second barrier.  K = k_scale * code is folded into the logit scale, V = v_scale * code into
-// the epilogue's 1 / l, so the MMAs and the softmax are the bf16 ones.
+// the producer warp then widens them in place to f16 in the layout above (one conversion per two
+// codes, exact) and releases the stage to the MMA with a second barrier.  The MMAs then run on f16
+// operands: the two producer warps convert each item's Q tile from bf16 to f16 in place once it has
+// landed, and the softmax writes P as f16.  K = k_scale * code is folded into the logit scale and
+// V = v_scale * code into the epilogue's 1 / l.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -121,7 +122,8 @@ struct PrefillSmem {
   float stat_m[2][kItemRows];        // [item parity][row]: running max at the end of the item
   float stat_l[2][kItemRows];        // [item parity][row]: row sum
   uint64_t q_full, q_empty, k_full[kKvStages], k_empty[kKvStages], v_full[kKvStages], v_empty[kKvStages];
-  uint64_t k_ready[kKvStages], v_ready[kKvStages];     // e4m3 pages: the stage widened to bf16
+  uint64_t k_ready[kKvStages], v_ready[kKvStages];     // e4m3 pages: the stage widened to f16
+  uint64_t q_ready;                                    // e4m3 pages: the item's Q converted to f16
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2];  // [half][S buffer]
   uint64_t o_free[2];                                   // per half of the item
   uint64_t stat_full[2], stat_empty[2];                  // per item parity
@@ -150,23 +152,27 @@ struct Item {
 // ---------------------------------------------------------------------------------------------
 // warps 12 (K and the item's Q) and 13 (V): TMA producers
 // ---------------------------------------------------------------------------------------------
-// Two e4m3 codes (bits 0-15) -> bf16x2, exactly: e4m3 -> f16 is exact, f16 -> f32 is exact, and the
-// f32 of a code has at most 3 mantissa bits, so its upper 16 bits are the bf16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+// Two e4m3 codes (bits 0-15) -> f16x2 (code of bits 0-7 in the low half), exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t h;
   const uint16_t v = static_cast<uint16_t>(two_codes);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
-  float lo, hi;
-  asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(static_cast<uint16_t>(h)));
-  asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(static_cast<uint16_t>(h >> 16)));
-  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+  return h;
+}
+
+// Two floats -> f16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t f2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // e4m3 pages: the stage's 128 keys x 128 codes arrived as 128-byte rows in its second 64-dim half;
-// rewrite them as bf16 in the MMA layout [2 dim halves][128 keys][128 B] (16-byte chunk c of row r
-// at position c ^ (r % 8)).  Eight lanes take one row, one 16-byte chunk of codes each; a row is
-// read whole before any lane writes, and writes go only to that row's place in each half (the
-// second half's row is the staged row itself), so rows never overlap.
+// rewrite them as f16 in the MMA layout [2 dim halves][128 keys][128 B] (16-byte chunk c of row r
+// at position c ^ (r % 8)).  Eight lanes take one row, one 16-byte chunk of codes each, so each
+// shared-memory phase reads one whole row without bank conflicts; a row is read whole before any
+// lane writes, and writes go only to that row's place in each half (the second half's row is the
+// staged row itself), so rows never overlap.
 __device__ __forceinline__ void widen_stage(uint8_t* stage, int lane) {
   const int c = lane & 7;  // staged chunk: dims 16c .. 16c + 15
   const uint32_t base = smem_u32(stage);
@@ -183,14 +189,38 @@ __device__ __forceinline__ void widen_stage(uint8_t* stage, int lane) {
     __syncwarp();
     const uint32_t row = base + half_off + uint32_t(r * 128);
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + uint32_t(((m ^ (r & 7)) << 4))),
-                 "r"(e4m3x2_to_bf16x2(w0)), "r"(e4m3x2_to_bf16x2(w0 >> 16)), "r"(e4m3x2_to_bf16x2(w1)),
-                 "r"(e4m3x2_to_bf16x2(w1 >> 16))
+                 "r"(e4m3x2_to_f16x2(w0)), "r"(e4m3x2_to_f16x2(w0 >> 16)), "r"(e4m3x2_to_f16x2(w1)),
+                 "r"(e4m3x2_to_f16x2(w1 >> 16))
                  : "memory");
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(row + uint32_t((((m + 1) ^ (r & 7)) << 4))),
-                 "r"(e4m3x2_to_bf16x2(w2)), "r"(e4m3x2_to_bf16x2(w2 >> 16)), "r"(e4m3x2_to_bf16x2(w3)),
-                 "r"(e4m3x2_to_bf16x2(w3 >> 16))
+                 "r"(e4m3x2_to_f16x2(w2)), "r"(e4m3x2_to_f16x2(w2 >> 16)), "r"(e4m3x2_to_f16x2(w3)),
+                 "r"(e4m3x2_to_f16x2(w3 >> 16))
                  : "memory");
     __syncwarp();
+  }
+}
+
+// e4m3 pages: rows 128 h .. 128 h + 127 of the item's Q (both 64-dim halves), bf16 -> f16 in place
+// (element positions unchanged, so the swizzle is unchanged).  A bf16 value is exactly a float
+// whose low 16 bits are zero; f16 keeps it exactly within f16's normal range.
+__device__ __forceinline__ void q_to_f16(uint8_t* q, int h, int lane) {
+#pragma unroll 1
+  for (int kh = 0; kh < 2; ++kh) {
+    const uint32_t base = smem_u32(q + kh * kQHalfBytes + h * kHalfBytes);
+#pragma unroll 4
+    for (int i = lane; i < kHalfBytes / 16; i += 32) {
+      uint32_t w[4];
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                   : "r"(base + uint32_t(16 * i))
+                   : "memory");
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = f2_to_f16x2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(base + uint32_t(16 * i)), "r"(w[0]), "r"(w[1]),
+                   "r"(w[2]), "r"(w[3])
+                   : "memory");
+    }
   }
 }
 
@@ -207,7 +237,19 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
   uint64_t* ready = kIsK ? sm.k_ready : sm.v_ready;
   int tt = 0, nq = 0;  // KV tiles and Q tiles issued
   int nw = 0;          // e4m3: tiles widened (one behind the loads, so a load is in flight while widening)
+  int nqc = 0;         // e4m3: Q tiles converted
   bool ok = true;
+  // e4m3: once item nqc's Q has landed, convert this warp's half of its rows to f16 (K warp rows
+  // 0-127, V warp rows 128-255) for the f16 MMAs
+  auto convert_q = [&]() {
+    ok = __all_sync(kFull, mbar_wait(&sm.q_full, nqc & 1, p.err, &sm.abort));
+    if (!ok) return;
+    q_to_f16(sm.q, kIsK ? 0 : 1, lane);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.q_ready);
+    ++nqc;
+  };
   // e4m3: wait for tile nw's codes, widen them, hand the stage to the MMA issuer
   auto widen_next = [&]() {
     const int st = nw % kKvStages;
@@ -240,7 +282,8 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
         }
       }
       // e4m3: widen the previous tile before waiting for this one's stage, so the widening
-      // overlaps the MMAs of the tile before it
+      // overlaps the MMAs of the tile before it (issuing this tile's load first, when its stage is
+      // already free, measured slower)
       if constexpr (kFp8) {
         if (nw < tt) widen_next();
         if (!ok) break;
@@ -282,7 +325,12 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
             tc::tma_load_3d(sm.q + kQHalfBytes, tm_q, 64, it.kv_head * p.group, it.q_start, &sm.q_full);
           }
           ++nq;
+          if constexpr (kFp8) convert_q();
+          if (!ok) break;
         }
+      } else if constexpr (kFp8) {
+        if (t == 0) convert_q();
+        if (!ok) break;
       }
     }
   }
@@ -304,7 +352,9 @@ __device__ void producer(const PrefillParams& p, PrefillSmem& sm, const CUtensor
 template <bool kFp8>
 __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
   uint64_t* k_in = kFp8 ? sm.k_ready : sm.k_full;  // e4m3: the widened stage
-  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kTile, kSub, 0, 0);  // A = Q_h (K-major), B = K rows (K-major)
+  uint64_t* q_in = kFp8 ? &sm.q_ready : &sm.q_full;  // e4m3: Q converted to f16
+  // A = Q_h (K-major), B = K rows (K-major); f16 operands with e4m3 pages
+  constexpr uint32_t idesc_qk = kFp8 ? tc::idesc_f16_f32(kTile, kSub, 0, 0) : tc::idesc_bf16_f32(kTile, kSub, 0, 0);
   const uint32_t q_addr = smem_u32(sm.q), k_addr = smem_u32(sm.k[0]);
   int tt = 0, uu = 0, nq = 0;  // K/V tiles, sub-tiles, items
   for (int pos = begin; pos < end; ++pos) {
@@ -312,7 +362,7 @@ __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem
     it.load(p.items, pos);
     const int n_tiles = it.tiles(), n_sub = it.subs();
     if (n_tiles == 0) continue;
-    if (!mbar_wait(&sm.q_full, nq & 1, p.err, &sm.abort)) return;
+    if (!mbar_wait(q_in, nq & 1, p.err, &sm.abort)) return;
     for (int t = 0; t < n_tiles; ++t, ++tt) {
       const int ks_ = tt % kKvStages;
       if (!mbar_wait(&k_in[ks_], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
@@ -350,7 +400,8 @@ __device__ void qk_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem
 template <bool kFp8>
 __device__ void pv_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end) {
   uint64_t* v_in = kFp8 ? sm.v_ready : sm.v_full;
-  constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kTile, kTile, 0, 1);  // A = P_h (TMEM), B = V (MN-major)
+  // A = P_h (TMEM), B = V (MN-major); f16 operands with e4m3 pages
+  constexpr uint32_t idesc_pv = kFp8 ? tc::idesc_f16_f32(kTile, kTile, 0, 1) : tc::idesc_bf16_f32(kTile, kTile, 0, 1);
   const uint32_t v_addr = smem_u32(sm.v[0]);
   int tt = 0, uu = 0, nq = 0;
   for (int pos = begin; pos < end; ++pos) {
@@ -423,7 +474,7 @@ __device__ __forceinline__ float tanh_fast(float x) {
 
 // One 64-key sub-tile of half h: scores -> (soft-cap) -> mask keys outside [lo, lim) -> online
 // softmax update -> P into the first 32 columns of the sub-tile's S buffer.
-template <bool kMasked, bool kCap>
+template <bool kMasked, bool kCap, bool kF16>
 __device__ __forceinline__ void softmax_sub(const uint32_t t_s, const uint32_t t_o, int lo, int lim, float scale,
                                             float& m, float& l, bool first, PrefillSmem& sm, uint64_t* pv_done,
                                             int pv_parity, const PrefillParams& p, bool& alive) {
@@ -473,7 +524,7 @@ __device__ __forceinline__ void softmax_sub(const uint32_t t_s, const uint32_t t
     const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[2 * j]), __uint_as_float(s[2 * j + 1])), sc2, nm2);
     const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
     sum4[j & 3] = __fadd2_rn(sum4[j & 3], pp);
-    s[j] = f2_to_bf16x2(pp.x, pp.y);  // P overwrites the front of S in place
+    s[j] = kF16 ? f2_to_f16x2(pp.x, pp.y) : f2_to_bf16x2(pp.x, pp.y);  // P overwrites the front of S in place
   }
   const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
   const float2 s0123 = __fadd2_rn(s01, s23);
@@ -498,7 +549,7 @@ __device__ __forceinline__ void softmax_sub(const uint32_t t_s, const uint32_t t
 }
 
 // Softmax warpgroup of half h (rows 128 h .. 128 h + 127 of each item).
-template <bool kWin, bool kCap>
+template <bool kWin, bool kCap, bool kF16>
 __device__ void softmax_group(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem, int begin, int end, int h) {
   const int r = threadIdx.x & (kTile - 1);  // == TMEM lane
   const int row = h * kTile + r;             // row of the item
@@ -528,9 +579,9 @@ __device__ void softmax_group(const PrefillParams& p, PrefillSmem& sm, uint32_t 
         uint64_t* prev_pv = &sm.pv_done[h][b ^ 1];
         const int prev_parity = ((uu - 1) >> 1) & 1;
         if (__all_sync(kFull, lim >= kSub && lo <= 0))
-          softmax_sub<false, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, prev_pv, prev_parity, p, alive);
+          softmax_sub<false, kCap, kF16>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, prev_pv, prev_parity, p, alive);
         else
-          softmax_sub<true, kCap>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, prev_pv, prev_parity, p, alive);
+          softmax_sub<true, kCap, kF16>(t_s, t_o, lo, lim, scale, m, l, t == 0, sm, prev_pv, prev_parity, p, alive);
         tc::fence_before_sync();
       }
       __syncwarp();
@@ -673,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.q_ready, 2);  // one arrival per producer warp
     for (int b = 0; b < kKvStages; ++b) {
       mbar_init(&sm.k_full[b], 1);
       mbar_init(&sm.k_empty[b], 1);
@@ -713,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicOr(p.err, FI_DEVERR_TMEM);
   } else if (warp < 8) {
     tc::regs_increase<kSoftmaxRegs>();
-    softmax_group<kWin, kCap>(p, sm, tmem, begin, end, warp >> 2);
+    softmax_group<kWin, kCap, kFp8>(p, sm, tmem, begin, end, warp >> 2);
   } else if (warp < 12) {
     static_assert(kEpilogueRegs < 128 && kControlRegs < 128 && kSoftmaxRegs > 128,
                   "setmaxnreg.inc only raises and setmaxnreg.dec only lowers the launch count (128)");

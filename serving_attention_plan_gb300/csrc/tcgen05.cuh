@@ -88,6 +88,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn, in
          | (uint32_t(m >> 4) << 24);    // M / 16
 }
 
+// The same with f16 A/B.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, int a_mn, int b_mn) {
+  return (1u << 4)                      // D format f32
+         | (uint32_t(a_mn) << 15)       // A major (A and B format 0: f16)
+         | (uint32_t(b_mn) << 16)       // B major
+         | (uint32_t(n >> 3) << 17)     // N / 8
+         | (uint32_t(m >> 4) << 24);    // M / 16
+}
+
 // D (TMEM) [+]= A (smem) * B (smem)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {

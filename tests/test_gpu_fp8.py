@@ -91,7 +91,7 @@ TC_CASES = [
 
 @pytest.mark.parametrize("case", range(len(TC_CASES)))
 def test_fp8_tensor_core_parity(case):
-    """e4m3 pages on 256-row tensor-core tiles: the producer widens each K/V tile to bf16 in shared
+    """e4m3 pages on 256-row tensor-core tiles: the producer widens each K/V tile to f16 in shared
     memory, and the kernel's result matches the oracle over the decoded codes."""
     hq, hk, ps, qr, kr, causal, n_sms, ks, vs, window, cap, layout = TC_CASES[case]
     b = W.random_small_batch(5200 + case, batch=5, num_qo_heads=hq, num_kv_heads=hk, page_size=ps, causal=causal,
