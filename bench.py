@@ -132,6 +132,9 @@ class Case:
         self.ws.run(self.q, self.k, self.v, self.o, self.lse)
 
 
+E2E_CONTEXTS = 3  # workspaces / streams the end-to-end steps rotate through
+
+
 def time_launches(torch, fn, steps, warmup, barrier=None):
     """Device time of `steps` back-to-back calls (CUDA events on the current stream), after warm-up."""
     for _ in range(warmup):
@@ -425,16 +428,16 @@ def main():
         e2e_step()
     serial_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
 
-    # The same steps pipelined: two workspaces, each with its own q/o/lse buffers and stream.
-    # Step i runs on context i % 2; before reusing a context the host waits for its previous
-    # step's completion event, i.e. for that step's o and lse to be in host memory.
+    # The same steps pipelined: E2E_CONTEXTS workspaces, each with its own q/o/lse buffers and
+    # stream.  Step i runs on context i % E2E_CONTEXTS; before reusing a context the host waits for
+    # its previous step's completion event, i.e. for that step's o and lse to be in host memory.
     from serving_attention_plan_gb300 import binding as B
 
     class _Ctx:
         pass
 
     ctxs = []
-    for _ in range(2):
+    for _ in range(E2E_CONTEXTS):
         c = _Ctx()
         c.ws = B.Workspace(b.batch_size, b.total_q, int(b.kv_indptr[-1]), b.num_qo_heads, b.num_kv_heads,
                            b.head_dim)
@@ -444,7 +447,7 @@ def main():
         ctxs.append(c)
 
     def e2e_step_pipelined(i):
-        c = ctxs[i % 2]
+        c = ctxs[i % E2E_CONTEXTS]
         if c.busy:
             c.done.synchronize()
         c.ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.page_size, b.causal, stream=c.stream)
@@ -501,7 +504,7 @@ def main():
                      "algorithmic_bytes_per_launch": abytes},
         "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "pipelining": "2 workspaces / 2 streams", "outputs_equal_serial": e2e_same,
+                "pipelining": f"{E2E_CONTEXTS} workspaces / {E2E_CONTEXTS} streams", "outputs_equal_serial": e2e_same,
                 "serial_ms_per_step": serial_ms,
                 "serial_value": world * nbytes / (serial_ms * 1e-3) / 1e9},
         "breakdown": {"plan_host_us_median": float(np.median(plan_us)), "graph_replay_us": graph_ms * 1e3,
