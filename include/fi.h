@@ -246,7 +246,10 @@ int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const 
  *   lse        DEVICE float32 [total_q, num_qo_heads]     (written)
  *
  * Every row of o/lse that the plan covers is written; a row that sees no key
- * gets o = 0, lse = -inf.  Asynchronous on `stream`; capturable in a CUDA
+ * gets o = 0, lse = -inf.  Asynchronous on `stream`.  A decode-tile launch is
+ * made a programmatic dependent of the previous kernel on the stream: its CTAs
+ * may set up shared memory while that kernel drains, and read no global memory
+ * before it has completed.  Capturable in a CUDA
  * graph, and a captured launch stays valid for later plans of the same
  * workspace that keep the same path and tile (fi_plan_info header[1..3]); on
  * the tensor-core path they must also keep the total query count (the launch

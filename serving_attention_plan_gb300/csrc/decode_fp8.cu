@@ -15,7 +15,7 @@ template <int R>
 constexpr int kFp8Stages = R >= 8 ? 11 : 12;
 
 template <int R, bool kNhd>
-int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream) {
+int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream, bool pdl) {
   using Smem = DecodeSmemFp8<R, kFp8Warps, kFp8Stages<R>>;
   static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
   auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers, kNhd>;
@@ -25,24 +25,39 @@ int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream) {
     attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
   });
   if (attr_err != cudaSuccess) return record_cuda_error(attr_err, "cudaFuncSetAttribute(decode fp8)");
-  kernel<<<grid, (kFp8Warps + 1 + kDecodeCopiers) * 32, sizeof(Smem), stream>>>(p);
+  const unsigned threads = (kFp8Warps + 1 + kDecodeCopiers) * 32;
+  if (pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = sizeof(Smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel_fp8 launch (programmatic)");
+  }
+  kernel<<<grid, threads, sizeof(Smem), stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel_fp8 launch");
 }
 
 }  // namespace
 
-int launch_decode_fp8(int rows_tile, bool nhd, int grid, const DecodeParams& p, cudaStream_t stream) {
+int launch_decode_fp8(int rows_tile, bool nhd, int grid, const DecodeParams& p, cudaStream_t stream, bool pdl) {
   if (p.page_shift < 0) return FI_ERR_UNSUPPORTED;
   switch (rows_tile * 2 + (nhd ? 1 : 0)) {
-    case 2: return launch_fp8_rows<1, false>(grid, p, stream);
-    case 3: return launch_fp8_rows<1, true>(grid, p, stream);
-    case 4: return launch_fp8_rows<2, false>(grid, p, stream);
-    case 5: return launch_fp8_rows<2, true>(grid, p, stream);
-    case 8: return launch_fp8_rows<4, false>(grid, p, stream);
-    case 9: return launch_fp8_rows<4, true>(grid, p, stream);
-    case 16: return launch_fp8_rows<8, false>(grid, p, stream);
-    case 17: return launch_fp8_rows<8, true>(grid, p, stream);
+    case 2: return launch_fp8_rows<1, false>(grid, p, stream, pdl);
+    case 3: return launch_fp8_rows<1, true>(grid, p, stream, pdl);
+    case 4: return launch_fp8_rows<2, false>(grid, p, stream, pdl);
+    case 5: return launch_fp8_rows<2, true>(grid, p, stream, pdl);
+    case 8: return launch_fp8_rows<4, false>(grid, p, stream, pdl);
+    case 9: return launch_fp8_rows<4, true>(grid, p, stream, pdl);
+    case 16: return launch_fp8_rows<8, false>(grid, p, stream, pdl);
+    case 17: return launch_fp8_rows<8, true>(grid, p, stream, pdl);
     default: return FI_ERR_UNSUPPORTED;
   }
 }

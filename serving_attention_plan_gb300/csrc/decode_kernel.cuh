@@ -77,6 +77,9 @@ struct DecodeParams {
   float cap_log2;   // > 0: logit soft-cap in the log2 domain, s -> cap_log2 * tanh(s / cap_log2)
   float inv_cap_log2;
   float v_scale;  // FP8 pages: V = v_scale * e4m3 code (the K scale is folded into scale_log2)
+  // 1: launched as a programmatic dependent of the previous kernel on the stream, which may still be
+  // running: the CTA sets up its shared memory, then waits for that kernel before any global read
+  int wait_prior;
 };
 
 
@@ -1000,6 +1003,9 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S, kMma>*>(smem_raw);
   const int warp = threadIdx.x >> 5;
+  // a following launch made dependent on this one may start its own set-up as SMs free up; it waits
+  // for this grid before it reads memory
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       sm.slot_consumed[s] = s - S;
@@ -1025,6 +1031,7 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
     }
   }
   __syncthreads();
+  if (p.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp >= kLoaders) {

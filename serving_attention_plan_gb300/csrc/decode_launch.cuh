@@ -28,8 +28,10 @@ struct DecodeConfig {
 };
 
 // pdl: launched with programmatic stream serialisation, so it may start while the previous kernel
-// on the stream (a composable plan's shared-part launch) finishes; it waits for that kernel with
-// griddepcontrol.wait before it reads the kernel's slots.
+// on the stream finishes: with p.wait_prior it waits for that kernel before its first global read
+// (a plain run: only its shared-memory set-up overlaps); without (a composable plan's per-request
+// part, whose only reads of the previous kernel's output are the shared slots) it waits with
+// griddepcontrol.wait before it reads those slots.
 template <int R, int kCopiers, int kFlags>
 int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream, bool pdl = false) {
   constexpr bool kMma = kCopiers > 0;
@@ -66,10 +68,14 @@ int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream, bool 
 
 // NHD decode (16-byte-copy loader): the page-row stride H_kv * 128 is a compile-time constant of
 // the kernel (a run-time stride in its copy loop measured a third slower), so the kernel is
-// instantiated per rows-per-tile and per log2(H_kv) in 0..4.  Returns an fi_status.
-int launch_decode_nhd(int rows_tile, int log2_heads, int grid, const DecodeParams& p, cudaStream_t stream);
+// instantiated per rows-per-tile and per log2(H_kv) in 0..4.  pdl as for launch_decode_as.
+// Returns an fi_status.
+int launch_decode_nhd(int rows_tile, int log2_heads, int grid, const DecodeParams& p, cudaStream_t stream,
+                      bool pdl = false);
 
-// FP8 (e4m3) KV pages, HND layout, 16-byte-copy loader (power-of-two pages).  Returns an fi_status.
-int launch_decode_fp8(int rows_tile, bool nhd, int grid, const DecodeParams& p, cudaStream_t stream);
+// FP8 (e4m3) KV pages, HND or NHD layout, 16-byte-copy loader (power-of-two pages).  pdl as for
+// launch_decode_as.  Returns an fi_status.
+int launch_decode_fp8(int rows_tile, bool nhd, int grid, const DecodeParams& p, cudaStream_t stream,
+                      bool pdl = false);
 
 }  // namespace fi

@@ -281,9 +281,23 @@ int fi_plan(fi_workspace* ws, const int32_t* qo_indptr, const int32_t* kv_indptr
       {ws->off_slot_unit, plan.slot_unit.size() * sizeof(int32_t)},
       {ws->off_kv, size_t(nnz) * sizeof(int32_t)},
   };
+  // adjacent segments go up in one copy when the unused capacity between them is small (it goes up
+  // too, and nothing reads it): fewer copy calls on the host path of every step
+  constexpr size_t kMergeGap = 16 << 10;
+  size_t run_off = 0, run_end = 0;  // the pending copy [run_off, run_end)
   for (const Seg& sg : segs) {
-    if (sg.bytes) FI_CUDA(cudaMemcpyAsync(ws->dbuf + sg.off, h + sg.off, sg.bytes, cudaMemcpyHostToDevice, s));
+    if (sg.bytes == 0) continue;
+    if (run_end > run_off && sg.off - run_end <= kMergeGap) {
+      run_end = sg.off + sg.bytes;
+      continue;
+    }
+    if (run_end > run_off)
+      FI_CUDA(cudaMemcpyAsync(ws->dbuf + run_off, h + run_off, run_end - run_off, cudaMemcpyHostToDevice, s));
+    run_off = sg.off;
+    run_end = sg.off + sg.bytes;
   }
+  if (run_end > run_off)
+    FI_CUDA(cudaMemcpyAsync(ws->dbuf + run_off, h + run_off, run_end - run_off, cudaMemcpyHostToDevice, s));
   FI_CUDA(cudaEventRecord(ws->copy_done, s));
   ws->copy_pending = true;
   std::memcpy(ws->header, plan.header, sizeof(plan.header));
@@ -532,19 +546,23 @@ int fi_run_merge(fi_workspace* ws, const void* q, const void* k_pages, const voi
     p.group = h[fi::H_GROUP];
     p.slot_rows = fi::kTcRows;
     p.scale_log2 = scale_log2;
+    // launched as a programmatic dependent: the CTAs set up their shared memory while the previous
+    // kernel on the stream drains, then wait for it before the first global read
+    p.wait_prior = 1;
     if (var.kv_dtype == FI_KV_DTYPE_E4M3) {  // every field above is set before this launch
       p.scale_log2 *= var.k_scale;           // logits of the stored codes, scaled back to K
       p.v_scale = var.v_scale;
-      return fi::launch_decode_fp8(h[fi::H_ROWS_TILE], nhd, h[fi::H_NUM_CTAS], p, s);
+      return fi::launch_decode_fp8(h[fi::H_ROWS_TILE], nhd, h[fi::H_NUM_CTAS], p, s, true);
     }
     const bool variant = var_on(var);
     if (nhd)
-      return fi::launch_decode_nhd(h[fi::H_ROWS_TILE], __builtin_ctz(unsigned(ws->hkv)), h[fi::H_NUM_CTAS], p, s);
+      return fi::launch_decode_nhd(h[fi::H_ROWS_TILE], __builtin_ctz(unsigned(ws->hkv)), h[fi::H_NUM_CTAS], p, s,
+                                   true);
     switch (h[fi::H_ROWS_TILE]) {
-      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s, variant);
-      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s, variant);
-      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s, variant);
-      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s, variant);
+      case 1: return launch_decode<1>(h[fi::H_NUM_CTAS], p, s, variant, true);
+      case 2: return launch_decode<2>(h[fi::H_NUM_CTAS], p, s, variant, true);
+      case 4: return launch_decode<4>(h[fi::H_NUM_CTAS], p, s, variant, true);
+      case 8: return launch_decode<8>(h[fi::H_NUM_CTAS], p, s, variant, true);
       default: return FI_ERR_UNSUPPORTED;
     }
   }

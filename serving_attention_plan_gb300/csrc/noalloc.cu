@@ -60,6 +60,7 @@ static int32_t g_order[kMaxItems];
 static int32_t g_cta_of[kMaxItems];
 static int32_t g_count[kMaxCtas];
 static std::pair<int64_t, int32_t> g_heap[kMaxCtas];
+static uint64_t g_key[kMaxItems > kMaxCtas ? kMaxItems : kMaxCtas];
 static unsigned char g_stage[kNoAllocScratchBytes];
 static std::mutex g_mutex;
 
@@ -177,7 +178,7 @@ extern "C" int fi_decode_noalloc(const int32_t* qo_indptr, const int32_t* kv_ind
   int32_t header[fi::kHeaderLen];
   fi::PlanStorage ps{reinterpret_cast<int32_t*>(h + L.cta), reinterpret_cast<int32_t*>(h + L.items),
                      reinterpret_cast<int32_t*>(h + L.units), reinterpret_cast<int32_t*>(h + L.slot_unit),
-                     nullptr, g_work, g_cost, g_order, g_cta_of, g_count, g_heap};
+                     nullptr, g_work, g_cost, g_order, g_cta_of, g_count, g_heap, g_key};
   fi::plan_fill(in, cm, shape, ps, header);
   std::memcpy(h + L.header, header, sizeof(header));
   if (nnz) std::memcpy(h + L.kv, kv_indices, sizeof(int32_t) * size_t(nnz));

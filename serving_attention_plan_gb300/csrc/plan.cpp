@@ -82,10 +82,14 @@ void for_each_unit(const PlanInput& in, const PlanShape& s, Visit&& visit) {
         extent(in, i, q0, qn, &lo_e, &e);
         const int64_t diag = in.causal ? lkv - lq + q0 : kNotCausalDiag;
         int64_t n = 1, cs = 0;
-        if (e - lo_e > 0) {
-          n = ceil_div(e - lo_e, s.l_chunk);
-          cs = ceil_div(ceil_div(e - lo_e, n), ps) * ps;
-          n = ceil_div(e - lo_e, cs);
+        const int64_t ext = e - lo_e;
+        if (ext > 0 && ext <= s.l_chunk) {
+          // one chunk (the common case; the general rule below gives the same n and cs)
+          cs = (ps & (ps - 1)) == 0 ? (ext + ps - 1) & ~int64_t(ps - 1) : ceil_div(ext, ps) * ps;
+        } else if (ext > 0) {
+          n = ceil_div(ext, s.l_chunk);
+          cs = ceil_div(ceil_div(ext, n), ps) * ps;
+          n = ceil_div(ext, cs);
         }
         visit(i, h, q0, qn, lo_e, e, cs, n, diag);
       }
@@ -223,25 +227,69 @@ void plan_fill(const PlanInput& in, const CostModel& cm, const PlanShape& s, con
 
   // a5: longest first (ties: enumeration order), then a min-queue of (load, CTA id)
   const int64_t* cost = st.cost;
-  std::sort(st.order, st.order + W,
-            [cost](int32_t a, int32_t b) { return cost[a] > cost[b] || (cost[a] == cost[b] && a < b); });
   const int C = s.num_ctas;
-  std::greater<std::pair<int64_t, int32_t>> later;
-  for (int c = 0; c < C; ++c) {
-    st.heap[c] = {0, c};
-    st.count[c] = 0;
-    if (st.loads) st.loads[c] = 0;
-  }
-  std::make_heap(st.heap, st.heap + C, later);
+  int64_t max_cost = 0, sum_cost = 0;
   for (int64_t k = 0; k < W; ++k) {
-    const int32_t it = st.order[k];
-    std::pop_heap(st.heap, st.heap + C, later);
-    std::pair<int64_t, int32_t>& top = st.heap[C - 1];
-    st.cta_of[it] = top.second;
-    st.count[top.second] += 1;
-    top.first += cost[it];
-    if (st.loads) st.loads[top.second] = top.first;
-    std::push_heap(st.heap, st.heap + C, later);
+    max_cost = std::max(max_cost, cost[k]);
+    sum_cost += cost[k];
+  }
+  // Both orders are total and the same as the tuple comparisons below; packed into one 64-bit key
+  // when the values fit (they do for any batch within the workspace limits and cost model weights
+  // up to 2^20), which makes the sort and the queue several times faster.
+  const bool packed = max_cost < (int64_t(1) << 34) && W < (int64_t(1) << 28) &&
+                      sum_cost < (int64_t(1) << 46) && C <= (1 << 16);
+  if (packed) {
+    // sort key: (max_cost - cost) << 28 | index, ascending = cost descending, then index ascending
+    uint64_t* key = st.cost_key;
+    for (int64_t k = 0; k < W; ++k) key[k] = (uint64_t(max_cost - cost[k]) << 28) | uint64_t(k);
+    std::sort(key, key + W);
+    for (int64_t k = 0; k < W; ++k) st.order[k] = static_cast<int32_t>(key[k] & ((uint64_t(1) << 28) - 1));
+    // min-queue of (load << 16 | CTA id): the root is replaced and sifted down once per item
+    uint64_t* q = key;  // the sort keys are no longer needed
+    for (int c = 0; c < C; ++c) {
+      q[c] = uint64_t(c);  // load 0: already a heap (ids ascending)
+      st.count[c] = 0;
+      if (st.loads) st.loads[c] = 0;
+    }
+    for (int64_t k = 0; k < W; ++k) {
+      const int32_t it = st.order[k];
+      const uint64_t top = q[0];
+      const int32_t cta = static_cast<int32_t>(top & 0xFFFFu);
+      st.cta_of[it] = cta;
+      st.count[cta] += 1;
+      const uint64_t v = top + (uint64_t(cost[it]) << 16);
+      if (st.loads) st.loads[cta] = static_cast<int64_t>(v >> 16);
+      int i = 0;
+      for (;;) {
+        const int l = 2 * i + 1;
+        if (l >= C) break;
+        const int m = (l + 1 < C && q[l + 1] < q[l]) ? l + 1 : l;
+        if (q[m] >= v) break;
+        q[i] = q[m];
+        i = m;
+      }
+      q[i] = v;
+    }
+  } else {
+    std::sort(st.order, st.order + W,
+              [cost](int32_t a, int32_t b) { return cost[a] > cost[b] || (cost[a] == cost[b] && a < b); });
+    std::greater<std::pair<int64_t, int32_t>> later;
+    for (int c = 0; c < C; ++c) {
+      st.heap[c] = {0, c};
+      st.count[c] = 0;
+      if (st.loads) st.loads[c] = 0;
+    }
+    std::make_heap(st.heap, st.heap + C, later);
+    for (int64_t k = 0; k < W; ++k) {
+      const int32_t it = st.order[k];
+      std::pop_heap(st.heap, st.heap + C, later);
+      std::pair<int64_t, int32_t>& top = st.heap[C - 1];
+      st.cta_of[it] = top.second;
+      st.count[top.second] += 1;
+      top.first += cost[it];
+      if (st.loads) st.loads[top.second] = top.first;
+      std::push_heap(st.heap, st.heap + C, later);
+    }
   }
 
   // queues in CSR form: each CTA's items in the order they were assigned
@@ -287,9 +335,10 @@ int build_plan(const PlanInput& in, const CostModel& cm, Plan* out) {
   std::vector<int32_t> work(W * kItemFields), order(W), cta_of(W), count(C);
   std::vector<int64_t> cost(W);
   std::vector<std::pair<int64_t, int32_t>> heap(C);
+  std::vector<uint64_t> key(std::max(W, C));
   PlanStorage ps{out->cta_indptr.data(), out->items.data(), out->units.data(), out->slot_unit.data(),
                  out->loads.data(), work.data(), cost.data(), order.data(), cta_of.data(), count.data(),
-                 heap.data()};
+                 heap.data(), key.data()};
   plan_fill(in, cm, s, ps, out->header);
   return FI_OK;
 }

@@ -107,6 +107,7 @@ struct PlanStorage {
   int32_t* cta_of;      // [n_items]
   int32_t* count;       // [num_ctas]
   std::pair<int64_t, int32_t>* heap;  // [num_ctas] (load, CTA id)
+  uint64_t* cost_key;  // [max(n_items, num_ctas)]: packed sort keys, then the packed queue
 };
 
 int plan_shape(const PlanInput& in, const CostModel& cost, PlanShape* shape);

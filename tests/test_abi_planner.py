@@ -72,6 +72,17 @@ def test_cpp_planner_matches_oracle(lib, seed):
              alpha=int(rng.integers(0, 4)), beta=int(rng.integers(1, 4)), l_min=int(rng.choice([1, 64, 256])))
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_cpp_planner_matches_oracle_with_large_cost_weights(lib, seed):
+    """Weights whose costs do not fit the planner's packed 64-bit sort and queue keys take its general
+    path; both paths must give the restatement's plan."""
+    rng = np.random.default_rng(900 + seed)
+    qo, kv, last, hq, hk, ps, causal = _case(rng)
+    if int(np.diff(qo).max(initial=0)) * (hq // hk) > 8 and (ps % 8 or 128 % ps):
+        return
+    _compare(qo, kv, last, hq, hk, ps, causal, int(rng.choice([7, 152])), alpha=1 << 40, beta=1 << 12, l_min=64)
+
+
 def test_hand_worked_plan_through_abi(lib, repo_root):
     import json
     gd = json.load(open(os.path.join(repo_root, "tests", "golden", "plan_hand_worked.json")))
