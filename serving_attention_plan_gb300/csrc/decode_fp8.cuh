@@ -344,7 +344,6 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   auto& sm = *reinterpret_cast<DecodeSmemFp8<R, NW, S>*>(smem_raw);
   const int warp = threadIdx.x >> 5;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in decode_kernel
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       sm.slot_consumed[s] = s - S;
@@ -368,6 +367,7 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   }
   __syncthreads();
   if (p.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in decode_kernel
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp > kCopiers) {

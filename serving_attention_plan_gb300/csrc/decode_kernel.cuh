@@ -1003,9 +1003,6 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S, kMma>*>(smem_raw);
   const int warp = threadIdx.x >> 5;
-  // a following launch made dependent on this one may start its own set-up as SMs free up; it waits
-  // for this grid before it reads memory
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       sm.slot_consumed[s] = s - S;
@@ -1032,6 +1029,10 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
   }
   __syncthreads();
   if (p.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a following launch made dependent on this one may start its own set-up as SMs free up; it waits
+  // for this grid before it reads memory.  Triggered after the wait above, so a follower can never
+  // run ahead of the kernel before this one.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp >= kLoaders) {

@@ -113,6 +113,9 @@ struct PrefillParams {
   float v_scale;     // 1 for bf16 pages
   int window_left;   // >= 0: a row at key position p sees keys p - window_left .. p
   float cap_log2;    // > 0: logit soft-cap in the log2 domain, s -> cap_log2 * tanh(s / cap_log2)
+  // 1: launched as a programmatic dependent of the previous kernel on the stream: the CTA sets up
+  // its barriers and tensor memory, then waits for that kernel before any global read
+  int wait_prior;
 };
 
 struct PrefillSmem {
@@ -715,9 +718,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ unsigned char smem_raw[];
-  // the contraction kernel that follows may be scheduled as soon as every CTA has started; it
-  // waits for this grid to complete before it reads a partial state
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // 128B-swizzled tiles want 1024-byte alignment
   PrefillSmem& sm = *reinterpret_cast<PrefillSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -758,6 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (p.wait_prior) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the launch that follows (the contraction, or the next kernel) may be scheduled from here on; it
+  // waits for this grid to complete before it reads anything this grid writes.  Triggered after the
+  // wait above, so a follower can never run ahead of the kernel before this one.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tmem = sm.tmem_base;
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
@@ -819,6 +824,8 @@ constexpr int kContractUnroll = 8;
 __global__ void __launch_bounds__(kContractThreads) contract_kernel(const __grid_constant__ ContractParams p) {
   // the attention grid has completed and its partial states are visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next launch on the stream may start its set-up (it waits for this grid before reading)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int n_warps = gridDim.x * (kContractThreads / 32);
   const int tasks = __ldg(p.header + H_NUM_UNITS) * kTcRows;
@@ -984,6 +991,7 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.v_scale = a.v_scale;
   p.window_left = a.window_left;
   p.cap_log2 = a.cap_log2;
+  p.wait_prior = 1;
 
   const size_t smem = sizeof(PrefillSmem) + 1024;
   // window, soft-cap, page layout and e4m3 pages are template flags: the plain bf16 HND kernel
@@ -1007,8 +1015,22 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
       attr = cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   });
   if (attr != cudaSuccess) return record_cuda_error(attr, "cudaFuncSetAttribute(prefill_kernel)");
-  kernel<<<a.num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
-  cudaError_t e = cudaGetLastError();
+  // a programmatic dependent of the previous kernel on the stream: set-up overlaps its tail
+  cudaError_t e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(a.num_ctas));
+    cfg.blockDim = dim3(unsigned(kThreads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, p, tq, tk, tv);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
   if (e == cudaSuccess && !a.contract) return FI_OK;
   if (e == cudaSuccess) {
     // the contraction of split rows; launched for every plan of this path (it reads the number
