@@ -166,6 +166,37 @@ def test_unaligned_rows_rejected_on_host():
     assert ei.value.status == 1
 
 
+@pytest.mark.parametrize("prefill", [False, True])
+def test_dependent_launch_reads_the_previous_output(prefill):
+    """Back-to-back runs on one stream, the second reading the first's output as its q: a run is
+    launched as a programmatic dependent of the kernel before it and may start its set-up early, so
+    this checks that it reads nothing before that kernel has finished."""
+    import dataclasses
+    torch = torch_mod()
+    from serving_attention_plan_gb300 import binding as B
+    if prefill:
+        b = W.random_small_batch(91, batch=6, num_qo_heads=32, num_kv_heads=8, page_size=16, causal=True,
+                                 q_len_range=(100, 400), kv_len_range=(400, 1200), scale=0.5)
+    else:
+        b = W.random_small_batch(90, batch=96, num_qo_heads=32, num_kv_heads=8, page_size=16, causal=False,
+                                 kv_len_range=(500, 3000))
+    q, k, v = to_device(b)
+    o1, lse1 = alloc_out(b)
+    o2, lse2 = alloc_out(b)
+    ws = B.Workspace(b.batch_size, b.total_q, int(b.kv_indptr[-1]), b.num_qo_heads, b.num_kv_heads, 128)
+    ws.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.page_size, b.causal)
+    assert ws.info()[1] == (1 if prefill else 0)
+    for _ in range(3):
+        o2.fill_(float("nan"))
+        ws.run(q, k, v, o1, lse1)
+        ws.run(o1, k, v, o2, lse2)  # q of the second run = output of the first
+        torch.cuda.synchronize()
+        assert ws.get_error() == 0
+        b2 = dataclasses.replace(b, q=o1.view(torch.int16).cpu().numpy().view(np.uint16))
+        ro, rl = A.batch_attention(b2)
+        assert_close(o2.float().cpu().numpy().astype(np.float64), lse2.cpu().numpy().astype(np.float64), ro, rl)
+
+
 def test_merge_states_kernel():
     torch = torch_mod()
     from serving_attention_plan_gb300 import binding as B
