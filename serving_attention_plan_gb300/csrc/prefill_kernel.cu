@@ -15,12 +15,11 @@
 //     and write the partial states of split rows to workspace slots; the
 //     contraction follows in a second kernel chained by programmatic dependent
 //     launch, so its launch overlaps the attention tail and every SM shares it,
-//     each row summing its chunks in the plan's slot order.  (A 128-row partial
-//     state is 64 KB: merged by the last chunk's CTA alone, as the decode kernel
-//     does with its <= 8-row states, a row cut into 19 chunks took ~70 us.  An
-//     in-kernel grid barrier would need a cooperative launch, which the driver
-//     refuses for this grid: it counts one TMEM-allocating CTA per SM, although
-//     two run side by side.)
+//     each row summing its chunks in the plan's slot order.  (A 256-row partial
+//     state is 128 KB.  Merged by the last chunk's CTA alone, as the decode kernel
+//     does with its <= 8-row states, a 128-row state cut into 19 chunks took
+//     ~70 us with the earlier 128-row design; an in-kernel grid barrier would need
+//     a cooperative launch, which the driver refused for that two-CTA-per-SM grid.)
 //
 // One CTA per SM (all 512 TMEM columns, ~200 KB of shared memory), 16 warps = 4 warpgroups.
 // A work item is 256 rows (256/g tokens x g heads) as two 128-row MMA tiles, Q0 (rows 0-127)
@@ -946,7 +945,7 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     return FI_ERR_INVALID_ARG;
   CUtensorMap tq, tk, tv;
   const uint64_t row_bytes = uint64_t(kHeadDim) * 2;
-  // q: (dim, head, token); a box is 64 dims x g heads x (128/g) tokens = up to 128 rows of 128 B
+  // q: (dim, head, token); a box is 64 dims x g heads x (256/g) tokens = up to 256 rows of 128 B
   if (!make_map(&tq, a.q, uint64_t(a.hqo), uint64_t(a.total_q), row_bytes, row_bytes * a.hqo, uint32_t(a.group),
                 uint32_t(a.tile_tokens)))
     return FI_ERR_INVALID_ARG;

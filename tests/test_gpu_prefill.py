@@ -18,7 +18,7 @@ def built():
 
 
 def test_single_tile_causal():
-    """One request, one 128-row tile (32 tokens x g=4), one KV tile: the smallest tensor-core case."""
+    """One request of 32 tokens x g=4 (half of one 256-row item), one KV tile: the smallest tensor-core case."""
     b = W.random_small_batch(1, batch=1, num_qo_heads=8, num_kv_heads=2, page_size=16, causal=True,
                              q_len_range=(32, 32), kv_len_range=(32, 32), extra_pages=0)
     o, lse, ws = run_library(b, num_sms=1)
