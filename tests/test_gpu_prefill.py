@@ -37,6 +37,9 @@ CASES = [
     (64, 8, 64, (2, 40), (50, 900), True, 7),        # g = 8, page 64
     (8, 8, 128, (17, 130), (10, 600), True, 1),      # g = 1, page 128, causal rows with no visible key
     (12, 4, 16, (10, 90), (90, 400), True, 2),       # g = 3: 42-token tiles of 126 rows
+    (64, 4, 16, (3, 60), (60, 500), True, 3),        # g = 16: 16-token items
+    (64, 4, 32, (1, 1), (1, 900), False, 0),         # g = 16 decode: 16 rows a request, tensor-core items
+    (128, 4, 16, (2, 30), (30, 300), True, 2),       # g = 32: 8-token items
 ]
 
 
