@@ -1,6 +1,7 @@
 // Launch of the FP8-KV decode kernel (核心机制 8, paper App. F), one instantiation per rows-per-tile.
 #include "decode_fp8.cuh"
 #include "decode_launch.cuh"
+#include "prefill_launch.h"
 
 namespace fi {
 
@@ -14,35 +15,44 @@ constexpr int kFp8Warps = 8;
 template <int R>
 constexpr int kFp8Stages = R >= 8 ? 11 : 12;
 
-template <int R, bool kNhd>
-int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream, bool pdl) {
+template <int R, bool kNhd, bool kTma>
+int launch_fp8_as(int grid, const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                  cudaStream_t stream, bool pdl) {
   using Smem = DecodeSmemFp8<R, kFp8Warps, kFp8Stages<R>>;
-  static_assert(sizeof(Smem) <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
-  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers, kNhd>;
+  constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // slack for the kernel's 1 KB alignment
+  static_assert(kSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+  auto kernel = decode_kernel_fp8<R, kFp8Warps, kFp8Stages<R>, kDecodeCopiers, kNhd, kTma>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
+    attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
   });
   if (attr_err != cudaSuccess) return record_cuda_error(attr_err, "cudaFuncSetAttribute(decode fp8)");
-  const unsigned threads = (kFp8Warps + 1 + kDecodeCopiers) * 32;
-  if (pdl) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(grid));
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = sizeof(Smem);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
-    return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel_fp8 launch (programmatic)");
-  }
-  kernel<<<grid, threads, sizeof(Smem), stream>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3((kFp8Warps + 1 + kDecodeCopiers) * 32);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p, tm_k, tm_v);
   return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel_fp8 launch");
+}
+
+// Pages of 8 or more tokens take the TMA copier (each box at least 1 KB, so boxes start on the
+// 1 KB boundaries the 128-byte swizzle needs); smaller pages the 16-byte copies.
+template <int R, bool kNhd>
+int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream, bool pdl) {
+  CUtensorMap tm_k{}, tm_v{};
+  if (p.page_size < 8) return launch_fp8_as<R, kNhd, false>(grid, p, tm_k, tm_v, stream, pdl);
+  const int hkv = int(p.page_stride / (int64_t(p.page_size) * kHeadDim));
+  if (!make_decode_map_e4m3(&tm_k, p.k, hkv, p.page_size, p.num_pages, kNhd) ||
+      !make_decode_map_e4m3(&tm_v, p.v, hkv, p.page_size, p.num_pages, kNhd))
+    return FI_ERR_INVALID_ARG;
+  return launch_fp8_as<R, kNhd, true>(grid, p, tm_k, tm_v, stream, pdl);
 }
 
 }  // namespace

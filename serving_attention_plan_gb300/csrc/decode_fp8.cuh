@@ -13,9 +13,11 @@
 // logit scale and the V scale into the output.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "decode_kernel.cuh"
+#include "tcgen05.cuh"
 
 namespace fi {
 
@@ -129,6 +131,73 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
   cp_async_wait_all();
 }
 
+// TMA variant of the copier (pages of at least 8 tokens): copier warp `cw` issues its stages as
+// tensor boxes, one per page (or per 64-token run of a longer page) for K and one for V, each box
+// page_tokens rows of 128 codes landing in the 128-byte swizzle, which puts 16-byte chunk c of
+// token t at chunk position c ^ (t & 7): the layout the consumers read.  A box of 8 or more rows
+// is at least 1 KB, so every box starts on a 1 KB boundary of the stage.  The copies bypass the
+// load/store pipeline the consumers' shared-memory instructions use.  Boxes are whole pages, so a
+// request's last page may bring codes past its last token: those rows are masked by the consumers.
+// tm_k / tm_v: HND (codes, token in page, page * H_kv + head) or NHD (codes, head, token, page).
+template <int R, int NW, int S, int kCopiers, bool kNhd>
+__device__ __forceinline__ void decode_tma_copier_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm,
+                                                      const CUtensorMap* tm_k, const CUtensorMap* tm_v, int begin,
+                                                      int end, int cw) {
+  const int lane = threadIdx.x & 31;
+  const int sh = p.page_shift;
+  const int box_tok = min(p.page_size, kFp8StageTokens);  // rows of a box
+  const int hkv = int(p.page_stride >> (sh + 7));        // page stride = H_kv * page_size * 128 codes
+  StageCursorT<kFp8StageTokens> c{begin, end, 0, 0, 0, 0, 0, 0};
+  bool ok = c.load(p.items);
+  for (int k = 0; k < cw && ok; ++k) ok = c.next(p.items);
+  int issued_last = -1;  // this warp's last stage
+  for (int n = cw; ok; n += kCopiers) {
+    const int islot = n % kIdxSlots;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.idx_full[islot], (n / kIdxSlots) & 1, p.err, &sm.abort))) break;
+    const int t0 = c.tok0();
+    const int nt = c.ntok();
+    // boxes of this stage: pages from the stage's first token (stages start on a page boundary, or
+    // on a 64-token boundary inside a longer page)
+    const int nbox = (nt + box_tok - 1) / box_tok;
+    int pg = (lane < nbox) ? sm.idx[islot][lane] : -1;
+    if (lane < nbox && (pg < 0 || pg >= p.num_pages)) {
+      atomicOr(p.err, FI_DEVERR_PAGE_OOB);
+      pg = -1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.idx_empty[islot]);
+    const int slot = n % S, fill = n / S;
+    if (!__all_sync(0xffffffffu, spin_until_eq(&sm.slot_filled[slot], n - S, p.err, &sm.abort))) break;
+    if (fill > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.empty[slot], (fill - 1) & 1, p.err, &sm.abort))) break;
+    const uint32_t bytes = pg >= 0 ? uint32_t(2 * box_tok * kHeadDim) : 0u;
+    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+    if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], total);
+    __syncwarp();
+    if (pg >= 0) {
+      const int y = t0 & (p.page_size - 1) & ~(box_tok - 1);  // 0 unless pages are longer than a stage
+      uint8_t* dk = &sm.kv8[slot][0][lane * box_tok][0];
+      uint8_t* dv = &sm.kv8[slot][1][lane * box_tok][0];
+      if constexpr (kNhd) {
+        tc::tma_load_4d(dk, tm_k, 0, c.kv_head, y, pg, &sm.full[slot]);
+        tc::tma_load_4d(dv, tm_v, 0, c.kv_head, y, pg, &sm.full[slot]);
+      } else {
+        tc::tma_load_3d(dk, tm_k, 0, y, pg * hkv + c.kv_head, &sm.full[slot]);
+        tc::tma_load_3d(dv, tm_v, 0, y, pg * hkv + c.kv_head, &sm.full[slot]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<volatile int*>(&sm.slot_filled[slot]) = n;
+    issued_last = n;
+    for (int k = 0; k < kCopiers && ok; ++k) ok = c.next(p.items);
+  }
+  // A normal run needs no drain: the consumers wait for every stage to land before the CTA ends.
+  // After an abort, wait (bounded) for this warp's recent stages so that no tensor copy is still
+  // landing in shared memory when the CTA exits.
+  if (*reinterpret_cast<volatile int*>(&sm.abort)) {
+    for (int n = issued_last; n >= 0 && n > issued_last - S; n -= kCopiers) mbar_wait_bounded(&sm.full[n % S], (n / S) & 1);
+  }
+}
+
 // Consumer warp w: stages w, w + NW, ... of the CTA's queue.  Fragment layouts as in
 // decode_consumer_mma, with the reduction dimension permuted where that lets ldmatrix hand each
 // lane whole code groups (a permutation of the summed index changes nothing):
@@ -140,7 +209,10 @@ __device__ __forceinline__ void decode_copier_fp8(const DecodeParams& p, DecodeS
 //     (gq, qd) codes of tokens 2qd, 2qd+1 (and 8 + those) at dims 2gq, 2gq+1 of each chunk; a byte
 //     permute splits them into the even-dim and the odd-dim fragment, so output tile mt = 2db + e
 //     holds dims 32db + 2gq + e (rows gq) and 32db + 16 + 2gq + e (rows gq + 8).
-template <int R, int NW, int S>
+// kWholePages: stages were filled with whole pages (the TMA copier), so rows past the stage's last
+// token may hold codes from past a request's last token (possibly NaN codes): their V codes are
+// cleared before the P.V MMAs, where a zero weight would not cancel a NaN.
+template <int R, int NW, int S, bool kWholePages = false>
 __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, DecodeSmemFp8<R, NW, S>& sm, int begin,
                                                     int end, int w) {
   const int lane = threadIdx.x & 31;
@@ -286,6 +358,16 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
             // r[2], r[3]: the same for chunk 2db + 1.  Bytes of each: [t0 d0, t0 d1, t1 d0, t1 d1].
             uint32_t r[4];
             ldsm_x4_trans(r, row + (((2 * db + lv_chunk) ^ (tok & 7)) * 16));
+            if (kWholePages && nt < kFp8StageTokens) {
+              // tokens of r[0] / r[2]: 16 kt + 2 qd (bytes 0-1) and + 1 (bytes 2-3); r[1] / r[3]: + 8
+              const int tl = 16 * kt + 2 * qd;
+              const uint32_t m_lo = (tl < nt ? 0x0000FFFFu : 0u) | (tl + 1 < nt ? 0xFFFF0000u : 0u);
+              const uint32_t m_hi = (tl + 8 < nt ? 0x0000FFFFu : 0u) | (tl + 9 < nt ? 0xFFFF0000u : 0u);
+              r[0] &= m_lo;
+              r[2] &= m_lo;
+              r[1] &= m_hi;
+              r[3] &= m_hi;
+            }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               uint32_t a[4];
@@ -338,17 +420,23 @@ __device__ __forceinline__ void decode_consumer_fp8(const DecodeParams& p, Decod
   }
 }
 
-template <int R, int NW, int S, int kCopiers, bool kNhd>
+// kTma: the copiers issue tensor boxes of whole pages (pages of 8 or more tokens) instead of
+// 16-byte copies; tm_k / tm_v are then the K and V page maps (unused otherwise).  Shared memory is
+// aligned to 1 KB here (the launch adds the slack): the boxes land 128-byte swizzled.
+template <int R, int NW, int S, int kCopiers, bool kNhd, bool kTma = false>
 __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
-    decode_kernel_fp8(const __grid_constant__ DecodeParams p) {
+    decode_kernel_fp8(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  auto& sm = *reinterpret_cast<DecodeSmemFp8<R, NW, S>*>(smem_raw);
+  auto& sm = *reinterpret_cast<DecodeSmemFp8<R, NW, S>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       sm.slot_consumed[s] = s - S;
       sm.slot_filled[s] = s - S;
-      mbar_init(&sm.full[s], 32);  // one arrival per lane of the stage's copier
+      // LDGSTS: one arrival per lane of the stage's copier; TMA: the copier's expect-tx arrival
+      mbar_init(&sm.full[s], kTma ? 1 : 32);
       mbar_init(&sm.empty[s], 1);
     }
     for (int s = 0; s < kIdxSlots; ++s) {
@@ -371,9 +459,11 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   const int begin = __ldg(p.cta_indptr + blockIdx.x);
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp > kCopiers) {
-    decode_consumer_fp8<R, NW, S>(p, sm, begin, end, warp - 1 - kCopiers);
+    decode_consumer_fp8<R, NW, S, kTma>(p, sm, begin, end, warp - 1 - kCopiers);
   } else if (warp == 0) {
     decode_index_warp<R, NW, S, DecodeSmemFp8<R, NW, S>, kFp8StageTokens>(p, sm, begin, end);
+  } else if constexpr (kTma) {
+    decode_tma_copier_fp8<R, NW, S, kCopiers, kNhd>(p, sm, &tm_k, &tm_v, begin, end, warp - 1);
   } else {
     decode_copier_fp8<R, NW, S, kCopiers, kNhd>(p, sm, begin, end, warp - 1);
   }

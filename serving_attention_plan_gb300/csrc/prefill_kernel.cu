@@ -935,6 +935,28 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, uint64_t page_size, uint64_
 
 }  // namespace
 
+bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, bool nhd) {
+  if (encode_fn() == nullptr) return false;
+  const cuuint32_t rows = cuuint32_t(page_size < 64 ? page_size : 64);
+  const cuuint64_t row = uint64_t(kHeadDim);  // one byte a code
+  if (nhd) {
+    const cuuint64_t dims[4] = {row, uint64_t(hkv), uint64_t(page_size), uint64_t(num_pages)};
+    const cuuint64_t strides[3] = {row, row * hkv, row * hkv * page_size};
+    const cuuint32_t box[4] = {128u, 1u, rows, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  const cuuint64_t dims[3] = {row, uint64_t(page_size), uint64_t(num_pages) * uint64_t(hkv)};
+  const cuuint64_t strides[2] = {row, row * page_size};
+  const cuuint32_t box[3] = {128u, rows, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (encode_fn() == nullptr) return record_cuda_error(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
   if (a.page_size % 8 != 0 || kTile % a.page_size != 0 || a.group > kItemRows || a.group * a.tile_tokens > kItemRows)

@@ -1,6 +1,7 @@
 // Launch interface of the tensor-core (tcgen05) tile path.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -47,5 +48,12 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
 // Records the text of a failed CUDA call for fi_last_error_message; returns FI_ERR_CUDA.
 int record_cuda_error(cudaError_t e, const char* what);
+
+// Tensor map of e4m3 K or V pages for the FP8 decode kernel's TMA copier: one box is
+// min(page_size, 64) rows of 128 codes of one page and KV head, 128-byte swizzled.  HND pages
+// [pages][H_kv][page_size][128] map as (code, token in page, page * H_kv + head), NHD pages
+// [pages][page_size][H_kv][128] as (code, head, token in page, page).  Returns false if the driver's
+// encoder is missing or refuses the map.
+bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, bool nhd);
 
 }  // namespace fi
