@@ -431,6 +431,12 @@ __global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
   auto& sm = *reinterpret_cast<DecodeSmemFp8<R, NW, S>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                           ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
+  if constexpr (kTma) {
+    if (threadIdx.x == 32) {  // first copier warp: fetch the two maps while the CTA sets up
+      tc::tma_prefetch_desc(&tm_k);
+      tc::tma_prefetch_desc(&tm_v);
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       sm.slot_consumed[s] = s - S;

@@ -37,10 +37,13 @@
 // Scores are kept in the log2 domain.
 #pragma once
 
+#include <cuda.h>
+
 #include <climits>
 
 #include "device_common.cuh"
 #include "plan.h"
+#include "tcgen05.cuh"
 
 namespace fi {
 
@@ -319,6 +322,70 @@ __device__ __forceinline__ void decode_copier_warp(const DecodeParams& p, Decode
     for (int k = 0; k < kCopiers && ok; ++k) ok = c.next(p.items);
   }
   cp_async_wait_all();
+}
+
+// TMA copier (HND pages of 8 or more tokens, tensor-core consumer): copier warp `cw` issues its
+// stages as tensor boxes of min(page_size, 32) tokens of one page and KV head, 64 dims each, so a
+// stage's K (and V) lands as two 64-dim halves [2][32 tokens][64] in the 128-byte swizzle: 16-byte
+// chunk c of token t's half at chunk position c ^ (t & 7).  A box of 8 or more rows is at least
+// 1 KB, so boxes start on 1 KB boundaries.  The copies bypass the load/store pipeline the
+// consumers' shared-memory instructions use.  Boxes are whole pages, so a request's last page may
+// bring rows past its last token; the consumers clear those rows' V before the P.V MMAs.
+// tm_k / tm_v map (dim, token in page, page * H_kv + head).
+template <int R, int NW, int S, int kCopiers, bool kMs>
+__device__ __forceinline__ void decode_tma_copier(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm,
+                                                  const CUtensorMap* tm_k, const CUtensorMap* tm_v, int begin, int end,
+                                                  int cw) {
+  const int lane = threadIdx.x & 31;
+  const int box_tok = min(p.page_size, kStageTokens);
+  const int hkv = int(p.page_stride >> (p.page_shift + 7));  // page stride = H_kv * page_size * 128
+  StageCursor c{begin, end, 0, 0, 0, 0, 0, 0};
+  bool ok = c.load(p.items);
+  for (int k = 0; k < cw && ok; ++k) ok = c.next(p.items);
+  int issued_last = -1;
+  for (int n = cw; ok; n += kCopiers) {
+    const int islot = n % kIdxSlots;
+    if (!__all_sync(0xffffffffu, mbar_wait(&sm.idx_full[islot], (n / kIdxSlots) & 1, p.err, &sm.abort))) break;
+    const int t0 = c.tok0();
+    const int nt = c.ntok();
+    // stages start on a page boundary, or on a 32-token boundary inside a longer page
+    const int nbox = (nt + box_tok - 1) / box_tok;
+    int pg = (lane < nbox) ? sm.idx[islot][lane] : -1;
+    if (lane < nbox && (pg < 0 || pg >= p.num_pages)) {
+      atomicOr(p.err, FI_DEVERR_PAGE_OOB);
+      pg = -1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.idx_empty[islot]);
+    const int slot = n % S, fill = n / S;
+    if (!__all_sync(0xffffffffu, spin_until_eq(&sm.slot_filled[slot], n - S, p.err, &sm.abort))) break;
+    if (fill > 0 && !__all_sync(0xffffffffu, mbar_wait(&sm.empty[slot], (fill - 1) & 1, p.err, &sm.abort))) break;
+    const uint32_t bytes = pg >= 0 ? uint32_t(4 * box_tok * 128) : 0u;  // K and V, two 128-byte halves a row
+    const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+    if (lane == 0) mbar_arrive_expect_tx(&sm.full[slot], total);
+    __syncwarp();
+    if (pg >= 0) {
+      const int y = t0 & (p.page_size - 1) & ~(box_tok - 1);
+      const int z = pg * hkv + c.kv_head;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        __nv_bfloat16* dk = &sm.kv[slot][0][0][0] + h * (kStageTokens * 64) + lane * box_tok * 64;
+        __nv_bfloat16* dv = &sm.kv[slot][1][0][0] + h * (kStageTokens * 64) + lane * box_tok * 64;
+        tc::tma_load_3d(dk, tm_k, 64 * h, y, z, &sm.full[slot]);
+        tc::tma_load_3d(dv, tm_v, 64 * h, y, z, &sm.full[slot]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) *reinterpret_cast<volatile int*>(&sm.slot_filled[slot]) = n;
+    issued_last = n;
+    for (int k = 0; k < kCopiers && ok; ++k) ok = c.next(p.items);
+  }
+  // A normal run needs no drain: the consumers wait for every stage to land before the CTA ends.
+  // After an abort, wait (bounded) for this warp's recent stages so that no tensor copy is still
+  // landing in shared memory when the CTA exits.
+  if (*reinterpret_cast<volatile int*>(&sm.abort)) {
+    for (int n = issued_last; n >= 0 && n > issued_last - S; n -= kCopiers) mbar_wait_bounded(&sm.full[n % S], (n / S) & 1);
+  }
 }
 
 template <int R>
@@ -781,7 +848,11 @@ __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSme
 // chunk position c ^ (t & 7), so the eight row addresses of every ldmatrix hit distinct banks.
 // Lane l holds query rows 2(l%4), 2(l%4)+1; a row's running max is reduced over the 8 lanes
 // that share it; its running sum stays per lane until the end of the item.
-template <int R, int NW, int S, bool kVar, bool kMs>
+// kHalves: the stages hold K and V as two 64-dim halves [2][32 tokens][64], chunk c of a half-row
+// at c ^ (t & 7) (the TMA copier's layout), and may hold rows past the stage's last token from a
+// request's last page: their V is cleared before the P.V MMAs.  Otherwise [32 tokens][128], chunk
+// c (of 16) at c ^ (t & 7), and rows past the last token hold earlier stages' rows.
+template <int R, int NW, int S, bool kVar, bool kHalves, bool kMs>
 __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin,
                                                     int end, int w) {
   const int lane = threadIdx.x & 31;
@@ -791,6 +862,13 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
   // ldmatrix row addresses (element offsets within a stage's K or V tile), swizzled chunks
   const int lk_tok = (lane & 7) + ((lane >> 3) & 1) * 8, lk_chunk = lane >> 4;  // K: m = token, k = dim
   const int lv_tok = (lane & 7) + (lane >> 4) * 8, lv_chunk = (lane >> 3) & 1;  // V^T: m = dim, k = token
+  // element offset of 16-byte chunk c16 (of 16) of token t within a stage's K or V tile
+  auto chunk_at = [](int t, int c16) {
+    if constexpr (kHalves)
+      return (c16 >> 3) * (kStageTokens * 64) + t * 64 + (((c16 & 7) ^ (t & 7)) * 8);
+    else
+      return t * kHeadDim + ((c16 ^ (t & 7)) * 8);
+  };
 
   int stage_n = 0;
   bool alive = true;
@@ -873,11 +951,10 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
         s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
         if (mt < n_mt) {
           const int tok = 16 * mt + lk_tok;
-          const __nv_bfloat16* row = Ks + tok * kHeadDim;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             uint32_t a[4];
-            ldsm_x4(a, row + (((2 * ks + lk_chunk) ^ (tok & 7)) * 8));
+            ldsm_x4(a, Ks + chunk_at(tok, 2 * ks + lk_chunk));
             mma_16816(s[mt], a, qb[ks][0], qb[ks][1]);
           }
         }
@@ -940,11 +1017,24 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
       for (int kt = 0; kt < 2; ++kt) {
         if (kt < n_mt) {
           const int tok = 16 * kt + lv_tok;
-          const __nv_bfloat16* row = Vs + tok * kHeadDim;
+          // kHalves, short stage: this lane's V^T fragments hold tokens 16 kt + 2 qd (+1) in a[0],
+          // a[1] and those + 8 in a[2], a[3] (low half: the even token)
+          uint32_t m_lo = 0xFFFFFFFFu, m_hi = 0xFFFFFFFFu;
+          if (kHalves && nt < kStageTokens) {
+            const int tl = 16 * kt + 2 * qd;
+            m_lo = (tl < nt ? 0x0000FFFFu : 0u) | (tl + 1 < nt ? 0xFFFF0000u : 0u);
+            m_hi = (tl + 8 < nt ? 0x0000FFFFu : 0u) | (tl + 9 < nt ? 0xFFFF0000u : 0u);
+          }
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
             uint32_t a[4];
-            ldsm_x4_trans(a, row + (((2 * mt + lv_chunk) ^ (tok & 7)) * 8));
+            ldsm_x4_trans(a, Vs + chunk_at(tok, 2 * mt + lv_chunk));
+            if (kHalves) {
+              a[0] &= m_lo;
+              a[1] &= m_lo;
+              a[2] &= m_hi;
+              a[3] &= m_hi;
+            }
             mma_16816(o[mt], a, pb[kt][0], pb[kt][1]);
           }
         }
@@ -991,23 +1081,36 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
 // kDecodeVariant (sliding window / soft-cap).
 constexpr int kDecodeNhd = 1;
 constexpr int kDecodeVariant = 2;
+constexpr int kDecodeTma = 8;  // HND pages of 8+ tokens: TMA copier, stages in 64-dim halves
 constexpr int kDecodeNhdHeadsShift = 4;
-template <int R, int NW, int S, int kCopiers = 0, bool kMma = false, int kFlags = 0>
-__global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
-    decode_kernel(const __grid_constant__ DecodeParams p) {
+// kFlags & kDecodeTma: the copiers issue TMA boxes (tm_k / tm_v) instead of 16-byte copies; the
+// stages then hold 64-dim halves and shared memory is aligned to 1 KB here (the launch adds the
+// slack) for the 128-byte swizzle.
+template <int R, int NW, int S, int kCopiers, bool kMma, int kFlags>
+__device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
   static_assert(!kMma || kCopiers > 0, "the tensor-core consumer reads swizzled LDGSTS stages");
   static_assert(!(kFlags & kDecodeNhd) || kCopiers > 0, "NHD pages are read by the 16-byte-copy loader");
   constexpr bool kVar = (kFlags & kDecodeVariant) != 0;
+  constexpr bool kTma = (kFlags & kDecodeTma) != 0;
+  static_assert(!kTma || (kMma && !(kFlags & kDecodeNhd)), "the TMA copier feeds the tensor-core consumer, HND pages");
   constexpr bool kLdgsts = kCopiers > 0;
   constexpr int kLoaders = kLdgsts ? 1 + kCopiers : 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S, kMma>*>(smem_raw);
+  auto& sm = *reinterpret_cast<DecodeSmem<R, NW, S, kMma>*>(
+      kTma ? ((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)) : reinterpret_cast<uintptr_t>(smem_raw));
   const int warp = threadIdx.x >> 5;
+  if constexpr (kTma) {
+    if (threadIdx.x == 32) {  // first copier warp: fetch the two maps while the CTA sets up
+      tc::tma_prefetch_desc(tm_k);
+      tc::tma_prefetch_desc(tm_v);
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       sm.slot_consumed[s] = s - S;
       sm.slot_filled[s] = s - S;
-      mbar_init(&sm.full[s], kLdgsts ? 32 : 1);  // LDGSTS: one arrival per lane of the stage's copier
+      // LDGSTS: one arrival per lane of the stage's copier; TMA and bulk copies: the expect-tx arrival
+      mbar_init(&sm.full[s], kLdgsts && !kTma ? 32 : 1);
       mbar_init(&sm.empty[s], 1);
     }
     for (int s = 0; s < kIdxSlots; ++s) {
@@ -1037,17 +1140,33 @@ __global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
   const int end = __ldg(p.cta_indptr + blockIdx.x + 1);
   if (warp >= kLoaders) {
     if constexpr (kMma)
-      decode_consumer_mma<R, NW, S, kVar>(p, sm, begin, end, warp - kLoaders);
+      decode_consumer_mma<R, NW, S, kVar, kTma>(p, sm, begin, end, warp - kLoaders);
     else
       decode_consumer<R, NW, S, kVar>(p, sm, begin, end, warp - kLoaders);
   } else if (!kLdgsts) {
     decode_producer<R, NW, S>(p, sm, begin, end);
   } else if (warp == 0) {
     decode_index_warp<R, NW, S>(p, sm, begin, end);
+  } else if constexpr (kTma) {
+    decode_tma_copier<R, NW, S, kCopiers>(p, sm, tm_k, tm_v, begin, end, warp - 1);
   } else {
     constexpr int kNhdStride = (kFlags & kDecodeNhd) ? kHeadDim << ((kFlags >> kDecodeNhdHeadsShift) & 7) : 0;
     decode_copier_warp<R, NW, S, kCopiers, kMma, kNhdStride>(p, sm, begin, end, warp - 1);
   }
+}
+
+template <int R, int NW, int S, int kCopiers = 0, bool kMma = false, int kFlags = 0>
+__global__ void __launch_bounds__((NW + (kCopiers ? 1 + kCopiers : 1)) * 32, 1)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
+  static_assert(!(kFlags & kDecodeTma), "TMA copies run in decode_kernel_tma");
+  decode_body<R, NW, S, kCopiers, kMma, kFlags>(p, nullptr, nullptr);
+}
+
+template <int R, int NW, int S, int kCopiers, int kFlags>
+__global__ void __launch_bounds__((NW + 1 + kCopiers) * 32, 1)
+    decode_kernel_tma(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v) {
+  decode_body<R, NW, S, kCopiers, true, kFlags | kDecodeTma>(p, &tm_k, &tm_v);
 }
 
 }  // namespace fi

@@ -66,6 +66,37 @@ int launch_decode_as(int grid, const DecodeParams& p, cudaStream_t stream, bool 
   return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel launch");
 }
 
+// Tensor-core decode with the TMA copier (HND pages of 8+ tokens); tm_k / tm_v as built by
+// make_decode_map_bf16.  pdl as for launch_decode_as.
+template <int R, int kFlags>
+int launch_decode_tma_as(int grid, const DecodeParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                         cudaStream_t stream, bool pdl) {
+  constexpr int kDecodeWarps = DecodeConfig<R, true>::kWarps;
+  constexpr int kDecodeStages = DecodeConfig<R, true>::kStages;
+  using Smem = DecodeSmem<R, kDecodeWarps, kDecodeStages, true>;
+  constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // slack for the kernel's 1 KB alignment
+  static_assert(kSmemBytes <= 227 * 1024, "decode shared memory exceeds the per-CTA limit");
+  auto kernel = decode_kernel_tma<R, kDecodeWarps, kDecodeStages, kDecodeCopiers, kFlags>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+  });
+  if (attr_err != cudaSuccess) return record_cuda_error(attr_err, "cudaFuncSetAttribute(decode tma)");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(unsigned((kDecodeWarps + 1 + kDecodeCopiers) * 32));
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p, tm_k, tm_v);
+  return e == cudaSuccess ? FI_OK : record_cuda_error(e, "decode_kernel_tma launch");
+}
+
 // NHD decode (16-byte-copy loader): the page-row stride H_kv * 128 is a compile-time constant of
 // the kernel (a run-time stride in its copy loop measured a third slower), so the kernel is
 // instantiated per rows-per-tile and per log2(H_kv) in 0..4.  pdl as for launch_decode_as.

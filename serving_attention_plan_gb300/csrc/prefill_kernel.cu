@@ -957,6 +957,13 @@ bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_si
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_decode_map_bf16(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages) {
+  if (encode_fn() == nullptr) return false;
+  const uint64_t row = uint64_t(kHeadDim) * 2;
+  return make_map(m, base, uint64_t(page_size), uint64_t(num_pages) * uint64_t(hkv), row, row * page_size,
+                  uint32_t(page_size < 32 ? page_size : 32), 1u);
+}
+
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (encode_fn() == nullptr) return record_cuda_error(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
   if (a.page_size % 8 != 0 || kTile % a.page_size != 0 || a.group > kItemRows || a.group * a.tile_tokens > kItemRows)

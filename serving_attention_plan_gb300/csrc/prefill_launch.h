@@ -56,4 +56,9 @@ int record_cuda_error(cudaError_t e, const char* what);
 // encoder is missing or refuses the map.
 bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, bool nhd);
 
+// Tensor map of bf16 HND K or V pages [pages][H_kv][page_size][128] for the decode kernel's TMA
+// copier: (dim, token in page, page * H_kv + head), one box 64 dims x min(page_size, 32) tokens,
+// 128-byte swizzled.  Returns false if the driver's encoder is missing or refuses the map.
+bool make_decode_map_bf16(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages);
+
 }  // namespace fi

@@ -1,4 +1,6 @@
 """GPU parity of the decode path (<= 8-row tiles) against the float64 oracle, through the C ABI."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -39,6 +41,8 @@ CASES = [
     (8, 8, 8, (1, 8), (8, 400), True, 3),        # g = 1, up to 8 query tokens: one causal limit per row
     (32, 8, 24, (1, 1), (0, 700), False, 4),     # g = 4, page 24: bulk loader, CUDA-core consumer
     (64, 8, 12, (1, 1), (0, 900), True, 5),      # g = 8, page 12: bulk loader, CUDA-core consumer
+    (32, 8, 4, (1, 1), (0, 600), False, 4),      # g = 4, page 4: 16-byte copies, tensor-core consumer
+    (32, 8, 128, (1, 1), (0, 2000), False, 0),   # g = 4, page 128: 32-token TMA boxes inside a page
 ]
 
 
@@ -233,3 +237,22 @@ def test_many_back_to_back_launches(name):
     assert ws.get_error() == 0
     assert np.array_equal(o.float().cpu().numpy(), o_ref)
     assert np.array_equal(lse.cpu().numpy().astype(np.float64), l_ref)
+
+
+def test_decode_ignores_values_past_the_last_token():
+    """Pages of 8 or more tokens are copied whole: NaN values in the unused slots of each request's
+    last page must not reach any output (rows 4 and 8 of a tile, g = 4 and g = 8)."""
+    for hq in (32, 64):
+        b = W.random_small_batch(95 + hq, batch=12, num_qo_heads=hq, num_kv_heads=8, page_size=16, causal=False,
+                                 q_len_range=(1, 1), kv_len_range=(1, 700), extra_pages=3)
+        k, v = b.k_pages.copy(), b.v_pages.copy()  # HND [pages, H_kv, page, D] bf16 bits
+        for i in range(b.batch_size):
+            lo, hi = int(b.kv_indptr[i]), int(b.kv_indptr[i + 1])
+            if hi > lo:
+                last, n = int(b.kv_indices[hi - 1]), int(b.last_page_len[i])
+                k[last, :, n:, :] = 0x7FC0
+                v[last, :, n:, :] = 0x7FC0
+        o, lse, ws = run_library(dataclasses.replace(b, k_pages=k, v_pages=v))
+        ro, rl = A.batch_attention(b)
+        assert np.isfinite(o).all()
+        assert_close(o, lse, ro, rl)

@@ -51,6 +51,9 @@ CASES = [
     (32, 8, 16, (1, 1), (1, 2000), False, 0, 0.5, 2.0, -1, 0.0, "NHD"),     # NHD, split rows merged
     (8, 2, 64, (1, 2), (2, 900), True, 3, 1.0, 0.25, 150, 30.0, "NHD"),     # NHD, page 64, window + cap
     (8, 1, 4, (1, 1), (1, 300), False, 2, 2.0, 1.0, -1, 0.0, "NHD"),        # NHD, one KV head, page 4
+    (32, 8, 8, (1, 1), (1, 900), False, 0, 0.5, 1.0, -1, 0.0, "HND"),       # page 8: smallest whole-page box
+    (32, 8, 128, (1, 1), (1, 1500), False, 0, 1.0, 0.5, -1, 0.0, "HND"),    # page 128: 64-token boxes in a page
+    (16, 4, 128, (1, 2), (2, 1200), True, 3, 0.5, 2.0, -1, 0.0, "NHD"),     # NHD, page 128, causal
 ]
 
 
@@ -73,6 +76,25 @@ def test_fp8_decode_parity(case):
     if case in (1, 5):
         assert ws.info()[7] > 0
     ro, rl = A.batch_attention(b8, layout=layout, k_scale=ks, v_scale=vs, window_left=window, soft_cap=cap)
+    assert_close(o, lse, ro, rl)
+
+
+def test_fp8_decode_ignores_codes_past_the_last_token():
+    """Pages of 8 or more tokens are copied whole: NaN codes (0x7f) in the unused slots of each
+    request's last page must not reach any output."""
+    b = W.random_small_batch(5400, batch=9, num_qo_heads=32, num_kv_heads=8, page_size=16, causal=False,
+                             q_len_range=(1, 1), kv_len_range=(1, 900), extra_pages=3)
+    b8 = W.as_e4m3(b, 0.5, 1.0)
+    k, v = b8.k_pages.copy(), b8.v_pages.copy()  # HND [pages, H_kv, page, D]
+    for i in range(b8.batch_size):
+        lo, hi = int(b8.kv_indptr[i]), int(b8.kv_indptr[i + 1])
+        if hi > lo:
+            last, n = int(b8.kv_indices[hi - 1]), int(b8.last_page_len[i])
+            k[last, :, n:, :] = 0x7F
+            v[last, :, n:, :] = 0x7F
+    o, lse, _ = run_fp8(dataclasses.replace(b8, k_pages=k, v_pages=v), 0.5, 1.0)
+    ro, rl = A.batch_attention(b8, k_scale=0.5, v_scale=1.0)
+    assert np.isfinite(o).all()
     assert_close(o, lse, ro, rl)
 
 
