@@ -245,15 +245,22 @@ int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const 
  *   o          DEVICE bf16 [total_q, num_qo_heads, 128]   (written)
  *   lse        DEVICE float32 [total_q, num_qo_heads]     (written)
  *
+ * Slots of a request's last page past its last token: decode tiles never let
+ * them reach an output, whatever they hold; tensor-core tiles copy whole pages
+ * and need them to hold finite values (a NaN there can make the request's rows
+ * NaN).
+ *
  * Every row of o/lse that the plan covers is written; a row that sees no key
  * gets o = 0, lse = -inf.  Asynchronous on `stream`.  A decode-tile launch is
  * made a programmatic dependent of the previous kernel on the stream: its CTAs
  * may set up shared memory while that kernel drains, and read no global memory
  * before it has completed.  Capturable in a CUDA
  * graph, and a captured launch stays valid for later plans of the same
- * workspace that keep the same path and tile (fi_plan_info header[1..3]); on
- * the tensor-core path they must also keep the total query count (the launch
- * holds a TMA descriptor of q whose extent is the plan's total_q).
+ * workspace that keep the same path and tile (fi_plan_info header[1..3]) and
+ * page size; on the tensor-core path they must also keep the total query count
+ * (the launch holds a TMA descriptor of q whose extent is the plan's total_q).
+ * Launches over pages of 8 or more tokens hold TMA descriptors of k_pages and
+ * v_pages built from the call's pointers, num_pages and page size.
  * Calls that share a workspace must not overlap on the GPU.
  * Errors: NO_PLAN, INVALID_ARG (null pointers, q / k_pages / v_pages not
  * 16-byte aligned, page id >= num_pages), CUDA.
