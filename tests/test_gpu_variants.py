@@ -48,6 +48,8 @@ CASES = [
     (32, 8, 16, (1, 1), (1, 900), True, 64, 0.0, "HND", 5),        # decode g=4, window, split rows
     (64, 8, 16, (1, 1), (1, 900), True, 200, 30.0, "NHD", 0),      # decode g=8: window + cap + NHD
     (8, 2, 1, (1, 1), (1, 500), False, -1, 5.0, "NHD", 3),         # decode, page 1, cap, NHD
+    (32, 8, 128, (1, 1), (1, 1500), False, -1, 0.0, "NHD", 0),     # decode, NHD page 128: boxes inside a page
+    (16, 16, 8, (1, 2), (2, 600), True, -1, 0.0, "NHD", 4),        # decode g = 1, 16 KV heads, NHD page 8
     (8, 8, 5, (1, 2), (2, 300), True, 17, 10.0, "HND", 2),         # bulk loader, CUDA-core consumer
     (16, 4, 12, (1, 1), (1, 700), True, 100, 0.0, "HND", 4),       # bulk loader, R = 4, window
     (8, 2, 16, (20, 200), (200, 1500), True, 128, 0.0, "HND", 4),  # tensor cores, window, split rows
