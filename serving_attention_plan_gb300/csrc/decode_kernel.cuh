@@ -650,6 +650,135 @@ __device__ __forceinline__ void decode_deferred_merges(const DecodeParams& p, SM
   }
 }
 
+// Composable plans, tensor-core consumer kernel, after every warp of the CTA is done with its
+// queue (a CTA barrier precedes this): all warps merge the deferred units' rows with the shared
+// part's states.  A warp takes two (unit, row) tasks at a time.  Everything that does not depend on
+// the shared part's launch -- the unit's fields, its shared-slot list, the row's own state -- is
+// loaded before the wait for that launch, so that only the slots' LSEs and states are read after
+// it, the two tasks' loads in flight together.  Lane e holds shared entry e of a task (entry lists
+// longer than kMergeFast go through merge_ext).  Same sums as merge_ext, in the same order.
+constexpr int kMergeFast = 8;
+template <int R, class SM>
+__device__ __forceinline__ void decode_deferred_merges_cta(const DecodeParams& p, SM& sm, int warp, int nwarps) {
+  const int nd = sm.n_deferred;  // final: every warp passed the barrier before this call
+  if (nd == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int ntask = nd * R;
+  bool waited = false;
+  for (int t0 = warp; t0 < ntask; t0 += 2 * nwarps) {
+    int unit[2], rr[2], ec[2], ef[2];
+    size_t orow[2], srow[2];
+    bool live[2], ent[2];
+    float4 O[2];
+    float lse_own[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const int t = t0 + b * nwarps;
+      live[b] = false;
+      ent[b] = false;
+      ec[b] = 0;
+      ef[b] = 0;
+      srow[b] = 0;
+      orow[b] = 0;
+      unit[b] = 0;
+      rr[b] = 0;
+      O[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+      lse_own[b] = -INFINITY;
+      if (t >= ntask) continue;
+      unit[b] = sm.deferred[t / R];
+      rr[b] = t % R;
+      const int* uf = p.units + unit[b] * kUnitFields;
+      const int q_len = __ldg(uf + U_Q_LEN);
+      if (rr[b] >= q_len * p.group) continue;
+      live[b] = true;
+      const int q_start = __ldg(uf + U_Q_START), kv_head = __ldg(uf + U_KV_HEAD);
+      orow[b] = (size_t)(q_start + rr[b] / p.group) * p.hqo + kv_head * p.group + rr[b] % p.group;
+      ef[b] = __ldg(uf + 5);
+      ec[b] = __ldg(uf + 6);
+      const size_t drow = (size_t)unit[b] * kDecodeMaxRows + rr[b];
+      O[b] = __ldcg(reinterpret_cast<const float4*>(p.def_o + drow * kHeadDim) + lane);
+      lse_own[b] = __ldcg(p.def_lse + drow);
+      if (ec[b] <= kMergeFast && lane < ec[b]) {
+        const int2 x = __ldg(p.ext + ef[b] + lane);
+        const int row = (x.y & 0xFFFF) - kExtRowBias + rr[b];
+        if (row >= 0 && row < (x.y >> 16)) {
+          srow[b] = (size_t)x.x * p.slot_rows + row;
+          ent[b] = true;
+        }
+      }
+    }
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the shared part's launch has completed
+      waited = true;
+    }
+    // the slots' LSEs of both tasks, then their weights
+    float le[2], wgt[2], M[2], L[2];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) le[b] = ent[b] ? __ldcg(p.part_lse + srow[b]) : -INFINITY;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      float m = le[b];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      M[b] = fmaxf(m, lse_own[b]);
+      wgt[b] = (le[b] == -INFINITY || M[b] == -INFINITY) ? 0.f : fast_exp2(le[b] - M[b]);
+      float l = wgt[b];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      const float w0 = (lse_own[b] == -INFINITY || M[b] == -INFINITY) ? 0.f : fast_exp2(lse_own[b] - M[b]);
+      L[b] = l + w0;
+      O[b] = make_float4(w0 * O[b].x, w0 * O[b].y, w0 * O[b].z, w0 * O[b].w);
+    }
+    // the slots' states: entry e of task b from lane e's slot row, both tasks' loads issued first
+    float4 a[2][kMergeFast];
+    float wj[2][kMergeFast];
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+#pragma unroll
+      for (int e = 0; e < kMergeFast; ++e) {
+        wj[b][e] = __shfl_sync(0xffffffffu, wgt[b], e);
+        const unsigned long long sr = __shfl_sync(0xffffffffu, (unsigned long long)srow[b], e);
+        a[b][e] = (ec[b] <= kMergeFast && e < ec[b] && wj[b][e] != 0.f)
+                      ? __ldcg(reinterpret_cast<const float4*>(p.part_o + sr * kHeadDim) + lane)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      if (!live[b]) continue;
+      float4 acc = O[b];
+      float lse2;
+      if (ec[b] <= kMergeFast) {
+#pragma unroll
+        for (int e = 0; e < kMergeFast; ++e) {
+          acc.x += wj[b][e] * a[b][e].x;
+          acc.y += wj[b][e] * a[b][e].y;
+          acc.z += wj[b][e] * a[b][e].z;
+          acc.w += wj[b][e] * a[b][e].w;
+        }
+        if (M[b] == -INFINITY) {
+          acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          lse2 = -INFINITY;
+        } else {
+          const float inv = 1.f / L[b];
+          acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          lse2 = M[b] + fast_log2(L[b]);
+        }
+      } else {  // a long entry list: the general merge
+        const size_t drow = (size_t)unit[b] * kDecodeMaxRows + rr[b];
+        acc = __ldcg(reinterpret_cast<const float4*>(p.def_o + drow * kHeadDim) + lane);
+        lse2 = lse_own[b];
+        merge_ext(p, unit[b], rr[b], lane, acc, lse2);
+      }
+      uint2 packed;
+      packed.x = f2_to_bf16x2(acc.x, acc.y);
+      packed.y = f2_to_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(p.o + orow[b] * kHeadDim + 4 * lane) = packed;
+      if (lane == 0) p.lse[orow[b]] = lse2 * kLn2;
+    }
+  }
+}
+
 template <int R, int NW, int S, bool kVar, bool kMs>
 __device__ __forceinline__ void decode_consumer(const DecodeParams& p, DecodeSmem<R, NW, S, kMs>& sm, int begin, int end,
                                                 int w) {
@@ -1073,7 +1202,7 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, Decod
     named_bar_sync(1, NW * 32);
     decode_finish_item<R, NW, S>(p, sm, ctid, q_start, kv_head, rows_valid, slot_out);
   }
-  if (p.ext) decode_deferred_merges<R, NW, S>(p, sm, w);
+  // composable plans: the deferred merges follow in decode_body, by every warp of the CTA
 }
 
 // kMma selects the tensor-core consumer (LDGSTS loader only, whose copies it swizzles).
@@ -1152,6 +1281,15 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
   } else {
     constexpr int kNhdStride = (kFlags & kDecodeNhd) ? kHeadDim << ((kFlags >> kDecodeNhdHeadsShift) & 7) : 0;
     decode_copier_warp<R, NW, S, kCopiers, kMma, kNhdStride>(p, sm, begin, end, warp - 1);
+  }
+  if constexpr (kMma) {
+    // composable plans: once every warp is done (the consumers' last item merge ended with their
+    // barrier, so the deferred list is final), all warps merge the deferred rows with the shared
+    // part's states.  Every role of this kernel returns here, aborted or not.
+    if (p.ext != nullptr) {
+      __syncthreads();
+      decode_deferred_merges_cta<R>(p, sm, warp, int(blockDim.x >> 5));
+    }
   }
 }
 
