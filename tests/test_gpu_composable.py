@@ -194,6 +194,9 @@ COMPOSABLE_CASES = [
     (7, 8, 4, 8, 2, (2, 200), 2, (1, 400), True, 6),            # 2 query tokens (4 rows), causal own part
     (33, 64, 8, 32, 1, (0, 500), 4, (0, 3000), False, 24),      # g = 8, page 32, empty prefixes possible
     (5, 16, 16, 16, 4, (4, 100), 1, (50, 300), True, 10),       # g = 1, 4 tokens per request
+    (8, 8, 2, 16, 1, (1, 50), 1, (20000, 20000), False, 0),     # 74 shared slots a row: lists of more than 32
+    (12, 8, 2, 16, 1, (1, 200), 1, (3000, 4000), False, 0),     # 13 shared slots a row
+    (40, 32, 8, 16, 1, (1, 200), 2, (100, 600), False, 4),      # ~107 deferred units a CTA: list overflows
 ]
 
 
