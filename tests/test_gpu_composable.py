@@ -196,7 +196,7 @@ COMPOSABLE_CASES = [
     (5, 16, 16, 16, 4, (4, 100), 1, (50, 300), True, 10),       # g = 1, 4 tokens per request
     (8, 8, 2, 16, 1, (1, 50), 1, (20000, 20000), False, 0),     # 74 shared slots a row: lists of more than 32
     (12, 8, 2, 16, 1, (1, 200), 1, (3000, 4000), False, 0),     # 13 shared slots a row
-    (40, 32, 8, 16, 1, (1, 200), 2, (100, 600), False, 4),      # ~107 deferred units a CTA: list overflows
+    (80, 2, 1, 16, 1, (1, 60), 1, (100, 300), False, 2),        # 80 deferred units in one CTA: 16 merged at once
 ]
 
 
