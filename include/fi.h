@@ -245,10 +245,8 @@ int fi_plan_composable(fi_workspace* ws, const int32_t* shared_qo_indptr, const 
  *   o          DEVICE bf16 [total_q, num_qo_heads, 128]   (written)
  *   lse        DEVICE float32 [total_q, num_qo_heads]     (written)
  *
- * Slots of a request's last page past its last token: decode tiles never let
- * them reach an output, whatever they hold; tensor-core tiles copy whole pages
- * and need them to hold finite values (a NaN there can make the request's rows
- * NaN).
+ * Slots of a request's last page past its last token may hold anything (NaN
+ * included): no kernel lets them reach an output.
  *
  * Every row of o/lse that the plan covers is written; a row that sees no key
  * gets o = 0, lse = -inf.  Asynchronous on `stream`.  A decode-tile launch is

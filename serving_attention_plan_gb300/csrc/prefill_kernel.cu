@@ -414,6 +414,23 @@ __device__ void pv_issuer(const PrefillParams& p, PrefillSmem& sm, uint32_t tmem
     for (int t = 0; t < n_tiles; ++t, ++tt) {
       const int vs = tt % kKvStages;
       if (!mbar_wait(&v_in[vs], (tt / kKvStages) & 1, p.err, &sm.abort)) return;
+      if (t == n_tiles - 1) {
+        // The item's last page may hold slots past its last key: the page box brought them in, and
+        // a NaN there would survive its zero weight in P.V.  Clear those V rows (the rest of the
+        // tile past that page came in as zeros).
+        const int base = it.kv_lo + t * kTile;
+        const int r0 = it.kv_hi - base;
+        const int r1 = min(kTile, (it.kv_hi + p.page_size - 1) / p.page_size * p.page_size - base);
+        if (r0 < r1) {
+          uint8_t* st = sm.v[vs];
+          for (int r = r0; r < r1; ++r) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              *reinterpret_cast<uint4*>(st + (c >> 3) * kHalfBytes + r * 128 + (c & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();  // the MMAs read the stage through the async proxy
+        }
+      }
       for (int sub = 0; sub < 2 && 2 * t + sub < n_sub; ++sub, ++uu) {
         const int b = uu & 1;
         const bool first = t == 0 && sub == 0;

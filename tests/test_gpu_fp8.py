@@ -98,6 +98,26 @@ def test_fp8_decode_ignores_codes_past_the_last_token():
     assert_close(o, lse, ro, rl)
 
 
+def test_fp8_prefill_ignores_codes_past_the_last_token():
+    """Tensor-core tiles over e4m3 pages: NaN codes (0x7f) in the unused slots of each request's last page
+    must not reach any output."""
+    b = W.random_small_batch(5410, batch=5, num_qo_heads=8, num_kv_heads=2, page_size=16, causal=True,
+                             q_len_range=(20, 150), kv_len_range=(150, 700), extra_pages=3)
+    b8 = W.as_e4m3(b, 0.5, 1.0)
+    k, v = b8.k_pages.copy(), b8.v_pages.copy()
+    for i in range(b8.batch_size):
+        lo, hi = int(b8.kv_indptr[i]), int(b8.kv_indptr[i + 1])
+        if hi > lo:
+            last, n = int(b8.kv_indices[hi - 1]), int(b8.last_page_len[i])
+            k[last, :, n:, :] = 0x7F
+            v[last, :, n:, :] = 0x7F
+    o, lse, ws = run_fp8(dataclasses.replace(b8, k_pages=k, v_pages=v), 0.5, 1.0, num_sms=3)
+    assert ws.info()[1] == 1
+    ro, rl = A.batch_attention(b8, k_scale=0.5, v_scale=1.0)
+    assert np.isfinite(o).all()
+    assert_close(o, lse, ro, rl)
+
+
 TC_CASES = [
     # (hq, hk, page, q range, kv range, causal, SM budget, k_scale, v_scale, window, cap, layout):
     # requests of more than 8 rows, so the plan takes tensor-core tiles

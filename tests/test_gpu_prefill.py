@@ -137,3 +137,25 @@ def test_graph_replay_with_split_rows():
         assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
         ro, rl = A.batch_attention(b)
         assert_close(outs[0][0], outs[0][1], ro, rl)
+
+
+def test_prefill_ignores_values_past_the_last_token():
+    """Tensor-core tiles copy whole pages: NaN values in the unused slots of each request's last page
+    must not reach any output (the V rows past the last key are cleared before P.V)."""
+    import dataclasses
+    for ps in (16, 64):
+        b = W.random_small_batch(2600 + ps, batch=5, num_qo_heads=8, num_kv_heads=2, page_size=ps, causal=True,
+                                 q_len_range=(20, 150), kv_len_range=(150, 700), extra_pages=3, scale=0.5)
+        k, v = b.k_pages.copy(), b.v_pages.copy()  # HND [pages, H_kv, page, D] bf16 bits
+        for i in range(b.batch_size):
+            lo, hi = int(b.kv_indptr[i]), int(b.kv_indptr[i + 1])
+            if hi > lo:
+                last, n = int(b.kv_indices[hi - 1]), int(b.last_page_len[i])
+                k[last, :, n:, :] = 0x7FC0
+                v[last, :, n:, :] = 0x7FC0
+        o, lse, ws = run_library(dataclasses.replace(b, k_pages=k, v_pages=v), num_sms=3)
+        assert ws.info()[1] == 1
+        ro, rl = A.batch_attention(b)
+        assert np.isfinite(o).all()
+        assert_close(o, lse, ro, rl)
+
