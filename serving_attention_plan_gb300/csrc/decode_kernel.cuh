@@ -658,21 +658,24 @@ __device__ __forceinline__ void decode_deferred_merges(const DecodeParams& p, SM
 // it, the two tasks' loads in flight together.  Lane e holds shared entry e of a task (entry lists
 // longer than kMergeFast go through merge_ext).  Same sums as merge_ext, in the same order.
 constexpr int kMergeFast = 8;
+constexpr int kMergeTasks = 3;  // (unit, row) tasks a warp merges together
+// Not inlined: its register needs then leave the allocation of the decode loop alone (inlined, the
+// kernel measured 0.2 % slower on plain decode batches, which never call it).
 template <int R, class SM>
-__device__ __forceinline__ void decode_deferred_merges_cta(const DecodeParams& p, SM& sm, int warp, int nwarps) {
+__device__ __noinline__ void decode_deferred_merges_cta(const DecodeParams& p, SM& sm, int warp, int nwarps) {
   const int nd = sm.n_deferred;  // final: every warp passed the barrier before this call
   if (nd == 0) return;
   const int lane = threadIdx.x & 31;
   const int ntask = nd * R;
   bool waited = false;
-  for (int t0 = warp; t0 < ntask; t0 += 2 * nwarps) {
-    int unit[2], rr[2], ec[2], ef[2];
-    size_t orow[2], srow[2];
-    bool live[2], ent[2];
-    float4 O[2];
-    float lse_own[2];
+  for (int t0 = warp; t0 < ntask; t0 += kMergeTasks * nwarps) {
+    int unit[kMergeTasks], rr[kMergeTasks], ec[kMergeTasks], ef[kMergeTasks];
+    size_t orow[kMergeTasks], srow[kMergeTasks];
+    bool live[kMergeTasks], ent[kMergeTasks];
+    float4 O[kMergeTasks];
+    float lse_own[kMergeTasks];
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMergeTasks; ++b) {
       const int t = t0 + b * nwarps;
       live[b] = false;
       ent[b] = false;
@@ -712,11 +715,11 @@ __device__ __forceinline__ void decode_deferred_merges_cta(const DecodeParams& p
       waited = true;
     }
     // the slots' LSEs of both tasks, then their weights
-    float le[2], wgt[2], M[2], L[2];
+    float le[kMergeTasks], wgt[kMergeTasks], M[kMergeTasks], L[kMergeTasks];
 #pragma unroll
-    for (int b = 0; b < 2; ++b) le[b] = ent[b] ? __ldcg(p.part_lse + srow[b]) : -INFINITY;
+    for (int b = 0; b < kMergeTasks; ++b) le[b] = ent[b] ? __ldcg(p.part_lse + srow[b]) : -INFINITY;
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMergeTasks; ++b) {
       float m = le[b];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -730,10 +733,10 @@ __device__ __forceinline__ void decode_deferred_merges_cta(const DecodeParams& p
       O[b] = make_float4(w0 * O[b].x, w0 * O[b].y, w0 * O[b].z, w0 * O[b].w);
     }
     // the slots' states: entry e of task b from lane e's slot row, both tasks' loads issued first
-    float4 a[2][kMergeFast];
-    float wj[2][kMergeFast];
+    float4 a[kMergeTasks][kMergeFast];
+    float wj[kMergeTasks][kMergeFast];
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMergeTasks; ++b) {
 #pragma unroll
       for (int e = 0; e < kMergeFast; ++e) {
         wj[b][e] = __shfl_sync(0xffffffffu, wgt[b], e);
@@ -744,7 +747,7 @@ __device__ __forceinline__ void decode_deferred_merges_cta(const DecodeParams& p
       }
     }
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMergeTasks; ++b) {
       if (!live[b]) continue;
       float4 acc = O[b];
       float lse2;
