@@ -49,8 +49,9 @@ int launch_fp8_rows(int grid, const DecodeParams& p, cudaStream_t stream, bool p
   CUtensorMap tm_k{}, tm_v{};
   if (p.page_size < 8) return launch_fp8_as<R, kNhd, false>(grid, p, tm_k, tm_v, stream, pdl);
   const int hkv = int(p.page_stride / (int64_t(p.page_size) * kHeadDim));
-  if (!make_decode_map_e4m3(&tm_k, p.k, hkv, p.page_size, p.num_pages, kNhd) ||
-      !make_decode_map_e4m3(&tm_v, p.v, hkv, p.page_size, p.num_pages, kNhd))
+  const int box_rows = p.page_size < kFp8StageTokens ? p.page_size : kFp8StageTokens;  // as the copier's boxes
+  if (!make_decode_map_e4m3(&tm_k, p.k, hkv, p.page_size, p.num_pages, kNhd, box_rows) ||
+      !make_decode_map_e4m3(&tm_v, p.v, hkv, p.page_size, p.num_pages, kNhd, box_rows))
     return FI_ERR_INVALID_ARG;
   return launch_fp8_as<R, kNhd, true>(grid, p, tm_k, tm_v, stream, pdl);
 }

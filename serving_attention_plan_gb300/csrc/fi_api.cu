@@ -83,8 +83,9 @@ int launch_decode(int grid, const fi::DecodeParams& p, cudaStream_t stream, bool
   if (tma && p.page_shift >= 0 && p.page_size >= 8) {
     CUtensorMap tm_k, tm_v;
     const int hkv = int(p.page_stride / (int64_t(p.page_size) * fi::kHeadDim));
-    if (!fi::make_decode_map_bf16(&tm_k, p.k, hkv, p.page_size, p.num_pages) ||
-        !fi::make_decode_map_bf16(&tm_v, p.v, hkv, p.page_size, p.num_pages))
+    const int box_rows = p.page_size < fi::kStageTokens ? p.page_size : fi::kStageTokens;  // as the copier's boxes
+    if (!fi::make_decode_map_bf16(&tm_k, p.k, hkv, p.page_size, p.num_pages, box_rows) ||
+        !fi::make_decode_map_bf16(&tm_v, p.v, hkv, p.page_size, p.num_pages, box_rows))
       return FI_ERR_INVALID_ARG;
     return var ? fi::launch_decode_tma_as<R, kV>(grid, p, tm_k, tm_v, stream, pdl)
                : fi::launch_decode_tma_as<R, 0>(grid, p, tm_k, tm_v, stream, pdl);

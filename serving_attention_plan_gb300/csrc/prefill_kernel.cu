@@ -952,9 +952,10 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, uint64_t page_size, uint64_
 
 }  // namespace
 
-bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, bool nhd) {
-  if (encode_fn() == nullptr) return false;
-  const cuuint32_t rows = cuuint32_t(page_size < 64 ? page_size : 64);
+bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, bool nhd,
+                          int box_rows) {
+  if (encode_fn() == nullptr || box_rows < 1 || box_rows > page_size) return false;
+  const cuuint32_t rows = cuuint32_t(box_rows);
   const cuuint64_t row = uint64_t(kHeadDim);  // one byte a code
   if (nhd) {
     const cuuint64_t dims[4] = {row, uint64_t(hkv), uint64_t(page_size), uint64_t(num_pages)};
@@ -974,11 +975,11 @@ bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_si
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_decode_map_bf16(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages) {
-  if (encode_fn() == nullptr) return false;
+bool make_decode_map_bf16(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, int box_rows) {
+  if (encode_fn() == nullptr || box_rows < 1 || box_rows > page_size) return false;
   const uint64_t row = uint64_t(kHeadDim) * 2;
   return make_map(m, base, uint64_t(page_size), uint64_t(num_pages) * uint64_t(hkv), row, row * page_size,
-                  uint32_t(page_size < 32 ? page_size : 32), 1u);
+                  uint32_t(box_rows), 1u);
 }
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t stream) {

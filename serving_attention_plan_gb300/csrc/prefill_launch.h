@@ -49,16 +49,18 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // Records the text of a failed CUDA call for fi_last_error_message; returns FI_ERR_CUDA.
 int record_cuda_error(cudaError_t e, const char* what);
 
-// Tensor map of e4m3 K or V pages for the FP8 decode kernel's TMA copier: one box is
-// min(page_size, 64) rows of 128 codes of one page and KV head, 128-byte swizzled.  HND pages
-// [pages][H_kv][page_size][128] map as (code, token in page, page * H_kv + head), NHD pages
-// [pages][page_size][H_kv][128] as (code, head, token in page, page).  Returns false if the driver's
-// encoder is missing or refuses the map.
-bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, bool nhd);
+// Tensor map of e4m3 K or V pages for the FP8 decode kernel's TMA copier: one box is box_rows
+// (the copier's min(page_size, stage tokens)) rows of 128 codes of one page and KV head, 128-byte
+// swizzled.  HND pages [pages][H_kv][page_size][128] map as (code, token in page, page * H_kv +
+// head), NHD pages [pages][page_size][H_kv][128] as (code, head, token in page, page).  Returns
+// false if the driver's encoder is missing or refuses the map.
+bool make_decode_map_e4m3(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, bool nhd,
+                          int box_rows);
 
 // Tensor map of bf16 HND K or V pages [pages][H_kv][page_size][128] for the decode kernel's TMA
-// copier: (dim, token in page, page * H_kv + head), one box 64 dims x min(page_size, 32) tokens,
-// 128-byte swizzled.  Returns false if the driver's encoder is missing or refuses the map.
-bool make_decode_map_bf16(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages);
+// copier: (dim, token in page, page * H_kv + head), one box 64 dims x box_rows tokens (the copier's
+// min(page_size, stage tokens)), 128-byte swizzled.  Returns false if the driver's encoder is
+// missing or refuses the map.
+bool make_decode_map_bf16(CUtensorMap* m, const void* base, int hkv, int page_size, int num_pages, int box_rows);
 
 }  // namespace fi
