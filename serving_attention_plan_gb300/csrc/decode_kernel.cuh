@@ -652,11 +652,11 @@ __device__ __forceinline__ void decode_deferred_merges(const DecodeParams& p, SM
 
 // Composable plans, tensor-core consumer kernel, after every warp of the CTA is done with its
 // queue (a CTA barrier precedes this): all warps merge the deferred units' rows with the shared
-// part's states.  A warp takes two (unit, row) tasks at a time.  Everything that does not depend on
-// the shared part's launch -- the unit's fields, its shared-slot list, the row's own state -- is
-// loaded before the wait for that launch, so that only the slots' LSEs and states are read after
-// it, the two tasks' loads in flight together.  Lane e holds shared entry e of a task (entry lists
-// longer than kMergeFast go through merge_ext).  Same sums as merge_ext, in the same order.
+// part's states.  A warp takes kMergeTasks (unit, row) tasks at a time.  Everything that does not
+// depend on the shared part's launch -- the unit's fields, its shared-slot list, the row's own
+// state -- is loaded before the wait for that launch, so that only the slots' LSEs and states are
+// read after it, the tasks' loads in flight together.  Lane e holds shared entry e of a task (entry
+// lists longer than kMergeFast go through merge_ext).  Same sums as merge_ext, in the same order.
 constexpr int kMergeFast = 8;
 constexpr int kMergeTasks = 3;  // (unit, row) tasks a warp merges together
 // Not inlined: its register needs then leave the allocation of the decode loop alone (inlined, the
@@ -714,7 +714,7 @@ __device__ __noinline__ void decode_deferred_merges_cta(const DecodeParams& p, S
       asm volatile("griddepcontrol.wait;" ::: "memory");  // the shared part's launch has completed
       waited = true;
     }
-    // the slots' LSEs of both tasks, then their weights
+    // the slots' LSEs of the tasks, then their weights
     float le[kMergeTasks], wgt[kMergeTasks], M[kMergeTasks], L[kMergeTasks];
 #pragma unroll
     for (int b = 0; b < kMergeTasks; ++b) le[b] = ent[b] ? __ldcg(p.part_lse + srow[b]) : -INFINITY;
@@ -732,7 +732,7 @@ __device__ __noinline__ void decode_deferred_merges_cta(const DecodeParams& p, S
       L[b] = l + w0;
       O[b] = make_float4(w0 * O[b].x, w0 * O[b].y, w0 * O[b].z, w0 * O[b].w);
     }
-    // the slots' states: entry e of task b from lane e's slot row, both tasks' loads issued first
+    // the slots' states: entry e of task b from lane e's slot row, every task's loads issued first
     float4 a[kMergeTasks][kMergeFast];
     float wj[kMergeTasks][kMergeFast];
 #pragma unroll
