@@ -271,3 +271,31 @@ def test_shared_prefix_composable_plan(lib):
     n_chunks = a.units[0]["n_chunks"]
     assert all(u["ext_count"] == n_chunks for u in b.units)   # each suffix unit merges every prefix chunk of its head
     assert len(ext) == len(b.units) * n_chunks
+
+
+@pytest.mark.parametrize("case", [
+    # (n_req, hq, hk, page, own range, prefix length, SM budget)
+    (8, 8, 2, 16, (1, 50), 20000, 152),   # one long prefix over many CTAs: 74 shared slots a row
+    (80, 2, 1, 16, (1, 60), 300, 2),      # one decode CTA holding 80 units with shared states
+])
+def test_composable_plan_long_slot_lists_and_crowded_ctas(lib, case):
+    """Composable plans at the ends the kernels treat specially: rows that merge dozens of shared
+    slots, and a decode CTA with more units to merge than its deferred list holds.  C++ ==
+    restatement, bit for bit, and the slot lists have the lengths those cases rely on."""
+    n_req, hq, hk, ps, own, plen, n_cta = case
+    rng = np.random.default_rng(1234 + n_req)
+    own_lens = rng.integers(own[0], own[1] + 1, size=n_req)
+    qo = np.arange(n_req + 1)
+    kv = np.concatenate([[0], np.cumsum((own_lens + ps - 1) // ps)])
+    last = own_lens - ((own_lens + ps - 1) // ps - 1) * ps
+    n_p = (plen + ps - 1) // ps
+    shared = (np.array([0, n_req]), np.array([0, n_p]), np.array([plen - (n_p - 1) * ps]))
+    unique = (qo, kv, last)
+    got = B.plan_composable_compute(shared, unique, hq, hk, ps, False, n_cta)
+    a, b, ext = P.plan_composable(shared, unique, hq, hk, ps, False, n_cta)
+    assert np.array_equal(got, P.serialize_composable(a, b, ext))
+    counts = [u["ext_count"] for u in b.units]
+    if plen > 10000:
+        assert max(counts) > 32          # longer than one warp's lanes
+    else:
+        assert len(b.queues) == 1 and len(b.units) > 64
